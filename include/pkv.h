@@ -1,0 +1,238 @@
+/*
+ * pkv.h -- C ABI of libpkv: causal attention over a paged, prefix-cached KV
+ * cache on GB300 (sm_103a).
+ *
+ * The operations and where they are described:
+ *
+ *  - pkv_write_slots: the KV append ("KV 写入") that stores this step's new
+ *    K/V rows at the physical slots the scheduler assigned them.  Page "vLLM
+ *    Agentic 推理｜面向 Agent 负载的推理优化", section 5.2 (每层两个 Kernel,
+ *    the KV write inside K1).
+ *  - pkv_attention_varlen: one step of attention for a mixed batch of
+ *    incremental-prefill chunks (l_incr new tokens attending to l_hist cached
+ *    tokens plus themselves) and decodes (l_incr = 1).  Page "AMPD：PD 分离遇上
+ *    多轮推理，incremental prefill 到底该在哪跑", sections 1 and 3; GQA head
+ *    sharing, page "vLLM Agentic 推理", section 4.3.1; split attention with a
+ *    log-sum-exp combine of partial results, same page, sections 4.3.3 (step
+ *    4) and 5.2 (Split Attention + Combine).
+ *  - Block tables: request i owns cdiv(seq_len, block_size) blocks, listed in
+ *    row i of block_tables; blocks may be shared by several requests with a
+ *    common prefix.  Page "vLLM/V1 推理调度器", section 源码片段
+ *    (KVCacheManager.allocate_slots and the per-request block-id record).
+ *
+ * Conventions shared by every call
+ *  - head_dim is 128.  Query heads h = 0..Hq-1 read KV head h / G, where
+ *    G = Hq / Hkv.
+ *  - A KV pool is [num_blocks][Hkv][block_size][128] elements: bf16, or E4M3
+ *    codes (OCP FP8, "FN" variant) with one fp32 scale per (block, KV head)
+ *    in a [num_blocks][Hkv] array; an element's value is e4m3(code) * scale.
+ *    Logical position p of request i lives in block block_tables[i][p / bs]
+ *    at row p % bs; its slot is block * bs + p % bs.
+ *  - Query token t (0-based) of request i, which has q_i new tokens and
+ *    seq_len L_i context tokens including them, sits at position
+ *    L_i - q_i + t and sees keys 0 .. L_i - q_i + t.
+ *  - Device pointers are CUDA device addresses on the handle's device; host
+ *    pointers are ordinary host memory.  The caller owns every buffer and the
+ *    stream; the library owns only the handle and its workspace.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Buffers must stay valid until that stream's work
+ *    completes.  Neither hot call allocates memory.  pkv_attention_varlen
+ *    plans on the host and uploads the plan from one of two pinned staging
+ *    buffers; before refilling a buffer it waits for that buffer's upload
+ *    from two calls earlier, and for nothing else on the device.
+ *  - Argument errors are detected on the host before anything is enqueued and
+ *    return PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED with a message in
+ *    pkv_last_error().  Launch failures return PKV_ERR_CUDA.  In validate
+ *    mode (PKV_FLAG_VALIDATE) the kernels also check block ids and slots on
+ *    the device, skip anything out of range and record it; the record is read
+ *    by pkv_check_device_errors().  No kernel ever traps.
+ *  - One handle is used from one host thread at a time.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pkv_handle pkv_handle;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* a pointer, size or metadata value is wrong */
+    PKV_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, ...) */
+    PKV_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    PKV_ERR_OUT_OF_MEMORY = 4, /* pkv_create could not allocate its workspace */
+    PKV_ERR_DEVICE_CHECK = 5,  /* validate mode found a bad block id or slot */
+    PKV_ERR_TIMEOUT = 6,       /* a device-side wait gave up (never expected) */
+    PKV_ERR_WORKSPACE = 7      /* the step needs more workspace than created */
+} pkv_status;
+
+typedef enum {
+    PKV_KV_BF16 = 0,
+    PKV_KV_FP8_E4M3 = 1
+} pkv_kv_dtype;
+
+enum {
+    PKV_FLAG_VALIDATE = 1u,    /* device-side checks of block ids and slots */
+    PKV_FLAG_TIMING = 2u       /* record CUDA events around every kernel */
+};
+
+/* Fixed shape of a KV cache and the largest step a handle serves. */
+typedef struct {
+    int32_t num_q_heads;       /* Hq, a multiple of num_kv_heads */
+    int32_t num_kv_heads;      /* Hkv */
+    int32_t head_dim;          /* must be 128 */
+    int32_t block_size;        /* tokens per block: 16, 32, 64, 128 or 256 */
+    int32_t kv_dtype;          /* pkv_kv_dtype */
+    float softmax_scale;       /* scores are softmax_scale * q . k */
+    int64_t num_blocks;        /* blocks in each pool */
+    int32_t max_num_seqs;      /* largest batch (requests) per step */
+    int32_t max_num_tokens;    /* largest number of query tokens per step */
+    uint32_t flags;            /* PKV_FLAG_* */
+} pkv_config;
+
+/*
+ * Create a handle on CUDA device `device` and allocate its workspace (work
+ * list, split partials, combine tickets, error word: a few tens of MB,
+ * sized from max_num_seqs and max_num_tokens).  *out receives the handle, or
+ * NULL on failure.  Errors: PKV_ERR_INVALID_ARG (NULL pointers, bad config),
+ * PKV_ERR_UNSUPPORTED (head_dim or block_size not handled), PKV_ERR_CUDA (no
+ * such device), PKV_ERR_OUT_OF_MEMORY.
+ */
+pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out);
+
+/*
+ * KV append.  For each token t < num_tokens with slot_mapping[t] >= 0, store
+ * row t of k_new and v_new (each [num_tokens][Hkv][128] bf16, device) at that
+ * slot of k_cache / v_cache for every KV head.  bf16 pools receive the bits
+ * unchanged.  FP8 pools receive E4M3(x / scale[block][head]): the quotient is
+ * one correctly rounded fp32 division, then rounded to nearest even and
+ * saturated to +-448; k_scale / v_scale ([num_blocks][Hkv] fp32, device) are
+ * read, never written, and must be finite and > 0 for the blocks written.
+ * slot_mapping is int64 on the device; negative entries are padding.
+ * Entries must be distinct.  A slot past the pool is an argument error the
+ * host cannot see: in validate mode it is skipped and reported, otherwise it
+ * is undefined behaviour.
+ */
+pkv_status pkv_write_slots(pkv_handle *h, const void *k_new, const void *v_new,
+                           const int64_t *slot_mapping, int32_t num_tokens,
+                           void *k_cache, void *v_cache, const float *k_scale,
+                           const float *v_scale, void *stream);
+
+/*
+ * Attention for one step.
+ *  q                [num_tokens][Hq][128] bf16, device; the tokens of request
+ *                   i are rows query_start_loc[i] .. query_start_loc[i+1]-1.
+ *  k_cache/v_cache  pools as above (FP8: with k_scale / v_scale, else NULL).
+ *  query_start_loc  [num_seqs + 1] int32, device, and its host mirror
+ *                   query_start_loc_host (identical contents): 0 = first,
+ *                   non-decreasing, last = num_tokens.
+ *  seq_lens         [num_seqs] int32, device, and host mirror seq_lens_host:
+ *                   L_i >= q_i >= 0, including this step's new tokens.
+ *  block_tables     [num_seqs][block_table_stride] int32, device; entries
+ *                   0 .. cdiv(L_i, block_size) - 1 of row i must be block ids
+ *                   < num_blocks; later entries are never read.
+ *  out              [num_tokens][Hq][128] bf16, device (written).
+ *  lse              NULL, or [num_tokens][Hq] fp32, device: natural-log
+ *                   log-sum-exp of each row's scaled scores (written).
+ * The work is planned on the host from the host mirrors (so they must match
+ * the device copies; validate mode checks that), uploaded asynchronously and
+ * executed by the kernels.  The new tokens' K/V must already be in the pools
+ * (call pkv_write_slots first on the same stream).  A step that needs more
+ * workspace than the handle was created for returns PKV_ERR_WORKSPACE.
+ */
+pkv_status pkv_attention_varlen(pkv_handle *h, const void *q,
+                                const void *k_cache, const void *v_cache,
+                                const float *k_scale, const float *v_scale,
+                                const int32_t *query_start_loc,
+                                const int32_t *seq_lens,
+                                const int32_t *block_tables,
+                                int32_t block_table_stride,
+                                const int32_t *query_start_loc_host,
+                                const int32_t *seq_lens_host, int32_t num_seqs,
+                                int32_t num_tokens, void *out, float *lse,
+                                void *stream);
+
+/*
+ * Wait for the handle's device (cudaDeviceSynchronize) and read the device
+ * error word, clearing it.  Returns PKV_OK, PKV_ERR_DEVICE_CHECK (validate
+ * mode found a bad block id, slot or host-mirror mismatch),
+ * PKV_ERR_TIMEOUT, or PKV_ERR_CUDA if the device reported an error.
+ */
+pkv_status pkv_check_device_errors(pkv_handle *h);
+
+/* Static description of a status code; never NULL. */
+const char *pkv_status_string(pkv_status status);
+
+/* Message of the last failed call on this handle ("" if none); never NULL.
+ * With h == NULL, the message of the last failed pkv_create. */
+const char *pkv_last_error(const pkv_handle *h);
+
+/* Free the workspace and the handle (waits for the device first).  NULL is
+ * accepted and ignored. */
+pkv_status pkv_destroy(pkv_handle *h);
+
+/* ---- planning and diagnostics -------------------------------------------- */
+
+/* One unit of kernel work: a (request, KV head) pair restricted to a query
+ * row range and a key range.  Rows r = t * G + g enumerate (query token t,
+ * head g of the group). */
+typedef struct {
+    int32_t kind;        /* 0 = split-KV decode, 1 = prefill tile */
+    int32_t seq;         /* request index */
+    int32_t kv_head;
+    int32_t tok0;        /* index of the request's first query token in q */
+    int32_t row0;        /* first row of this item */
+    int32_t n_rows;      /* rows in this item */
+    int32_t hist;        /* l_hist = L - q of the request */
+    int32_t k_begin;     /* first key position */
+    int32_t k_end;       /* one past the last key position */
+    int32_t part;        /* partial-result slot, or -1: writes the output */
+    int32_t pair;        /* combine ticket index, or -1 */
+    int32_t n_split;     /* splits of this (request, KV head) */
+} pkv_work_item;
+
+/*
+ * Plan a step on the host without a GPU: the work items the kernels of
+ * pkv_attention_varlen would run for these lengths on a device with
+ * `num_sms` multiprocessors.  Items of each kind are in launch order
+ * (longest first).  *num_items receives the count; if it exceeds
+ * max_items only the first max_items are stored.  *num_partials receives the
+ * split partial slots used.  Errors: PKV_ERR_INVALID_ARG for inconsistent
+ * metadata (same checks as pkv_attention_varlen).
+ */
+pkv_status pkv_plan(const pkv_config *config, const int32_t *query_start_loc_host,
+                    const int32_t *seq_lens_host, int32_t num_seqs,
+                    int32_t num_tokens, int32_t num_sms,
+                    pkv_work_item *items, int32_t max_items,
+                    int32_t *num_items, int32_t *num_partials);
+
+/* Kernel kinds reported by pkv_timing_read. */
+enum {
+    PKV_KERNEL_APPEND = 0,
+    PKV_KERNEL_DECODE = 1,
+    PKV_KERNEL_PREFILL = 2,
+    PKV_KERNEL_KINDS = 3
+};
+
+/*
+ * With PKV_FLAG_TIMING, every kernel launch of the handle is bracketed by CUDA
+ * events on its stream (the first 512 launches per kind since the last
+ * reset are kept).
+ * pkv_timing_read waits for those events and returns, per kind, the number
+ * of launches recorded and their summed device time in milliseconds;
+ * pkv_timing_reset forgets them.  Both take a NULL-safe handle; reading
+ * without the flag returns counts of 0.
+ */
+pkv_status pkv_timing_reset(pkv_handle *h);
+pkv_status pkv_timing_read(pkv_handle *h, int32_t kind, int32_t *launches,
+                           double *total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,239 @@
+"""Python binding of libpkv: paged, prefix-cached KV attention on GB300.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+kernels of ``libpkv.so`` behind the C ABI in ``include/pkv.h``; the names here
+mirror those entry points.  PyTorch is used for device memory and streams.
+If the library has not been built (``python -m
+paged_kv_attention_pkv_gb300.build`` or ``__graft_entry__.build()``), loading
+fails with an error: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpkv.so")
+
+PKV_OK = 0
+STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
+                3: "PKV_ERR_CUDA", 4: "PKV_ERR_OUT_OF_MEMORY",
+                5: "PKV_ERR_DEVICE_CHECK", 6: "PKV_ERR_TIMEOUT",
+                7: "PKV_ERR_WORKSPACE"}
+KV_BF16, KV_FP8_E4M3 = 0, 1
+FLAG_VALIDATE, FLAG_TIMING = 1, 2
+KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL = 0, 1, 2
+
+# Every symbol include/pkv.h declares.
+EXPORTS = ["pkv_create", "pkv_write_slots", "pkv_attention_varlen",
+           "pkv_check_device_errors", "pkv_status_string", "pkv_last_error",
+           "pkv_destroy", "pkv_plan", "pkv_timing_reset", "pkv_timing_read"]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
+                ("num_blocks", ctypes.c_int64), ("max_num_seqs", ctypes.c_int32),
+                ("max_num_tokens", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class WorkItem(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("kind", "seq", "kv_head", "tok0", "row0", "n_rows", "hist",
+                 "k_begin", "k_end", "part", "pair", "n_split")]
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libpkv.so and declare its C signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    so = path or LIB_PATH
+    if not os.path.exists(so):
+        raise RuntimeError(
+            f"{so} is missing: build the CUDA library first "
+            "(python -m paged_kv_attention_pkv_gb300.build)")
+    lib = ctypes.CDLL(so)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.pkv_create.restype = ctypes.c_int
+    lib.pkv_create.argtypes = [ctypes.POINTER(Config), ctypes.c_int, ctypes.POINTER(vp)]
+    lib.pkv_write_slots.restype = ctypes.c_int
+    lib.pkv_write_slots.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]
+    lib.pkv_attention_varlen.restype = ctypes.c_int
+    lib.pkv_attention_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                         vp, vp, i32, i32, vp, vp, vp]
+    lib.pkv_check_device_errors.restype = ctypes.c_int
+    lib.pkv_check_device_errors.argtypes = [vp]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_status_string.argtypes = [ctypes.c_int]
+    lib.pkv_last_error.restype = ctypes.c_char_p
+    lib.pkv_last_error.argtypes = [vp]
+    lib.pkv_destroy.restype = ctypes.c_int
+    lib.pkv_destroy.argtypes = [vp]
+    lib.pkv_plan.restype = ctypes.c_int
+    lib.pkv_plan.argtypes = [ctypes.POINTER(Config), vp, vp, i32, i32, i32,
+                             ctypes.POINTER(WorkItem), i32, ctypes.POINTER(i32),
+                             ctypes.POINTER(i32)]
+    lib.pkv_timing_reset.restype = ctypes.c_int
+    lib.pkv_timing_reset.argtypes = [vp]
+    lib.pkv_timing_read.restype = ctypes.c_int
+    lib.pkv_timing_read.argtypes = [vp, i32, ctypes.POINTER(i32),
+                                    ctypes.POINTER(ctypes.c_double)]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(status).decode()
+
+
+def _ptr(x) -> ctypes.c_void_p | None:
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return ctypes.c_void_p(x.data_ptr())
+    if isinstance(x, np.ndarray):
+        return ctypes.c_void_p(x.ctypes.data)
+    return ctypes.c_void_p(int(x))
+
+
+def _host_i32(a) -> np.ndarray:
+    if isinstance(a, torch.Tensor):
+        a = a.cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _stream(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def make_config(num_q_heads, num_kv_heads, block_size, num_blocks, max_num_seqs,
+                max_num_tokens, kv_dtype=KV_BF16, softmax_scale=None, flags=0,
+                head_dim=128) -> Config:
+    if softmax_scale is None:
+        softmax_scale = head_dim ** -0.5
+    return Config(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype,
+                  float(softmax_scale), int(num_blocks), max_num_seqs,
+                  max_num_tokens, flags)
+
+
+class Handle:
+    """A libpkv handle bound to one CUDA device (pkv_create / pkv_destroy)."""
+
+    def __init__(self, config: Config, device: int = 0):
+        self._lib = load()
+        self.config = config
+        self.device = device
+        h = ctypes.c_void_p()
+        st = self._lib.pkv_create(ctypes.byref(config), device, ctypes.byref(h))
+        if st != PKV_OK:
+            raise PkvError(st, self._lib.pkv_last_error(None).decode())
+        self._h = h
+
+    def _check(self, st: int):
+        if st != PKV_OK:
+            raise PkvError(st, self._lib.pkv_last_error(self._h).decode())
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pkv_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @property
+    def fp8(self) -> bool:
+        return self.config.kv_dtype == KV_FP8_E4M3
+
+    def write_slots(self, k_new, v_new, slot_mapping, k_cache, v_cache,
+                    k_scale=None, v_scale=None, stream=None) -> None:
+        """pkv_write_slots: append this step's K/V rows at their slots."""
+        self._check(self._lib.pkv_write_slots(
+            self._h, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+            int(slot_mapping.shape[0]), _ptr(k_cache), _ptr(v_cache),
+            _ptr(k_scale), _ptr(v_scale), _stream(stream, self.device)))
+
+    def attention_varlen(self, q, k_cache, v_cache, query_start_loc, seq_lens,
+                         block_tables, query_start_loc_host, seq_lens_host,
+                         out=None, lse=None, k_scale=None, v_scale=None,
+                         stream=None):
+        """pkv_attention_varlen: one step over a mixed varlen batch.
+
+        Returns ``(out, lse)``; ``out`` is allocated if not given.  ``lse``
+        is written only when a tensor is passed.
+        """
+        qslh = _host_i32(query_start_loc_host)
+        lenh = _host_i32(seq_lens_host)
+        if out is None:
+            out = torch.empty_like(q)
+        self._check(self._lib.pkv_attention_varlen(
+            self._h, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+            _ptr(v_scale), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_tables),
+            int(block_tables.shape[1]), _ptr(qslh), _ptr(lenh), int(lenh.shape[0]),
+            int(q.shape[0]), _ptr(out), _ptr(lse), _stream(stream, self.device)))
+        return out, lse
+
+    def check_device_errors(self) -> None:
+        """pkv_check_device_errors: raise PkvError if the device recorded one."""
+        self._check(self._lib.pkv_check_device_errors(self._h))
+
+    def timing_reset(self) -> None:
+        self._check(self._lib.pkv_timing_reset(self._h))
+
+    def timing_read(self, kind: int) -> tuple[int, float]:
+        """(launches, total milliseconds) of one kernel kind since the reset."""
+        n = ctypes.c_int32()
+        ms = ctypes.c_double()
+        self._check(self._lib.pkv_timing_read(self._h, kind, ctypes.byref(n),
+                                              ctypes.byref(ms)))
+        return n.value, ms.value
+
+
+def plan(config: Config, query_start_loc_host, seq_lens_host, num_sms: int = 152):
+    """pkv_plan: the work items a step would run, as a list of dicts."""
+    lib = load()
+    qslh = _host_i32(query_start_loc_host)
+    lenh = _host_i32(seq_lens_host)
+    n = ctypes.c_int32()
+    parts = ctypes.c_int32()
+    st = lib.pkv_plan(ctypes.byref(config), _ptr(qslh), _ptr(lenh), int(lenh.shape[0]),
+                      int(qslh[-1]) if qslh.size else 0, num_sms, None, 0,
+                      ctypes.byref(n), ctypes.byref(parts))
+    if st != PKV_OK:
+        raise PkvError(st, lib.pkv_last_error(None).decode())
+    arr = (WorkItem * max(n.value, 1))()
+    st = lib.pkv_plan(ctypes.byref(config), _ptr(qslh), _ptr(lenh), int(lenh.shape[0]),
+                      int(qslh[-1]), num_sms, arr, n.value, ctypes.byref(n),
+                      ctypes.byref(parts))
+    if st != PKV_OK:
+        raise PkvError(st, lib.pkv_last_error(None).decode())
+    items = [{f: getattr(arr[i], f) for f, _ in WorkItem._fields_} for i in range(n.value)]
+    return items, parts.value

@@ -1,0 +1,667 @@
+// libpkv host side: the C ABI of include/pkv.h.  Argument validation, the
+// work planner (split-KV decode items and prefill tiles), workspace, TMA
+// descriptors for the paged pools, kernel launches and timing.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+cudaError_t configure_decode();
+cudaError_t configure_prefill();
+}  // namespace pkv
+
+using namespace pkv;
+
+namespace {
+
+constexpr int kTimingSlots = 512;
+constexpr int kMaxPartials = 16384;        // split-KV partial slots
+constexpr int64_t kMaxPoolRows = (int64_t(1) << 31) - 4096;
+
+thread_local std::string g_create_error;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
+                                  void *, const cuuint64_t *, const cuuint64_t *,
+                                  const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+std::string fmt(const char *f, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, f);
+  vsnprintf(buf, sizeof buf, f, ap);
+  va_end(ap);
+  return buf;
+}
+
+struct TimingRing {
+  cudaEvent_t start[kTimingSlots];
+  cudaEvent_t stop[kTimingSlots];
+  int count = 0;
+};
+
+}  // namespace
+
+struct pkv_handle {
+  pkv_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  std::string last_error;
+  // workspace
+  uint8_t *d_work = nullptr;      // work list + host-mirror copies
+  size_t work_bytes = 0;
+  int max_items = 0;
+  float *d_part_o = nullptr;
+  float *d_part_lse = nullptr;
+  int32_t *d_tickets = nullptr;
+  int32_t *d_err = nullptr;
+  uint8_t *h_stage[2] = {nullptr, nullptr};   // pinned staging (double buffer)
+  cudaEvent_t staged[2] = {nullptr, nullptr};
+  int stage_cur = 0;
+  // timing
+  bool timing = false;
+  TimingRing rings[PKV_KERNEL_KINDS];
+  // cached pool descriptors
+  const void *map_k_ptr = nullptr, *map_v_ptr = nullptr;
+  CUtensorMap dec_k{}, dec_v{}, pf_k{}, pf_v{};
+};
+
+namespace {
+
+pkv_status fail(pkv_handle *h, pkv_status s, const std::string &msg) {
+  if (h) h->last_error = msg;
+  return s;
+}
+
+pkv_status cuda_fail(pkv_handle *h, cudaError_t e, const char *what) {
+  return fail(h, PKV_ERR_CUDA, fmt("%s: %s", what, cudaGetErrorString(e)));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+std::string check_config(const pkv_config *c, pkv_status *st) {
+  *st = PKV_ERR_INVALID_ARG;
+  if (c == nullptr) return "config is NULL";
+  if (c->num_kv_heads <= 0 || c->num_q_heads <= 0 ||
+      c->num_q_heads % c->num_kv_heads != 0)
+    return fmt("num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+               c->num_q_heads, c->num_kv_heads);
+  if (!(c->softmax_scale > 0.f) || c->softmax_scale > 1e30f)
+    return "softmax_scale must be finite and > 0";
+  if (c->num_blocks <= 0) return "num_blocks must be > 0";
+  if (c->max_num_seqs <= 0 || c->max_num_tokens <= 0)
+    return "max_num_seqs and max_num_tokens must be > 0";
+  if (c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_FP8_E4M3)
+    return fmt("unknown kv_dtype %d", c->kv_dtype);
+  *st = PKV_ERR_UNSUPPORTED;
+  if (c->head_dim != kHeadDim) return fmt("head_dim %d is not supported (only 128)", c->head_dim);
+  const int bs = c->block_size;
+  if (bs != 16 && bs != 32 && bs != 64 && bs != 128 && bs != 256)
+    return fmt("block_size %d is not supported (16, 32, 64, 128 or 256)", bs);
+  if (c->num_blocks * c->num_kv_heads * bs > kMaxPoolRows)
+    return "pool too large: num_blocks * num_kv_heads * block_size must be < 2^31 - 4096";
+  *st = PKV_OK;
+  return "";
+}
+
+// Planner: split-KV decode items and prefill tiles, longest first.
+struct Plan {
+  std::vector<pkv_work_item> dec, pre;
+  int partials = 0;
+};
+
+std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *lens,
+                      int32_t B, int32_t T, int num_sms, int max_partials, Plan *plan,
+                      pkv_status *st) {
+  *st = PKV_ERR_INVALID_ARG;
+  if (B < 0 || T < 0) return "num_seqs and num_tokens must be >= 0";
+  if (B > 0 && (qsl == nullptr || lens == nullptr))
+    return "query_start_loc_host and seq_lens_host are required";
+  if (B == 0) {
+    if (T != 0) return "num_tokens must be 0 when num_seqs is 0";
+    *st = PKV_OK;
+    return "";
+  }
+  if (qsl[0] != 0) return "query_start_loc_host[0] must be 0";
+  if (qsl[B] != T)
+    return fmt("query_start_loc_host[num_seqs] = %d but num_tokens = %d", qsl[B], T);
+  const int G = c.num_q_heads / c.num_kv_heads;
+  const int H = c.num_kv_heads;
+  int64_t dec_keys = 0;
+  for (int i = 0; i < B; ++i) {
+    const int64_t q = int64_t(qsl[i + 1]) - qsl[i];
+    if (q < 0) return fmt("query_start_loc_host decreases at %d", i);
+    if (lens[i] < q) return fmt("seq_lens_host[%d] = %d is less than its %lld new tokens", i, lens[i], (long long)q);
+    if (q > 0 && q * G <= kDecCols) dec_keys += int64_t(lens[i]) * H;
+  }
+  // decode split size: ~4 waves of 2 CTAs per SM, at least 1024 keys
+  const int64_t target = int64_t(8) * std::max(num_sms, 1);
+  int64_t chunk = std::max<int64_t>(1024, (dec_keys / target + kSplitAlign - 1) / kSplitAlign * kSplitAlign);
+  for (;;) {
+    int64_t parts = 0;
+    for (int i = 0; i < B; ++i) {
+      const int64_t q = int64_t(qsl[i + 1]) - qsl[i];
+      if (q > 0 && q * G <= kDecCols) {
+        const int64_t ns = (lens[i] + chunk - 1) / chunk;
+        if (ns > 1) parts += ns * H;
+      }
+    }
+    if (parts <= max_partials) break;
+    chunk *= 2;
+  }
+  plan->dec.clear();
+  plan->pre.clear();
+  int part = 0;
+  for (int i = 0; i < B; ++i) {
+    const int q = qsl[i + 1] - qsl[i];
+    if (q == 0) continue;
+    const int L = lens[i];
+    const int hist = L - q;
+    if (q * G <= kDecCols) {
+      const int ns = static_cast<int>((L + chunk - 1) / chunk);
+      for (int h = 0; h < H; ++h) {
+        const int base = ns > 1 ? part : -1;
+        for (int s = 0; s < ns; ++s) {
+          pkv_work_item w{};
+          w.kind = 0;
+          w.seq = i;
+          w.kv_head = h;
+          w.tok0 = qsl[i];
+          w.row0 = 0;
+          w.n_rows = q * G;
+          w.hist = hist;
+          w.k_begin = static_cast<int32_t>(s * chunk);
+          w.k_end = static_cast<int32_t>(std::min<int64_t>(L, (s + 1) * chunk));
+          w.part = ns > 1 ? part++ : -1;
+          w.pair = base;
+          w.n_split = ns;
+          plan->dec.push_back(w);
+        }
+      }
+    } else {
+      const int rows = q * G;
+      for (int h = 0; h < H; ++h) {
+        for (int r0 = 0; r0 < rows; r0 += kPfRows) {
+          pkv_work_item w{};
+          w.kind = 1;
+          w.seq = i;
+          w.kv_head = h;
+          w.tok0 = qsl[i];
+          w.row0 = r0;
+          w.n_rows = std::min(kPfRows, rows - r0);
+          w.hist = hist;
+          w.k_begin = 0;
+          w.k_end = hist + (r0 + w.n_rows - 1) / G + 1;
+          w.part = -1;
+          w.pair = -1;
+          w.n_split = 1;
+          plan->pre.push_back(w);
+        }
+      }
+    }
+  }
+  plan->partials = part;
+  auto dec_cost = [](const pkv_work_item &w) { return int64_t(w.k_end) - w.k_begin; };
+  std::stable_sort(plan->dec.begin(), plan->dec.end(),
+                   [&](const pkv_work_item &a, const pkv_work_item &b) {
+                     return dec_cost(a) > dec_cost(b);
+                   });
+  auto pre_cost = [](const pkv_work_item &w) { return int64_t(w.k_end) * w.n_rows; };
+  std::stable_sort(plan->pre.begin(), plan->pre.end(),
+                   [&](const pkv_work_item &a, const pkv_work_item &b) {
+                     return pre_cost(a) > pre_cost(b);
+                   });
+  *st = PKV_OK;
+  return "";
+}
+
+bool encode_pool_map(CUtensorMap *m, const void *base, bool fp8, int64_t rows,
+                     int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * (fp8 ? 1 : 2))};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(fp8 ? 128 : 64),
+                             static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t items_bytes(int max_items) { return sizeof(pkv_work_item) * size_t(max_items); }
+
+void timing_begin(pkv_handle *h, int kind, cudaStream_t s) {
+  if (!h->timing) return;
+  TimingRing &r = h->rings[kind];
+  cudaEventRecord(r.start[r.count % kTimingSlots], s);
+}
+void timing_end(pkv_handle *h, int kind, cudaStream_t s) {
+  if (!h->timing) return;
+  TimingRing &r = h->rings[kind];
+  cudaEventRecord(r.stop[r.count % kTimingSlots], s);
+  ++r.count;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_OUT_OF_MEMORY: return "out of device memory";
+    case PKV_ERR_DEVICE_CHECK: return "device-side check failed";
+    case PKV_ERR_TIMEOUT: return "device-side wait timed out";
+    case PKV_ERR_WORKSPACE: return "workspace too small for this step";
+  }
+  return "unknown status";
+}
+
+const char *pkv_last_error(const pkv_handle *h) {
+  return h ? h->last_error.c_str() : g_create_error.c_str();
+}
+
+pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out) {
+  g_create_error.clear();
+  if (out == nullptr) {
+    g_create_error = "out is NULL";
+    return PKV_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  pkv_status st;
+  std::string msg = check_config(config, &st);
+  if (st != PKV_OK) {
+    g_create_error = msg;
+    return st;
+  }
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess || device < 0 || device >= ndev) {
+    g_create_error = fmt("no CUDA device %d (%s)", device,
+                         e != cudaSuccess ? cudaGetErrorString(e) : "out of range");
+    return PKV_ERR_CUDA;
+  }
+  if ((e = cudaSetDevice(device)) != cudaSuccess) {
+    g_create_error = fmt("cudaSetDevice: %s", cudaGetErrorString(e));
+    return PKV_ERR_CUDA;
+  }
+  if (encode_fn() == nullptr) {
+    g_create_error = "cuTensorMapEncodeTiled is not available from the driver";
+    return PKV_ERR_CUDA;
+  }
+  if ((e = configure_decode()) != cudaSuccess || (e = configure_prefill()) != cudaSuccess) {
+    g_create_error = fmt("configuring kernels: %s", cudaGetErrorString(e));
+    return PKV_ERR_CUDA;
+  }
+  pkv_handle *h = new pkv_handle();
+  h->cfg = *config;
+  h->device = device;
+  cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device);
+  const int64_t G = config->num_q_heads / config->num_kv_heads;
+  const int64_t pre_items =
+      (int64_t(config->max_num_tokens) * G / kPfRows + config->max_num_seqs) *
+      config->num_kv_heads;
+  h->max_items = static_cast<int>(kMaxPartials + int64_t(config->max_num_seqs) * config->num_kv_heads + pre_items);
+  h->work_bytes = items_bytes(h->max_items) + sizeof(int32_t) * (2 * size_t(config->max_num_seqs) + 1);
+  bool ok = cudaMalloc(&h->d_work, h->work_bytes) == cudaSuccess &&
+            cudaMalloc(&h->d_part_o, sizeof(float) * size_t(kMaxPartials) * kDecCols * kHeadDim) == cudaSuccess &&
+            cudaMalloc(&h->d_part_lse, sizeof(float) * size_t(kMaxPartials) * kDecCols) == cudaSuccess &&
+            cudaMalloc(&h->d_tickets, sizeof(int32_t) * kMaxPartials) == cudaSuccess &&
+            cudaMalloc(&h->d_err, sizeof(int32_t)) == cudaSuccess &&
+            cudaMallocHost(&h->h_stage[0], h->work_bytes) == cudaSuccess &&
+            cudaMallocHost(&h->h_stage[1], h->work_bytes) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->staged[0], cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->staged[1], cudaEventDisableTiming) == cudaSuccess;
+  if (ok) {
+    ok = cudaMemset(h->d_tickets, 0, sizeof(int32_t) * kMaxPartials) == cudaSuccess &&
+         cudaMemset(h->d_err, 0, sizeof(int32_t)) == cudaSuccess;
+  }
+  if (ok && (config->flags & PKV_FLAG_TIMING)) {
+    h->timing = true;
+    for (auto &r : h->rings)
+      for (int i = 0; i < kTimingSlots && ok; ++i)
+        ok = cudaEventCreate(&r.start[i]) == cudaSuccess &&
+             cudaEventCreate(&r.stop[i]) == cudaSuccess;
+  }
+  if (!ok) {
+    cudaGetLastError();
+    pkv_destroy(h);
+    g_create_error = "could not allocate the workspace";
+    return PKV_ERR_OUT_OF_MEMORY;
+  }
+  *out = h;
+  return PKV_OK;
+}
+
+pkv_status pkv_destroy(pkv_handle *h) {
+  if (h == nullptr) return PKV_OK;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  cudaFree(h->d_work);
+  cudaFree(h->d_part_o);
+  cudaFree(h->d_part_lse);
+  cudaFree(h->d_tickets);
+  cudaFree(h->d_err);
+  for (int i = 0; i < 2; ++i) {
+    if (h->h_stage[i]) cudaFreeHost(h->h_stage[i]);
+    if (h->staged[i]) cudaEventDestroy(h->staged[i]);
+  }
+  if (h->timing)
+    for (auto &r : h->rings)
+      for (int i = 0; i < kTimingSlots; ++i) {
+        if (r.start[i]) cudaEventDestroy(r.start[i]);
+        if (r.stop[i]) cudaEventDestroy(r.stop[i]);
+      }
+  delete h;
+  return PKV_OK;
+}
+
+pkv_status pkv_write_slots(pkv_handle *h, const void *k_new, const void *v_new,
+                           const int64_t *slot_mapping, int32_t num_tokens,
+                           void *k_cache, void *v_cache, const float *k_scale,
+                           const float *v_scale, void *stream) {
+  if (h == nullptr) return PKV_ERR_INVALID_ARG;
+  h->last_error.clear();
+  if (num_tokens < 0) return fail(h, PKV_ERR_INVALID_ARG, "num_tokens must be >= 0");
+  if (num_tokens > h->cfg.max_num_tokens)
+    return fail(h, PKV_ERR_INVALID_ARG,
+                fmt("num_tokens %d exceeds max_num_tokens %d", num_tokens, h->cfg.max_num_tokens));
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
+    return fail(h, PKV_ERR_INVALID_ARG, "NULL buffer");
+  const bool fp8 = h->cfg.kv_dtype == PKV_KV_FP8_E4M3;
+  if (fp8 && (!k_scale || !v_scale))
+    return fail(h, PKV_ERR_INVALID_ARG, "FP8 pools need k_scale and v_scale");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(h, PKV_ERR_INVALID_ARG, "K/V buffers must be 16-byte aligned");
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  AppendParams p{};
+  p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  p.slots = slot_mapping;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.err = h->d_err;
+  p.num_tokens = num_tokens;
+  p.hkv = h->cfg.num_kv_heads;
+  p.bs = h->cfg.block_size;
+  p.num_blocks = h->cfg.num_blocks;
+  p.validate = (h->cfg.flags & PKV_FLAG_VALIDATE) != 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  timing_begin(h, PKV_KERNEL_APPEND, s);
+  e = launch_append(p, fp8, s);
+  timing_end(h, PKV_KERNEL_APPEND, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "KV append launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cache,
+                                const void *v_cache, const float *k_scale,
+                                const float *v_scale, const int32_t *query_start_loc,
+                                const int32_t *seq_lens, const int32_t *block_tables,
+                                int32_t block_table_stride,
+                                const int32_t *qsl_host, const int32_t *lens_host,
+                                int32_t num_seqs, int32_t num_tokens, void *out,
+                                float *lse, void *stream) {
+  if (h == nullptr) return PKV_ERR_INVALID_ARG;
+  h->last_error.clear();
+  const pkv_config &c = h->cfg;
+  if (num_seqs > c.max_num_seqs)
+    return fail(h, PKV_ERR_INVALID_ARG, fmt("num_seqs %d exceeds max_num_seqs %d", num_seqs, c.max_num_seqs));
+  if (num_tokens > c.max_num_tokens)
+    return fail(h, PKV_ERR_INVALID_ARG, fmt("num_tokens %d exceeds max_num_tokens %d", num_tokens, c.max_num_tokens));
+  Plan plan;
+  pkv_status st;
+  std::string msg = make_plan(c, qsl_host, lens_host, num_seqs, num_tokens, h->num_sms,
+                              kMaxPartials, &plan, &st);
+  if (st != PKV_OK) return fail(h, st, msg);
+  if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !query_start_loc || !seq_lens || !block_tables || !out)
+    return fail(h, PKV_ERR_INVALID_ARG, "NULL buffer");
+  const bool fp8 = c.kv_dtype == PKV_KV_FP8_E4M3;
+  if (fp8 && (!k_scale || !v_scale))
+    return fail(h, PKV_ERR_INVALID_ARG, "FP8 pools need k_scale and v_scale");
+  if (fp8 && !plan.pre.empty())
+    return fail(h, PKV_ERR_UNSUPPORTED,
+                "prefill rows (q * G > 8) over FP8 pools are not supported");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return fail(h, PKV_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
+  const int bs = c.block_size;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int64_t nb = (int64_t(lens_host[i]) + bs - 1) / bs;
+    if (nb > block_table_stride)
+      return fail(h, PKV_ERR_INVALID_ARG,
+                  fmt("request %d needs %lld block-table entries but the stride is %d", i,
+                      (long long)nb, block_table_stride));
+  }
+  const int n_items = static_cast<int>(plan.dec.size() + plan.pre.size());
+  if (n_items > h->max_items)
+    return fail(h, PKV_ERR_WORKSPACE, fmt("step needs %d work items, workspace holds %d", n_items, h->max_items));
+
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // pool descriptors (re-encoded when the pools move)
+  if (k_cache != h->map_k_ptr || v_cache != h->map_v_ptr) {
+    const int64_t rows = c.num_blocks * c.num_kv_heads * bs;
+    const int dec_box = std::min(bs, fp8 ? kDecKeysFp8 : kDecKeysBf16);
+    const int pf_box = std::min(bs, kPfKeys);
+    bool ok = encode_pool_map(&h->dec_k, k_cache, fp8, rows, dec_box) &&
+              encode_pool_map(&h->dec_v, v_cache, fp8, rows, dec_box);
+    if (ok && !fp8)
+      ok = encode_pool_map(&h->pf_k, k_cache, false, rows, pf_box) &&
+           encode_pool_map(&h->pf_v, v_cache, false, rows, pf_box);
+    if (!ok) {
+      h->map_k_ptr = h->map_v_ptr = nullptr;
+      return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled rejected the pool layout");
+    }
+    h->map_k_ptr = k_cache;
+    h->map_v_ptr = v_cache;
+  }
+
+  // stage the work list (+ host mirrors for validate mode) and upload it
+  const int cur = h->stage_cur;
+  h->stage_cur ^= 1;
+  e = cudaEventSynchronize(h->staged[cur]);   // this buffer's previous copy is done
+  if (e != cudaSuccess) return cuda_fail(h, e, "staging event");
+  uint8_t *hs = h->h_stage[cur];
+  size_t nbytes = items_bytes(n_items);
+  std::memcpy(hs, plan.dec.data(), items_bytes(plan.dec.size()));
+  std::memcpy(hs + items_bytes(plan.dec.size()), plan.pre.data(), items_bytes(plan.pre.size()));
+  const bool validate = (c.flags & PKV_FLAG_VALIDATE) != 0;
+  const size_t mirror_off = items_bytes(h->max_items);
+  if (validate) {
+    std::memcpy(hs + mirror_off, qsl_host, sizeof(int32_t) * (num_seqs + 1));
+    std::memcpy(hs + mirror_off + sizeof(int32_t) * (num_seqs + 1), lens_host,
+                sizeof(int32_t) * num_seqs);
+  }
+  e = cudaMemcpyAsync(h->d_work, hs, nbytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && validate)
+    e = cudaMemcpyAsync(h->d_work + mirror_off, hs + mirror_off,
+                        sizeof(int32_t) * (2 * num_seqs + 1), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaEventRecord(h->staged[cur], s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "work-list upload");
+  const pkv_work_item *d_items = reinterpret_cast<const pkv_work_item *>(h->d_work);
+
+  if (validate) {
+    CheckParams cp{};
+    cp.qsl = query_start_loc;
+    cp.seq_lens = seq_lens;
+    cp.block_tables = block_tables;
+    cp.qsl_expect = reinterpret_cast<const int32_t *>(h->d_work + mirror_off);
+    cp.seq_lens_expect = cp.qsl_expect + num_seqs + 1;
+    cp.bt_stride = block_table_stride;
+    cp.num_seqs = num_seqs;
+    cp.bs = bs;
+    cp.num_blocks = c.num_blocks;
+    cp.err = h->d_err;
+    if ((e = launch_check(cp, s)) != cudaSuccess) return cuda_fail(h, e, "check launch");
+  }
+
+  const float scale_log2 = c.softmax_scale * 1.4426950408889634f;
+  const int G = c.num_q_heads / c.num_kv_heads;
+  const int32_t rows_total = static_cast<int32_t>(c.num_blocks * c.num_kv_heads * bs);
+  if (!plan.dec.empty()) {
+    DecodeParams p{};
+    p.items = d_items;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.block_tables = block_tables;
+    p.bt_stride = block_table_stride;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.part_o = h->d_part_o;
+    p.part_lse = h->d_part_lse;
+    p.tickets = h->d_tickets;
+    p.err = h->d_err;
+    p.hq = c.num_q_heads;
+    p.hkv = c.num_kv_heads;
+    p.group = G;
+    p.bs = bs;
+    p.rows_total = rows_total;
+    p.num_blocks = c.num_blocks;
+    p.scale_log2 = scale_log2;
+    p.validate = validate;
+    timing_begin(h, PKV_KERNEL_DECODE, s);
+    e = launch_decode(h->dec_k, h->dec_v, p, static_cast<int>(plan.dec.size()), fp8, s);
+    timing_end(h, PKV_KERNEL_DECODE, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
+  }
+  if (!plan.pre.empty()) {
+    PrefillParams p{};
+    p.items = d_items + plan.dec.size();
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.block_tables = block_tables;
+    p.bt_stride = block_table_stride;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.err = h->d_err;
+    p.hq = c.num_q_heads;
+    p.hkv = c.num_kv_heads;
+    p.group = G;
+    p.bs = bs;
+    p.rows_total = rows_total;
+    p.num_blocks = c.num_blocks;
+    p.scale_log2 = scale_log2;
+    p.validate = validate;
+    timing_begin(h, PKV_KERNEL_PREFILL, s);
+    e = launch_prefill(h->pf_k, h->pf_v, p, static_cast<int>(plan.pre.size()), s);
+    timing_end(h, PKV_KERNEL_PREFILL, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_check_device_errors(pkv_handle *h) {
+  if (h == nullptr) return PKV_ERR_INVALID_ARG;
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(h, e, "device");
+  int32_t word = 0;
+  e = cudaMemcpy(&word, h->d_err, sizeof word, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int32_t));
+  if (e != cudaSuccess) return cuda_fail(h, e, "reading the error word");
+  if (word & kErrTimeout)
+    return fail(h, PKV_ERR_TIMEOUT, "a device-side wait gave up (error word 0x" + fmt("%x", word) + ")");
+  if (word != 0) {
+    std::string what;
+    if (word & kErrBadBlock) what += " block-table entry outside the pool;";
+    if (word & kErrBadSlot) what += " slot outside the pool;";
+    if (word & kErrMismatch) what += " device metadata differs from the host mirrors;";
+    return fail(h, PKV_ERR_DEVICE_CHECK, "device check:" + what);
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_plan(const pkv_config *config, const int32_t *qsl_host,
+                    const int32_t *lens_host, int32_t num_seqs, int32_t num_tokens,
+                    int32_t num_sms, pkv_work_item *items, int32_t max_items,
+                    int32_t *num_items, int32_t *num_partials) {
+  pkv_status st;
+  std::string msg = check_config(config, &st);
+  if (st != PKV_OK) {
+    g_create_error = msg;
+    return st;
+  }
+  Plan plan;
+  msg = make_plan(*config, qsl_host, lens_host, num_seqs, num_tokens, num_sms,
+                  kMaxPartials, &plan, &st);
+  if (st != PKV_OK) {
+    g_create_error = msg;
+    return st;
+  }
+  const int n = static_cast<int>(plan.dec.size() + plan.pre.size());
+  if (num_items) *num_items = n;
+  if (num_partials) *num_partials = plan.partials;
+  if (items) {
+    int k = 0;
+    for (const auto &w : plan.dec)
+      if (k < max_items) items[k++] = w;
+    for (const auto &w : plan.pre)
+      if (k < max_items) items[k++] = w;
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_timing_reset(pkv_handle *h) {
+  if (h == nullptr) return PKV_OK;
+  for (auto &r : h->rings) r.count = 0;
+  return PKV_OK;
+}
+
+pkv_status pkv_timing_read(pkv_handle *h, int32_t kind, int32_t *launches,
+                           double *total_ms) {
+  if (launches) *launches = 0;
+  if (total_ms) *total_ms = 0.0;
+  if (h == nullptr) return PKV_OK;
+  if (kind < 0 || kind >= PKV_KERNEL_KINDS)
+    return fail(h, PKV_ERR_INVALID_ARG, fmt("unknown kernel kind %d", kind));
+  if (!h->timing) return PKV_OK;
+  TimingRing &r = h->rings[kind];
+  const int n = std::min(r.count, kTimingSlots);
+  double sum = 0.0;
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = cudaEventSynchronize(r.stop[i]);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start[i], r.stop[i]);
+    if (e != cudaSuccess) return cuda_fail(h, e, "timing events");
+    sum += ms;
+  }
+  if (launches) *launches = n;
+  if (total_ms) *total_ms = sum;
+  return PKV_OK;
+}
+
+}  // extern "C"

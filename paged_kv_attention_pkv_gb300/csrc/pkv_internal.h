@@ -1,0 +1,117 @@
+// Internal definitions shared by the libpkv host code and kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kHeadDim = 128;
+
+// Device error word bits (validate mode and bounded waits).
+enum : int32_t {
+  kErrBadBlock = 1,     // a block-table entry in use is outside the pool
+  kErrBadSlot = 2,      // a slot_mapping entry is outside the pool
+  kErrTimeout = 4,      // a bounded wait gave up
+  kErrMismatch = 8,     // device metadata differs from the host mirrors
+};
+
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+// ---- decode (split-KV) kernel geometry ---------------------------------------
+constexpr int kDecWarps = 4;              // consumer warps, each its own ring
+constexpr int kDecStages = 3;             // ring depth per warp
+constexpr int kDecStageBytes = 8192;      // K 4 KB + V 4 KB per stage
+constexpr int kDecCols = 8;               // query rows per item (MMA N)
+constexpr int kDecKeysBf16 = 16;          // keys per stage, bf16 pools
+constexpr int kDecKeysFp8 = 32;           // keys per stage, E4M3 pools
+constexpr int kDecSmemBytes =
+    kDecWarps * kDecStages * kDecStageBytes + 1024 /* align */ + 256;
+constexpr int kSplitAlign = 256;          // split ranges start at multiples
+
+// ---- prefill kernel geometry ---------------------------------------------------
+constexpr int kPfRows = 64;               // query rows per item (4 warps x 16)
+constexpr int kPfKeys = 64;               // keys per stage
+constexpr int kPfStages = 3;
+constexpr int kPfStageBytes = 2 * kPfKeys * kHeadDim * 2;  // K + V, bf16
+constexpr int kPfSmemBytes = kPfStages * kPfStageBytes + 1024 + 256;
+
+struct DecodeParams {
+  const pkv_work_item *items;
+  const __nv_bfloat16 *q;
+  const int32_t *block_tables;
+  int32_t bt_stride;
+  const float *k_scale;
+  const float *v_scale;
+  __nv_bfloat16 *out;
+  float *lse;
+  float *part_o;     // [slots][kDecCols][128]
+  float *part_lse;   // [slots][kDecCols], log2 domain
+  int32_t *tickets;  // indexed by an item's first partial slot
+  int32_t *err;
+  int32_t hq, hkv, group, bs;
+  int32_t rows_total;   // num_blocks * hkv * bs (rows of the pool maps)
+  int64_t num_blocks;
+  float scale_log2;     // softmax_scale * log2(e)
+  int32_t validate;
+};
+
+struct PrefillParams {
+  const pkv_work_item *items;
+  const __nv_bfloat16 *q;
+  const int32_t *block_tables;
+  int32_t bt_stride;
+  __nv_bfloat16 *out;
+  float *lse;
+  int32_t *err;
+  int32_t hq, hkv, group, bs;
+  int32_t rows_total;
+  int64_t num_blocks;
+  float scale_log2;
+  int32_t validate;
+};
+
+struct AppendParams {
+  const __nv_bfloat16 *k_new;
+  const __nv_bfloat16 *v_new;
+  const int64_t *slots;
+  void *k_cache;
+  void *v_cache;
+  const float *k_scale;
+  const float *v_scale;
+  int32_t *err;
+  int64_t num_tokens;
+  int32_t hkv, bs;
+  int64_t num_blocks;
+  int32_t validate;
+};
+
+struct CheckParams {
+  const int32_t *qsl;
+  const int32_t *seq_lens;
+  const int32_t *block_tables;
+  const int32_t *qsl_expect;       // host mirrors uploaded with the plan
+  const int32_t *seq_lens_expect;
+  int32_t bt_stride;
+  int32_t num_seqs;
+  int32_t bs;
+  int64_t num_blocks;
+  int32_t *err;
+};
+
+// Launchers (each returns the launch's cudaError_t).
+cudaError_t launch_append(const AppendParams &p, bool fp8, cudaStream_t s);
+cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                          const DecodeParams &p, int num_items, bool fp8,
+                          cudaStream_t s);
+cudaError_t launch_prefill(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                           const PrefillParams &p, int num_items,
+                           cudaStream_t s);
+cudaError_t launch_check(const CheckParams &p, cudaStream_t s);
+cudaError_t configure_kernels();
+
+}  // namespace pkv

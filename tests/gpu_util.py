@@ -1,0 +1,111 @@
+"""Helpers for the GPU parity tests: run a step through the C ABI and the
+same step through the fp64 oracle on host copies of the inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_attention_pkv_gb300 as pkv
+import workloads as W
+
+# The gate: max-abs 1e-2 and mean-abs 1e-3 on bf16 outputs, max-abs 2e-2 with
+# E4M3 KV.  Because these absolute bounds cannot tell a correct answer from
+# zeros at long context (outputs shrink like sqrt(e / L)), every check also
+# bounds the per-row relative L2 error and the log-sum-exp error.
+TOL = {
+    "bf16": dict(max_abs=1e-2, mean_abs=1e-3, rel=1e-2, lse=1e-3),
+    "fp8": dict(max_abs=2e-2, mean_abs=1e-3, rel=2e-2, lse=1e-3),
+}
+
+
+def make_handle(batch: W.Batch, flags: int = pkv.FLAG_VALIDATE) -> pkv.Handle:
+    s = batch.spec
+    cfg = pkv.make_config(s.hq, s.hkv, s.block_size, batch.num_blocks,
+                          max(1, s.num_seqs), max(1, s.num_tokens),
+                          kv_dtype=pkv.KV_FP8_E4M3 if s.kv_dtype == "fp8" else pkv.KV_BF16,
+                          softmax_scale=s.softmax_scale, flags=flags)
+    return pkv.Handle(cfg)
+
+
+def device_meta(batch: W.Batch) -> dict:
+    dev = batch.q.device
+    return {
+        "slots": torch.from_numpy(batch.slot_mapping).to(dev),
+        "qsl": torch.from_numpy(batch.qsl).to(dev),
+        "lens": torch.from_numpy(batch.seq_lens).to(dev),
+        "bt": torch.from_numpy(batch.block_tables).to(dev),
+    }
+
+
+def gpu_step(batch: W.Batch, handle: pkv.Handle | None = None,
+             flags: int = pkv.FLAG_VALIDATE, append: bool = True):
+    """write_slots + attention_varlen through the C ABI; returns (out, lse)."""
+    h = handle or make_handle(batch, flags)
+    m = device_meta(batch)
+    if append:
+        h.write_slots(batch.k_new, batch.v_new, m["slots"], batch.k_cache,
+                      batch.v_cache, batch.k_scale, batch.v_scale)
+    out = torch.full_like(batch.q, float("nan"))
+    lse = torch.full((batch.q.shape[0], batch.q.shape[1]), float("nan"),
+                     dtype=torch.float32, device=batch.q.device)
+    h.attention_varlen(batch.q, batch.k_cache, batch.v_cache, m["qsl"], m["lens"],
+                       m["bt"], batch.qsl, batch.seq_lens, out=out, lse=lse,
+                       k_scale=batch.k_scale, v_scale=batch.v_scale)
+    torch.cuda.synchronize()
+    h.check_device_errors()
+    if handle is None:
+        h.close()
+    return out, lse
+
+
+def oracle_subset(sub: dict, spec: W.Spec, rows=None):
+    """The oracle on a host subset: its own append, then attention."""
+    kc = sub["k_cache"].copy()
+    vc = sub["v_cache"].copy()
+    ks = sub.get("k_scale")
+    vs = sub.get("v_scale")
+    oracle.write_slots(kc, vc, sub["k_new"], sub["v_new"], sub["slot_mapping"],
+                       k_scale=ks, v_scale=vs)
+    return oracle.attention(kc, vc, sub["q"], sub["qsl"], sub["seq_lens"],
+                            sub["block_tables"], spec.softmax_scale,
+                            k_scale=ks, v_scale=vs, rows=rows)
+
+
+def gpu_rows(out: torch.Tensor, lse: torch.Tensor, sub: dict, rows=None):
+    """GPU results at the subset's rows (token * hq_sub + head_sub order)."""
+    hq = len(sub["heads"])
+    if rows is None:
+        rows = np.arange(len(sub["tokens"]) * hq)
+    tok = torch.as_tensor(sub["tokens"][rows // hq], device=out.device)
+    head = torch.as_tensor(sub["heads"][rows % hq], device=out.device)
+    o = out[tok, head].double().cpu().numpy()
+    l = lse[tok, head].double().cpu().numpy()
+    return o, l
+
+
+def check(got, ref, got_lse, ref_lse, kind: str = "bf16", what: str = ""):
+    """Raise AssertionError unless got matches the oracle within TOL[kind]."""
+    t = TOL[kind]
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    assert err.max() <= t["max_abs"], f"{what}: max-abs {err.max():.3e}"
+    assert err.mean() <= t["mean_abs"], f"{what}: mean-abs {err.mean():.3e}"
+    rel = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+    assert rel.max() <= t["rel"], f"{what}: row relative L2 {rel.max():.3e} at row {rel.argmax()}"
+    if got_lse is not None:
+        le = np.abs(got_lse - ref_lse)
+        assert le.max() <= t["lse"], f"{what}: lse error {le.max():.3e}"
+    return dict(max_abs=float(err.max()), mean_abs=float(err.mean()),
+                rel=float(rel.max()),
+                lse=float(np.abs(got_lse - ref_lse).max()) if got_lse is not None else None)
+
+
+def full_parity(batch: W.Batch, flags: int = pkv.FLAG_VALIDATE, what: str = ""):
+    """Every row of a (small) batch against the oracle."""
+    sub = W.subset(batch, list(range(batch.spec.num_seqs)))
+    out, lse = gpu_step(batch, flags=flags)
+    ref, ref_lse = oracle_subset(sub, batch.spec)
+    got, got_lse = gpu_rows(out, lse, sub)
+    return check(got, ref, got_lse, ref_lse, batch.spec.kv_dtype, what)

@@ -1,0 +1,98 @@
+"""Host planner (pkv_plan): work items cover every (request, KV head, row,
+key) exactly as the causal definition needs, split partials are laid out for
+the combine, and bad metadata is rejected (CPU only)."""
+import numpy as np
+import pytest
+
+import paged_kv_attention_pkv_gb300 as pkv
+import workloads
+
+
+def _plan(spec, num_sms=152):
+    cfg = pkv.make_config(spec.hq, spec.hkv, spec.block_size, 10 ** 6,
+                          max(1, spec.num_seqs), max(1, spec.num_tokens),
+                          kv_dtype=1 if spec.kv_dtype == "fp8" else 0)
+    qsl = np.concatenate([[0], np.cumsum(spec.q_lens)]).astype(np.int32)
+    items, parts = pkv.plan(cfg, qsl, np.asarray(spec.seq_lens, np.int32), num_sms)
+    return items, parts, qsl
+
+
+@pytest.mark.parametrize("index", range(5))
+def test_plan_covers_the_workloads(index):
+    spec = workloads.config_spec(index)
+    items, parts, qsl = _plan(spec)
+    G = spec.hq // spec.hkv
+    dec_keys = {}
+    rows = {}
+    slots = []
+    for w in items:
+        i, h = w["seq"], w["kv_head"]
+        q, L = spec.q_lens[i], spec.seq_lens[i]
+        assert w["tok0"] == qsl[i] and w["hist"] == L - q
+        if w["kind"] == 0:
+            assert q * G <= 8 and w["row0"] == 0 and w["n_rows"] == q * G
+            dec_keys.setdefault((i, h), []).append((w["k_begin"], w["k_end"], w))
+        else:
+            assert q * G > 8
+            assert w["k_begin"] == 0
+            last_tok = (w["row0"] + w["n_rows"] - 1) // G
+            assert w["k_end"] == L - q + last_tok + 1          # causal reach
+            rows.setdefault((i, h), []).append((w["row0"], w["n_rows"]))
+        if w["part"] >= 0:
+            slots.append(w["part"])
+    # decode: the ranges of each (request, KV head) tile [0, L) in order
+    for (i, h), rs in dec_keys.items():
+        rs.sort()
+        assert rs[0][0] == 0 and rs[-1][1] == spec.seq_lens[i]
+        for (a0, b0, _), (a1, b1, _) in zip(rs, rs[1:]):
+            assert b0 == a1 and a1 % 256 == 0
+        ns = len(rs)
+        for k, (_, _, w) in enumerate(rs):
+            assert w["n_split"] == ns
+            if ns == 1:
+                assert w["part"] == -1 and w["pair"] == -1
+            else:
+                assert w["part"] == w["pair"] + k          # contiguous slots
+    # prefill: tiles of each (request, KV head) cover rows [0, q*G)
+    for (i, h), rs in rows.items():
+        rs.sort()
+        assert rs[0][0] == 0
+        assert sum(n for _, n in rs) == spec.q_lens[i] * G
+    assert sorted(slots) == list(range(parts))
+    # every (request, KV head) pair with tokens appears
+    seen = set(dec_keys) | set(rows)
+    assert len(seen) == sum(1 for q in spec.q_lens if q > 0) * spec.hkv
+
+
+def test_plan_orders_longest_first():
+    items, _, _ = _plan(workloads.config_spec(3))
+    dec = [w["k_end"] - w["k_begin"] for w in items if w["kind"] == 0]
+    pre = [w["k_end"] * w["n_rows"] for w in items if w["kind"] == 1]
+    assert dec == sorted(dec, reverse=True) and pre == sorted(pre, reverse=True)
+
+
+def test_plan_splits_fill_the_machine():
+    items, parts, _ = _plan(workloads.config_spec(1))
+    assert len(items) >= 4 * 152
+    items, parts, _ = _plan(workloads.config_spec(4))
+    assert len(items) >= 4 * 152 and parts <= 16384
+
+
+@pytest.mark.parametrize("qsl,lens,msg", [
+    ([1, 2], [5], "query_start_loc_host[0]"),
+    ([0, 3, 2], [5, 5], "decreases"),
+    ([0, 6], [5], "less than"),
+])
+def test_plan_rejects_bad_metadata(qsl, lens, msg):
+    cfg = pkv.make_config(8, 2, 16, 100, 4, 64)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.plan(cfg, np.asarray(qsl, np.int32), np.asarray(lens, np.int32))
+    assert e.value.status == 1 and msg in str(e.value)
+
+
+def test_plan_empty_and_zero_token_requests():
+    cfg = pkv.make_config(8, 2, 16, 100, 4, 64)
+    items, parts = pkv.plan(cfg, np.asarray([0, 0, 3], np.int32), np.asarray([7, 9], np.int32))
+    assert all(w["seq"] == 1 for w in items) and parts == 0
+    items, parts = pkv.plan(cfg, np.asarray([0], np.int32), np.asarray([], np.int32))
+    assert items == []

@@ -350,28 +350,36 @@ def host_pool(batch: Batch, which: str) -> np.ndarray:
     return bf16_bits(c)
 
 
-def subset(batch: Batch, seq_ids: list[int], k_cache=None, v_cache=None):
-    """Host inputs restricted to some sequences, for sampled oracle checks.
+def subset(batch: Batch, seq_ids: list[int], kv_heads: list[int] | None = None):
+    """Host inputs restricted to some sequences and KV heads, for sampled
+    oracle checks at full size.
 
     Returns a dict of numpy arrays: a compact pool holding only the blocks the
     chosen sequences reference (renumbered; attention does not depend on
-    physical ids), their block tables, lengths, queries and new K/V rows, and
-    the slots of those new rows in the compact pool.  ``k_cache``/``v_cache``
-    override the pools read (e.g. a copy taken before the append).
+    physical ids) and only the chosen KV heads, their block tables, lengths,
+    the query rows of those heads' groups, the new K/V rows, and the slots of
+    those new rows in the compact pool.  Call it before the append so the
+    pools still hold the generator's contents.  All query tokens of the
+    chosen sequences are kept (positions depend on the token count); pick
+    rows to evaluate with the oracle's ``rows`` argument.
     """
     spec = batch.spec
     bs = spec.block_size
-    kc = batch.k_cache if k_cache is None else k_cache
-    vc = batch.v_cache if v_cache is None else v_cache
+    G = spec.hq // spec.hkv
+    kvh = list(range(spec.hkv)) if kv_heads is None else list(kv_heads)
+    heads = [h * G + g for h in kvh for g in range(G)]
+    kc, vc = batch.k_cache, batch.v_cache
     ids = []
     for i in seq_ids:
         ids.extend(batch.block_tables[i, :cdiv(int(batch.seq_lens[i]), bs)].tolist())
     uniq = sorted(set(ids))
     remap = {b: j for j, b in enumerate(uniq)}
-    idx = torch.as_tensor(uniq, dtype=torch.int64, device=kc.device)
+    dev = kc.device
+    idx = torch.as_tensor(uniq, dtype=torch.int64, device=dev)
+    hidx = torch.as_tensor(kvh, dtype=torch.int64, device=dev)
 
     def take(c):
-        sub = c.index_select(0, idx)
+        sub = c.index_select(0, idx).index_select(1, hidx).contiguous()
         if sub.dtype == torch.uint8:
             return sub.cpu().numpy()
         return bf16_bits(sub)
@@ -388,20 +396,22 @@ def subset(batch: Batch, seq_ids: list[int], k_cache=None, v_cache=None):
         qsl.append(qsl[-1] + (b - a))
         for s in batch.slot_mapping[a:b].tolist():
             slots.append(remap[s // bs] * bs + s % bs)
-    tok_t = torch.as_tensor(tok, dtype=torch.int64, device=batch.q.device)
+    qt = torch.as_tensor(tok, dtype=torch.int64, device=batch.q.device)
+    hq_idx = torch.as_tensor(heads, dtype=torch.int64, device=batch.q.device)
     out = {
         "k_cache": take(kc), "v_cache": take(vc),
-        "block_tables": bt, "qsl": np.asarray(qsl, dtype=np.int32),
-        "seq_lens": batch.seq_lens[seq_ids].astype(np.int32),
-        "q": bf16_bits(batch.q.index_select(0, tok_t)),
-        "k_new": bf16_bits(batch.k_new.index_select(0, tok_t)),
-        "v_new": bf16_bits(batch.v_new.index_select(0, tok_t)),
+        "block_tables": bt, "seq_lens": batch.seq_lens[seq_ids].astype(np.int32),
+        "qsl": np.asarray(qsl, dtype=np.int32),
+        "q": bf16_bits(batch.q.index_select(0, qt).index_select(1, hq_idx)),
+        "k_new": bf16_bits(batch.k_new.index_select(0, qt).index_select(1, hidx)),
+        "v_new": bf16_bits(batch.v_new.index_select(0, qt).index_select(1, hidx)),
         "slot_mapping": np.asarray(slots, dtype=np.int64),
         "tokens": np.asarray(tok, dtype=np.int64),
+        "heads": np.asarray(heads, dtype=np.int64),
     }
     if batch.k_scale is not None:
-        out["k_scale"] = batch.k_scale.index_select(0, idx).cpu().numpy()
-        out["v_scale"] = batch.v_scale.index_select(0, idx).cpu().numpy()
+        out["k_scale"] = batch.k_scale.index_select(0, idx).index_select(1, hidx).cpu().numpy()
+        out["v_scale"] = batch.v_scale.index_select(0, idx).index_select(1, hidx).cpu().numpy()
     return out
 
 
