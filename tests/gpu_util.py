@@ -84,14 +84,24 @@ def gpu_rows(out: torch.Tensor, lse: torch.Tensor, sub: dict, rows=None):
     return o, l
 
 
-def check(got, ref, got_lse, ref_lse, kind: str = "bf16", what: str = ""):
+# Peaked variants (queries scaled x8, so a few keys dominate each softmax)
+# have outputs of order 1, where rounding the output to bf16 alone costs up
+# to 2^-9 |x| per element and rounding P to bf16 about as much again.  Their
+# mean-abs bound is therefore 1e-3 + 2^-8 * mean|ref| (derived, not given);
+# the five workloads keep the plain 1e-3.
+PEAKED_MEAN_REL = 2.0 ** -8
+
+
+def check(got, ref, got_lse, ref_lse, kind: str = "bf16", what: str = "",
+          peaked: bool = False):
     """Raise AssertionError unless got matches the oracle within TOL[kind]."""
     t = TOL[kind]
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     err = np.abs(got - ref)
     assert err.max() <= t["max_abs"], f"{what}: max-abs {err.max():.3e}"
-    assert err.mean() <= t["mean_abs"], f"{what}: mean-abs {err.mean():.3e}"
+    mean_bound = t["mean_abs"] + (PEAKED_MEAN_REL * np.abs(ref).mean() if peaked else 0.0)
+    assert err.mean() <= mean_bound, f"{what}: mean-abs {err.mean():.3e} > {mean_bound:.3e}"
     rel = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
     assert rel.max() <= t["rel"], f"{what}: row relative L2 {rel.max():.3e} at row {rel.argmax()}"
     if got_lse is not None:
@@ -102,10 +112,11 @@ def check(got, ref, got_lse, ref_lse, kind: str = "bf16", what: str = ""):
                 lse=float(np.abs(got_lse - ref_lse).max()) if got_lse is not None else None)
 
 
-def full_parity(batch: W.Batch, flags: int = pkv.FLAG_VALIDATE, what: str = ""):
+def full_parity(batch: W.Batch, flags: int = pkv.FLAG_VALIDATE, what: str = "",
+                peaked: bool = False):
     """Every row of a (small) batch against the oracle."""
     sub = W.subset(batch, list(range(batch.spec.num_seqs)))
     out, lse = gpu_step(batch, flags=flags)
     ref, ref_lse = oracle_subset(sub, batch.spec)
     got, got_lse = gpu_rows(out, lse, sub)
-    return check(got, ref, got_lse, ref_lse, batch.spec.kv_dtype, what)
+    return check(got, ref, got_lse, ref_lse, batch.spec.kv_dtype, what, peaked)
