@@ -220,7 +220,7 @@ enum {
 
 /*
  * With PKV_FLAG_TIMING, every kernel launch of the handle is bracketed by CUDA
- * events on its stream (the first 512 launches per kind since the last
+ * events on its stream (the first 4096 launches per kind since the last
  * reset are kept).
  * pkv_timing_read waits for those events and returns, per kind, the number
  * of launches recorded and their summed device time in milliseconds;

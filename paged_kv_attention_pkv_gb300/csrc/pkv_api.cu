@@ -20,7 +20,7 @@ using namespace pkv;
 
 namespace {
 
-constexpr int kTimingSlots = 512;
+constexpr int kTimingSlots = 4096;
 constexpr int kMaxPartials = 16384;        // split-KV partial slots
 constexpr int64_t kMaxPoolRows = (int64_t(1) << 31) - 4096;
 
