@@ -231,6 +231,48 @@ pkv_status pkv_timing_reset(pkv_handle *h);
 pkv_status pkv_timing_read(pkv_handle *h, int32_t kind, int32_t *launches,
                            double *total_ms);
 
+/* ---- decode without allocation ----------------------------------------------
+ *
+ * The pages describe nothing like this entry point; it exists for callers
+ * that cannot allocate GPU memory: an engine whose memory pool already owns
+ * all of HBM (the KV cache reservation), code that must not allocate after
+ * start-up, or code that cannot hold a handle (pkv_create allocates its
+ * workspace).
+ *
+ * pkv_decode_static runs the split-KV decode of pkv_attention_varlen for a
+ * batch in which every request has q_i * G <= 8 query rows, on the CURRENT
+ * CUDA device, without a handle.  The caller passes the inputs and outputs
+ * exactly as for pkv_attention_varlen (same layouts and meaning, minus the
+ * device copies of query_start_loc and seq_lens, which are not read) and a
+ * config describing the pools (max_num_seqs, max_num_tokens and flags are
+ * ignored).  Nothing is allocated: the work list, split partials and combine
+ * tickets live in one fixed array of about 4.3 MB compiled into the library,
+ * which every GPU that loads the library keeps until the process exits.
+ * Limits: at most 2048 work items and 1024 split partials per call (the split
+ * size grows to fit; a batch with more than 2048 (request, KV head) pairs is
+ * rejected with PKV_ERR_WORKSPACE).
+ *  - The first call on a device looks up the array's device address and sets
+ *    the kernel's shared-memory limit; make that first call before any stream
+ *    capture.
+ *  - Every call shares the array and leaves its contents behind; each call
+ *    clears what must start at zero.  Calls whose GPU work overlaps (on
+ *    different streams, or from different threads) race on it: serialise
+ *    them.
+ *  - Returns PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED (prefill rows,
+ *    head_dim or block_size not handled), PKV_ERR_WORKSPACE or PKV_ERR_CUDA.
+ *    It does not update pkv_last_error() and performs no device-side
+ *    validation.
+ */
+pkv_status pkv_decode_static(const pkv_config *config, const void *q,
+                             const void *k_cache, const void *v_cache,
+                             const float *k_scale, const float *v_scale,
+                             const int32_t *block_tables,
+                             int32_t block_table_stride,
+                             const int32_t *query_start_loc_host,
+                             const int32_t *seq_lens_host, int32_t num_seqs,
+                             int32_t num_tokens, void *out, float *lse,
+                             void *stream);
+
 #ifdef __cplusplus
 }
 #endif

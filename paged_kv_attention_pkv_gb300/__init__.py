@@ -30,7 +30,8 @@ KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL = 0, 1, 2
 # Every symbol include/pkv.h declares.
 EXPORTS = ["pkv_create", "pkv_write_slots", "pkv_attention_varlen",
            "pkv_check_device_errors", "pkv_status_string", "pkv_last_error",
-           "pkv_destroy", "pkv_plan", "pkv_timing_reset", "pkv_timing_read"]
+           "pkv_destroy", "pkv_plan", "pkv_timing_reset", "pkv_timing_read",
+           "pkv_decode_static"]
 
 
 class PkvError(RuntimeError):
@@ -92,6 +93,9 @@ def load(path: str | None = None):
     lib.pkv_timing_read.restype = ctypes.c_int
     lib.pkv_timing_read.argtypes = [vp, i32, ctypes.POINTER(i32),
                                     ctypes.POINTER(ctypes.c_double)]
+    lib.pkv_decode_static.restype = ctypes.c_int
+    lib.pkv_decode_static.argtypes = [ctypes.POINTER(Config), vp, vp, vp, vp, vp, vp,
+                                      i32, vp, vp, i32, i32, vp, vp, vp]
     if path is None:
         _lib = lib
     return lib
@@ -237,3 +241,25 @@ def plan(config: Config, query_start_loc_host, seq_lens_host, num_sms: int = 152
         raise PkvError(st, lib.pkv_last_error(None).decode())
     items = [{f: getattr(arr[i], f) for f, _ in WorkItem._fields_} for i in range(n.value)]
     return items, parts.value
+
+
+def decode_static(config: Config, q, k_cache, v_cache, block_tables,
+                  query_start_loc_host, seq_lens_host, out=None, lse=None,
+                  k_scale=None, v_scale=None, stream=None):
+    """pkv_decode_static: split-KV decode on the current device with no
+    handle and no allocation inside the library (its scratch is a fixed
+    array compiled into libpkv).  For callers that cannot allocate GPU memory
+    themselves; ``out`` must then be passed in.  Returns ``(out, lse)``."""
+    lib = load()
+    qslh = _host_i32(query_start_loc_host)
+    lenh = _host_i32(seq_lens_host)
+    if out is None:
+        out = torch.empty_like(q)
+    st = lib.pkv_decode_static(
+        ctypes.byref(config), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_tables), int(block_tables.shape[1]), _ptr(qslh),
+        _ptr(lenh), int(lenh.shape[0]), int(q.shape[0]), _ptr(out), _ptr(lse),
+        _stream(stream, q.device))
+    if st != PKV_OK:
+        raise PkvError(st, status_string(st))
+    return out, lse
