@@ -14,6 +14,7 @@
 namespace pkv {
 cudaError_t configure_decode();
 cudaError_t configure_prefill();
+cudaError_t configure_prefill_tc();
 }  // namespace pkv
 
 using namespace pkv;
@@ -201,15 +202,16 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
       }
     } else {
       const int rows = q * G;
+      const int tile = prefill_uses_tc(c) ? kPfRowsTc : kPfRows;
       for (int h = 0; h < H; ++h) {
-        for (int r0 = 0; r0 < rows; r0 += kPfRows) {
+        for (int r0 = 0; r0 < rows; r0 += tile) {
           pkv_work_item w{};
           w.kind = 1;
           w.seq = i;
           w.kv_head = h;
           w.tok0 = qsl[i];
           w.row0 = r0;
-          w.n_rows = std::min(kPfRows, rows - r0);
+          w.n_rows = std::min(tile, rows - r0);
           w.hist = hist;
           w.k_begin = 0;
           w.k_end = hist + (r0 + w.n_rows - 1) / G + 1;
@@ -227,9 +229,19 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
                    [&](const pkv_work_item &a, const pkv_work_item &b) {
                      return dec_cost(a) > dec_cost(b);
                    });
+  // Prefill tiles of one (request, KV head) read the same K/V stream: keep
+  // them adjacent so the CTAs running together share it through L2, and
+  // order the groups longest first.
   auto pre_cost = [](const pkv_work_item &w) { return int64_t(w.k_end) * w.n_rows; };
+  std::vector<int64_t> group_cost(size_t(B) * H, 0);
+  for (const auto &w : plan->pre) group_cost[size_t(w.seq) * H + w.kv_head] += pre_cost(w);
   std::stable_sort(plan->pre.begin(), plan->pre.end(),
                    [&](const pkv_work_item &a, const pkv_work_item &b) {
+                     const int64_t ga = group_cost[size_t(a.seq) * H + a.kv_head];
+                     const int64_t gb = group_cost[size_t(b.seq) * H + b.kv_head];
+                     if (ga != gb) return ga > gb;
+                     if (a.seq != b.seq) return a.seq < b.seq;
+                     if (a.kv_head != b.kv_head) return a.kv_head < b.kv_head;
                      return pre_cost(a) > pre_cost(b);
                    });
   *st = PKV_OK;
@@ -248,6 +260,22 @@ bool encode_pool_map(CUtensorMap *m, const void *base, bool fp8, int64_t rows,
   return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
              const_cast<void *>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Q viewed as [T][Hq][128] bf16 with boxes of {64 columns, G heads, 128/G
+// tokens}: one box is a 64-column half of a 128-row prefill tile with rows
+// r = t * G + g, 128-byte swizzled.
+bool encode_q_map(CUtensorMap *m, const void *q, int hq, int group, int64_t tokens) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(kHeadDim), cuuint64_t(hq), cuuint64_t(tokens)};
+  const cuuint64_t strides[2] = {cuuint64_t(kHeadDim * 2), cuuint64_t(hq) * kHeadDim * 2};
+  const cuuint32_t box[3] = {64, cuuint32_t(group), cuuint32_t(kPfRowsTc / group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -316,7 +344,8 @@ pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out) {
     g_create_error = "cuTensorMapEncodeTiled is not available from the driver";
     return PKV_ERR_CUDA;
   }
-  if ((e = configure_decode()) != cudaSuccess || (e = configure_prefill()) != cudaSuccess) {
+  if ((e = configure_decode()) != cudaSuccess || (e = configure_prefill()) != cudaSuccess ||
+      (e = configure_prefill_tc()) != cudaSuccess) {
     g_create_error = fmt("configuring kernels: %s", cudaGetErrorString(e));
     return PKV_ERR_CUDA;
   }
@@ -476,7 +505,7 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
   if (k_cache != h->map_k_ptr || v_cache != h->map_v_ptr) {
     const int64_t rows = c.num_blocks * c.num_kv_heads * bs;
     const int dec_box = std::min(bs, fp8 ? kDecKeysFp8 : kDecKeysBf16);
-    const int pf_box = std::min(bs, kPfKeys);
+    const int pf_box = std::min(bs, prefill_uses_tc(c) ? 128 : kPfKeys);
     bool ok = encode_pool_map(&h->dec_k, k_cache, fp8, rows, dec_box) &&
               encode_pool_map(&h->dec_v, v_cache, fp8, rows, dec_box);
     if (ok && !fp8)
@@ -576,8 +605,15 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
     p.num_blocks = c.num_blocks;
     p.scale_log2 = scale_log2;
     p.validate = validate;
+    CUtensorMap qmap;
+    const bool tc = prefill_uses_tc(c);
+    if (tc && !encode_q_map(&qmap, q, c.num_q_heads, G, num_tokens))
+      return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled rejected the query layout");
     timing_begin(h, PKV_KERNEL_PREFILL, s);
-    e = launch_prefill(h->pf_k, h->pf_v, p, static_cast<int>(plan.pre.size()), s);
+    if (tc)
+      e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, p, static_cast<int>(plan.pre.size()), s);
+    else
+      e = launch_prefill(h->pf_k, h->pf_v, p, static_cast<int>(plan.pre.size()), s);
     timing_end(h, PKV_KERNEL_PREFILL, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
   }

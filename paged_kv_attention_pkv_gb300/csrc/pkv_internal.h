@@ -111,7 +111,19 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
 cudaError_t launch_prefill(const CUtensorMap &kmap, const CUtensorMap &vmap,
                            const PrefillParams &p, int num_items,
                            cudaStream_t s);
+cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                              const CUtensorMap &vmap, const PrefillParams &p,
+                              int num_items, cudaStream_t s);
 cudaError_t launch_check(const CheckParams &p, cudaStream_t s);
+
+// Prefill tiles run on the tcgen05 kernel (128 rows) when the query group
+// size is a power of two (so a tile is a whole number of tokens) and the KV
+// pools are bf16; otherwise on the warp-MMA kernel (64 rows).
+constexpr int kPfRowsTc = 128;
+inline bool prefill_uses_tc(const pkv_config &c) {
+  const int G = c.num_q_heads / c.num_kv_heads;
+  return G > 0 && (G & (G - 1)) == 0 && G <= 128 && c.kv_dtype == PKV_KV_BF16;
+}
 cudaError_t configure_kernels();
 
 }  // namespace pkv

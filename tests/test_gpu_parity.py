@@ -74,6 +74,8 @@ SWEEP = [
     ("gqa8_bs64", 64, 8, 64, [1, 1, 2, 17, 1], [1, 64, 65, 1000, 4097], "bf16"),
     ("gqa2_bs32", 4, 2, 32, [3, 1, 31, 33], [3, 32, 95, 33], "bf16"),
     ("gqa4_bs128", 8, 2, 128, [2, 70], [129, 300], "bf16"),
+    ("gqa3_warpmma", 6, 2, 16, [1, 2, 3, 40, 22], [5, 100, 40, 300, 22], "bf16"),
+    ("gqa16_tc", 32, 2, 16, [1, 9, 200], [300, 1000, 4000], "bf16"),
     ("fp8_gqa8_bs64", 64, 8, 64, [1, 1, 1, 1], [1, 63, 65, 5000], "fp8"),
     ("fp8_gqa4_bs16", 32, 8, 16, [1, 2, 1], [17, 33, 2000], "fp8"),
 ]

@@ -67,8 +67,21 @@ def test_plan_covers_the_workloads(index):
 def test_plan_orders_longest_first():
     items, _, _ = _plan(workloads.config_spec(3))
     dec = [w["k_end"] - w["k_begin"] for w in items if w["kind"] == 0]
-    pre = [w["k_end"] * w["n_rows"] for w in items if w["kind"] == 1]
-    assert dec == sorted(dec, reverse=True) and pre == sorted(pre, reverse=True)
+    assert dec == sorted(dec, reverse=True)
+    # prefill tiles: grouped by (request, KV head), groups longest first,
+    # tiles longest first within a group
+    pre = [w for w in items if w["kind"] == 1]
+    groups = []
+    for w in pre:
+        key = (w["seq"], w["kv_head"])
+        if not groups or groups[-1][0] != key:
+            groups.append((key, []))
+        groups[-1][1].append(w["k_end"] * w["n_rows"])
+    assert len({g[0] for g in groups}) == len(groups)      # contiguous groups
+    totals = [sum(c) for _, c in groups]
+    assert totals == sorted(totals, reverse=True)
+    for _, c in groups:
+        assert c == sorted(c, reverse=True)
 
 
 def test_plan_splits_fill_the_machine():
