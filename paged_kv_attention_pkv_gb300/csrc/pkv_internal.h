@@ -62,6 +62,7 @@ struct DecodeParams {
 
 struct PrefillParams {
   const pkv_work_item *items;
+  int32_t paired;    // tcgen05 kernel: 16-token blocks in one 3D box each
   const __nv_bfloat16 *q;
   const int32_t *block_tables;
   int32_t bt_stride;
@@ -119,7 +120,8 @@ cudaError_t launch_check(const CheckParams &p, cudaStream_t s);
 // Prefill tiles run on the tcgen05 kernel (128 rows) when the query group
 // size is a power of two (so a tile is a whole number of tokens) and the KV
 // pools are bf16; otherwise on the warp-MMA kernel (64 rows).
-constexpr int kPfRowsTc = 128;
+constexpr int kPfRowsTc = 256;   // two 128-row Q tiles per item
+constexpr int kPfQTile = 128;
 inline bool prefill_uses_tc(const pkv_config &c) {
   const int G = c.num_q_heads / c.num_kv_heads;
   return G > 0 && (G & (G - 1)) == 0 && G <= 128 && c.kv_dtype == PKV_KV_BF16;
