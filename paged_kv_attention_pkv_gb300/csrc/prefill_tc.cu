@@ -28,7 +28,8 @@
 //               O_t += P_t V (V an MN-major shared-memory operand).  Work is
 //               signalled with tcgen05.commit on mbarriers.
 //   warps 0-3   softmax of Q tile 0, warps 4-7 of Q tile 1: thread r owns row
-//               r (TMEM lane r), masks causally on diagonal tiles, keeps a
+//               r (TMEM lane r), loads its 128 scores with one tcgen05.ld,
+//               masks causally on diagonal tiles, keeps a
 //               running max in log2 units that only moves when it grows by
 //               more than 8 (O is rescaled rarely), writes P, and finally
 //               normalises O.
@@ -73,16 +74,10 @@ __device__ __forceinline__ int paired_key(int c) {
   return ((c & 63) >> 3) * 16 + ((c >> 6) << 3) + (c & 7);
 }
 
-// 64 consecutive fp32 TMEM columns of this thread's lane (wait included).
+// 64 consecutive fp32 TMEM columns of this thread's lane (one load, wait
+// included).
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  float a[32], b[32];
-  tmem_ld32(taddr, a);
-  tmem_ld32(taddr + 32, b);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    v[i] = a[i];
-    v[32 + i] = b[i];
-  }
+  tmem_ld64x(taddr, v);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -309,28 +304,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_after();
       const int key0 = j * 128;
-      const bool diag = key0 + 127 > pos;
-      // pass 1: the tile's row max (two 64-column halves)
+      // one pass: the whole S row in registers (one TMEM load)
+      float s[128];
+      tmem_ld128(lane_addr + col_s, s);
+      if (key0 + 127 > pos) {   // diagonal tile: causal mask
+#pragma unroll
+        for (int k = 0; k < 128; ++k) {
+          const int key = key0 + (p.paired ? paired_key(k) : k);
+          s[k] = key > pos ? -CUDART_INF_F : s[k];
+        }
+      }
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = -CUDART_INF_F;
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float s[64];
-        tmem_ld64(lane_addr + col_s + 64 * hh, s);
-        if (diag) {
+      for (int k = 8; k < 128; k += 8)
 #pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const int col = 64 * hh + k;
-            const int key = key0 + (p.paired ? paired_key(col) : col);
-            if (key > pos) s[k] = -CUDART_INF_F;
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < 64; k += 8)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[k + i]);
-      }
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[k + i]);
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float mt2 = mt * c;
@@ -341,26 +331,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         rescale = j > 0;
         m = mt2;
       }
-      // pass 2: P = 2^(s c - m) as bf16 pairs over the S columns.  Half 0 of
-      // P (columns 0-31) only overwrites S columns 0-63, already read.
+      // P = 2^(s c - m) as bf16 pairs over the S columns, in two 64-column
+      // chunks (chunk 0's P lands on S columns 0-31, already in registers)
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        float s[64];
-        tmem_ld64(lane_addr + col_s + 64 * hh, s);
-        if (diag) {
-#pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const int col = 64 * hh + k;
-            const int key = key0 + (p.paired ? paired_key(col) : col);
-            if (key > pos) s[k] = -CUDART_INF_F;
-          }
-        }
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float e0 = ex2(fmaf(s[2 * k], c, -m));
-          const float e1 = ex2(fmaf(s[2 * k + 1], c, -m));
+          const float e0 = ex2(fmaf(s[64 * hh + 2 * k], c, -m));
+          const float e1 = ex2(fmaf(s[64 * hh + 2 * k + 1], c, -m));
           acc[(2 * k) & 7] += e0;
           acc[(2 * k + 1) & 7] += e1;
           pk[k] = pack_bf16(e0, e1);
@@ -379,20 +359,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
+        tmem_ld128(lane_addr + col_o, s);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float o[64];
-          tmem_ld64(lane_addr + col_o + 64 * hh, o);
-          float a[32], b[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            a[i] = o[i] * alpha;
-            b[i] = o[32 + i] * alpha;
-          }
-          tmem_st32(lane_addr + col_o + 64 * hh, a);
-          tmem_st32(lane_addr + col_o + 64 * hh + 32, b);
-        }
-        tmem_wait_st();
+        for (int i = 0; i < 128; ++i) s[i] *= alpha;
+        tmem_st128(lane_addr + col_o, s);
       }
       // The last K/V tile may carry V rows past the item's last key (rows
       // of other requests or never loaded): zero them before any PV reads
