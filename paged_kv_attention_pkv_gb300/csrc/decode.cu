@@ -16,8 +16,11 @@
 // memory.  Lane 0 fills a stage with 2D TMA tile copies of the (block, KV
 // head) rows of K and V, 128-byte swizzled, completing on an mbarrier; the
 // warp's lanes read it with conflict-free ldmatrix / ld.shared patterns.
-// E4M3 pools are dequantised in registers (exact bit placement into bf16, the
-// per-block scale folded into the fp32 scores and into P).
+// E4M3 pools: QK runs on FP8 MMAs over the stored K codes with the query
+// split into two E4M3 parts (about bf16 precision); V codes are paired per
+// head-dim column with byte permutes and converted exactly to f16 in
+// hardware, PV runs in f16 with V's per-block scale folded into P.  K's
+// per-block scale is folded into the fp32 scores.
 #include <math_constants.h>
 
 #include "pkv_device.cuh"
@@ -130,15 +133,68 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2)
   const int group = p.group;
   const bool col_ok = g < it.n_rows;
   uint32_t qf[8][2];
-  {
+  // E4M3 pools: QK runs on FP8 MMAs over the stored K codes.  Each query
+  // column is scaled by a power of two sq (max |q sq| <= 448) and split into
+  // q sq = hi + lo, both E4M3 (about bf16 precision); 1/sq is folded into
+  // the score scale of that column.
+  float inv_sq0 = 1.f, inv_sq1 = 1.f;
+  if constexpr (FP8) {
+    const int r = it.row0 + g;
+    const __nv_bfloat16 *qrow =
+        p.q + (static_cast<int64_t>(it.tok0 + r / group) * p.hq +
+               it.kv_head * group + r % group) * kHeadDim + 32 * t;
+    float qv[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (col_ok) w = __ldg(reinterpret_cast<const uint4 *>(qrow) + i);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        qv[8 * i + 2 * k] = __uint_as_float(ww[k] << 16);
+        qv[8 * i + 2 * k + 1] = __uint_as_float(ww[k] & 0xFFFF0000u);
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qv[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float sq = amax > 0.f ? exp2f(floorf(log2f(448.f / amax))) : 1.f;
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint32_t hcode[2], lcode[2];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const float x0 = qv[4 * k + 2 * h2] * sq, x1 = qv[4 * k + 2 * h2 + 1] * sq;
+        hcode[h2] = e4m3x2_from_f32(x0, x1);
+        const float2 back = e4m3x2_to_f32(hcode[h2]);
+        lcode[h2] = e4m3x2_from_f32(x0 - back.x, x1 - back.y);
+      }
+      hw[k] = hcode[0] | (hcode[1] << 16);
+      lw[k] = lcode[0] | (lcode[1] << 16);
+    }
+    // step s (32 head-dim values): b0 = word 4(s>>1) + 2(s&1), b1 = next
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+      const int w0 = 4 * (st >> 1) + 2 * (st & 1);
+      qf[st][0] = hw[w0];
+      qf[st][1] = hw[w0 + 1];
+      qf[4 + st][0] = lw[w0];
+      qf[4 + st][1] = lw[w0 + 1];
+    }
+    const float inv = 1.f / sq;
+    inv_sq0 = __shfl_sync(0xffffffffu, inv, (2 * t) * 4);
+    inv_sq1 = __shfl_sync(0xffffffffu, inv, (2 * t + 1) * 4);
+  } else {
     const int r = it.row0 + g;
     const __nv_bfloat16 *qrow =
         p.q + (static_cast<int64_t>(it.tok0 + r / group) * p.hq +
                it.kv_head * group + r % group) * kHeadDim;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const int d0 = FP8 ? 32 * t + 4 * ks
-                         : 64 * (ks >> 2) + 16 * t + 8 * ((ks >> 1) & 1) + 4 * (ks & 1);
+      const int d0 = 64 * (ks >> 2) + 16 * t + 8 * ((ks >> 1) & 1) + 4 * (ks & 1);
       uint2 v = make_uint2(0u, 0u);
       if (col_ok) v = __ldg(reinterpret_cast<const uint2 *>(qrow + d0));
       qf[ks][0] = v.x;
@@ -175,22 +231,16 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2)
       // ---- S^T = K Q^T for 16 keys x 8 columns
       float s[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (FP8) {
+        // raw K codes straight into FP8 MMAs: thread t's 16 bytes of a row
+        // are steps 2h, 2h+1 (words 0,1 -> a0,a2 of step 2h; 2,3 of 2h+1)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint4 x = lds128(kbase + swz128(16 * sub + g, 2 * t + h));
           const uint4 y = lds128(kbase + swz128(16 * sub + g + 8, 2 * t + h));
-          const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-          const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int ks = 4 * h + w;
-            mma_bf16(s,
-                     e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(xw[w], 0, 0x1100)),
-                     e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(yw[w], 0, 0x1100)),
-                     e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(xw[w], 0, 0x3322)),
-                     e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(yw[w], 0, 0x3322)),
-                     qf[ks][0], qf[ks][1]);
-          }
+          mma_e4m3(s, x.x, y.x, x.y, y.y, qf[2 * h][0], qf[2 * h][1]);
+          mma_e4m3(s, x.x, y.x, x.y, y.y, qf[4 + 2 * h][0], qf[4 + 2 * h][1]);
+          mma_e4m3(s, x.z, y.z, x.w, y.w, qf[2 * h + 1][0], qf[2 * h + 1][1]);
+          mma_e4m3(s, x.z, y.z, x.w, y.w, qf[4 + 2 * h + 1][0], qf[4 + 2 * h + 1][1]);
         }
       } else {
 #pragma unroll
@@ -204,7 +254,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2)
         }
       }
       // ---- scale, mask, online softmax per column
-      float sc = p.scale_log2;
+      float sc0 = p.scale_log2, sc1 = p.scale_log2;
       float pv_scale = 1.f;
       if constexpr (FP8) {
         const int32_t blk = __ldg(bt + k16 / p.bs);
@@ -214,14 +264,15 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2)
           sk = __ldg(p.k_scale + si);
           sv = __ldg(p.v_scale + si);
         }
-        sc *= sk * kE4M3BitScale;
-        pv_scale = sv * kE4M3BitScale;
+        sc0 *= sk * inv_sq0;
+        sc1 *= sk * inv_sq1;
+        pv_scale = sv;
       }
       const int kr0 = k16 + g, kr1 = k16 + g + 8;
-      s[0] = (kr0 < ke && kr0 <= pos0) ? s[0] * sc : -CUDART_INF_F;
-      s[1] = (kr0 < ke && kr0 <= pos1) ? s[1] * sc : -CUDART_INF_F;
-      s[2] = (kr1 < ke && kr1 <= pos0) ? s[2] * sc : -CUDART_INF_F;
-      s[3] = (kr1 < ke && kr1 <= pos1) ? s[3] * sc : -CUDART_INF_F;
+      s[0] = (kr0 < ke && kr0 <= pos0) ? s[0] * sc0 : -CUDART_INF_F;
+      s[1] = (kr0 < ke && kr0 <= pos1) ? s[1] * sc1 : -CUDART_INF_F;
+      s[2] = (kr1 < ke && kr1 <= pos0) ? s[2] * sc0 : -CUDART_INF_F;
+      s[3] = (kr1 < ke && kr1 <= pos1) ? s[3] * sc1 : -CUDART_INF_F;
       float tm0 = fmaxf(s[0], s[2]);
       float tm1 = fmaxf(s[1], s[3]);
 #pragma unroll
@@ -247,8 +298,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2)
         acc[mt][3] *= al1;
       }
       // ---- P^T as the B operand: transpose the two 8x8 halves in registers
-      const uint32_t b0 = movmatrix_trans(pack_bf16(p0 * pv_scale, p1 * pv_scale));
-      const uint32_t b1 = movmatrix_trans(pack_bf16(p2 * pv_scale, p3 * pv_scale));
+      // (f16 for E4M3 pools, whose V is unpacked to f16; bf16 otherwise)
+      const uint32_t b0 = movmatrix_trans(FP8 ? pack_f16(p0 * pv_scale, p1 * pv_scale)
+                                              : pack_bf16(p0 * pv_scale, p1 * pv_scale));
+      const uint32_t b1 = movmatrix_trans(FP8 ? pack_f16(p2 * pv_scale, p3 * pv_scale)
+                                              : pack_bf16(p2 * pv_scale, p3 * pv_scale));
       // keys of this thread's V^T fragment halves
       const bool tail = k16 + 16 > ke;
       const int ka = k16 + 2 * t;
@@ -267,18 +321,16 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2)
           const uint32_t wB = lds32(vbase + swz128(kA + 1, ch) + bo);
           const uint32_t wC = lds32(vbase + swz128(kA + 8, ch) + bo);
           const uint32_t wD = lds32(vbase + swz128(kA + 9, ch) + bo);
-          mma_bf16(acc[2 * j],
-                   mlo & e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(wA, wB, 0x4400)),
-                   mlo & e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(wA, wB, 0x5511)),
-                   mhi & e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(wC, wD, 0x4400)),
-                   mhi & e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(wC, wD, 0x5511)),
-                   b0, b1);
-          mma_bf16(acc[2 * j + 1],
-                   mlo & e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(wA, wB, 0x6622)),
-                   mlo & e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(wA, wB, 0x7733)),
-                   mhi & e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(wC, wD, 0x6622)),
-                   mhi & e4m3x2_lanes13_to_bf16x2_scaled(__byte_perm(wC, wD, 0x7733)),
-                   b0, b1);
+          // pair the two keys' bytes per head-dim column, then convert
+          // in hardware: [A0 B0 A1 B1] and [A2 B2 A3 B3]
+          const uint32_t x01 = __byte_perm(wA, wB, 0x5140);
+          const uint32_t x23 = __byte_perm(wA, wB, 0x7362);
+          const uint32_t y01 = __byte_perm(wC, wD, 0x5140);
+          const uint32_t y23 = __byte_perm(wC, wD, 0x7362);
+          mma_f16(acc[2 * j], mlo & e4m3x2lo_to_f16x2(x01), mlo & e4m3x2hi_to_f16x2(x01),
+                  mhi & e4m3x2lo_to_f16x2(y01), mhi & e4m3x2hi_to_f16x2(y01), b0, b1);
+          mma_f16(acc[2 * j + 1], mlo & e4m3x2lo_to_f16x2(x23), mlo & e4m3x2hi_to_f16x2(x23),
+                  mhi & e4m3x2lo_to_f16x2(y23), mhi & e4m3x2hi_to_f16x2(y23), b0, b1);
         }
       } else {
         const int mi = lane >> 3;
