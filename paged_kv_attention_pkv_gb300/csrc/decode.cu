@@ -60,12 +60,13 @@ __device__ __forceinline__ int fp8_dmap(int mt, int dr) {
 }
 
 template <bool FP8>
-__global__ void __launch_bounds__(kDecWarps * 32, 2)
+__global__ void __launch_bounds__(kDecWarps * 32, FP8 ? 3 : 2)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p) {
   using Tile = DecTile<FP8>;
   constexpr int KS = Tile::kKeys;
+  constexpr int kDecStages = FP8 ? kDecStagesFp8 : pkv::kDecStages;  // ring depth
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -453,7 +454,7 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
                           cudaStream_t s) {
   if (num_items == 0) return cudaSuccess;
   if (fp8)
-    decode_kernel<true><<<num_items, kDecWarps * 32, kDecSmemBytes, s>>>(kmap, vmap, p);
+    decode_kernel<true><<<num_items, kDecWarps * 32, kDecSmemBytesFp8, s>>>(kmap, vmap, p);
   else
     decode_kernel<false><<<num_items, kDecWarps * 32, kDecSmemBytes, s>>>(kmap, vmap, p);
   return cudaGetLastError();
@@ -462,7 +463,7 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
 cudaError_t configure_decode() {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kDecSmemBytes);
+                                       kDecSmemBytesFp8);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(decode_kernel<false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,

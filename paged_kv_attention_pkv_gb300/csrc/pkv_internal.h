@@ -31,6 +31,11 @@ constexpr int kDecKeysBf16 = 16;          // keys per stage, bf16 pools
 constexpr int kDecKeysFp8 = 32;           // keys per stage, E4M3 pools
 constexpr int kDecSmemBytes =
     kDecWarps * kDecStages * kDecStageBytes + 1024 /* align */ + 256;
+// E4M3 pools: shorter rings and three CTAs per SM (same bytes in flight, more
+// warps to hide the latency of the longer per-key instruction stream).
+constexpr int kDecStagesFp8 = 2;
+constexpr int kDecSmemBytesFp8 =
+    kDecWarps * kDecStagesFp8 * kDecStageBytes + 1024 + 256;
 constexpr int kSplitAlign = 256;          // split ranges start at multiples
 
 // ---- prefill kernel geometry ---------------------------------------------------
