@@ -191,13 +191,14 @@ def device_meta(batch):
 
 
 def time_workload(index, steps: int, warmup: int, world: int, peaks: dict,
-                  device: str, sampler: ClockSampler | None = None, e2e: bool = False):
+                  device: str, sampler: ClockSampler | None = None, e2e: bool = False,
+                  separate: bool = False):
     import paged_kv_attention_pkv_gb300 as pkv
 
     spec = W.config_spec(index) if isinstance(index, int) else index
     batch = W.generate(spec, device)
     work = W.algorithmic_work(spec)
-    h = make_handle(batch, pkv.FLAG_TIMING)
+    h = make_handle(batch, pkv.FLAG_TIMING | (pkv.FLAG_SEPARATE if separate else 0))
     m = device_meta(batch)
     out = torch.empty_like(batch.q)
     stream = torch.cuda.current_stream()
@@ -233,11 +234,14 @@ def time_workload(index, steps: int, warmup: int, world: int, peaks: dict,
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     per_kind = {}
     for kind, name in ((pkv.KERNEL_APPEND, "append"), (pkv.KERNEL_DECODE, "decode"),
-                       (pkv.KERNEL_PREFILL, "prefill")):
+                       (pkv.KERNEL_PREFILL, "prefill"), (pkv.KERNEL_MIXED, "mixed")):
         n, tot = h.timing_read(kind)
         if n:
             per_kind[name] = (n, tot / n)
-    launches_per_step = (1 + (work["num_decode"] > 0) + (work["num_prefill"] > 0))
+    # every step launches each kind it uses once (the timing ring keeps the
+    # first 4096 launches of each kind)
+    assert all(n == min(steps, 4096) for n, _ in per_kind.values()), per_kind
+    launches_per_step = len(per_kind)
     res = {"spec": spec, "work": work, "ms": ms, "steps": steps, "kinds": per_kind,
            "gpu_launches": launches_per_step * steps, "wall": (w0, w1)}
     if e2e:
@@ -389,6 +393,20 @@ def secondary(args, world, peaks, device):
         ms_step = r["ms"] / steps
         ent = {"workload": spec.name, "ms_per_step": round(ms_step, 4),
                "kernel_ms": {k: round(v[1], 4) for k, v in r["kinds"].items()}}
+        if "mixed" in r["kinds"]:
+            # one launch for both kinds; the per-kind figures below come from
+            # the same step run as separate decode and prefill launches
+            n, avg = r["kinds"]["mixed"]
+            t_ideal = (work["decode_bytes"] / (peaks["hbm_gbs"] * 1e9) +
+                       work["prefill_flops"] / (peaks["bf16_tflops"] * 1e12))
+            ent["mixed"] = {"kernel_ms": round(avg, 4),
+                            "roofline_frac": round(t_ideal / (avg * 1e-3), 4),
+                            "note": "ideal time (decode bytes at HBM peak + prefill "
+                                    "flops at bf16 peak) / mixed-launch time"}
+            r = time_workload(idx, steps, 3, world, peaks, device, separate=True)
+            ent["separate"] = {"ms_per_step": round(r["ms"] / steps, 4),
+                               "kernel_ms": {k: round(v[1], 4)
+                                             for k, v in r["kinds"].items()}}
         if work["prefill_flops"]:
             n, avg = r["kinds"]["prefill"]
             tf = work["prefill_flops"] / (avg * 1e-3) / 1e12

@@ -77,7 +77,9 @@ typedef enum {
 
 enum {
     PKV_FLAG_VALIDATE = 1u,    /* device-side checks of block ids and slots */
-    PKV_FLAG_TIMING = 2u       /* record CUDA events around every kernel */
+    PKV_FLAG_TIMING = 2u,      /* record CUDA events around every kernel */
+    PKV_FLAG_SEPARATE = 4u     /* run a mixed step as separate decode and
+                                  prefill launches (per-kind timing) */
 };
 
 /* Fixed shape of a KV cache and the largest step a handle serves. */
@@ -210,12 +212,15 @@ pkv_status pkv_plan(const pkv_config *config, const int32_t *query_start_loc_hos
                     pkv_work_item *items, int32_t max_items,
                     int32_t *num_items, int32_t *num_partials);
 
-/* Kernel kinds reported by pkv_timing_read. */
+/* Kernel kinds reported by pkv_timing_read.  A step holding both decodes
+ * and prefill chunks (bf16 pools, query groups of power-of-two size) runs as
+ * one PKV_KERNEL_MIXED launch; otherwise decode and prefill launch apart. */
 enum {
     PKV_KERNEL_APPEND = 0,
     PKV_KERNEL_DECODE = 1,
     PKV_KERNEL_PREFILL = 2,
-    PKV_KERNEL_KINDS = 3
+    PKV_KERNEL_MIXED = 3,
+    PKV_KERNEL_KINDS = 4
 };
 
 /*

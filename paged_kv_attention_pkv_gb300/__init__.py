@@ -24,8 +24,8 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                 5: "PKV_ERR_DEVICE_CHECK", 6: "PKV_ERR_TIMEOUT",
                 7: "PKV_ERR_WORKSPACE"}
 KV_BF16, KV_FP8_E4M3 = 0, 1
-FLAG_VALIDATE, FLAG_TIMING = 1, 2
-KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL = 0, 1, 2
+FLAG_VALIDATE, FLAG_TIMING, FLAG_SEPARATE = 1, 2, 4
+KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL, KERNEL_MIXED = 0, 1, 2, 3
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ["pkv_create", "pkv_write_slots", "pkv_attention_varlen",

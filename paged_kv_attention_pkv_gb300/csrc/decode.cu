@@ -21,430 +21,20 @@
 // head-dim column with byte permutes and converted exactly to f16 in
 // hardware, PV runs in f16 with V's per-block scale folded into P.  K's
 // per-block scale is folded into the fp32 scores.
-#include <math_constants.h>
-
-#include "pkv_device.cuh"
+#include "decode_body.cuh"
 
 namespace pkv {
 namespace {
-
-constexpr float kLn2 = 0.6931471805599453f;
-
-template <bool FP8>
-struct DecTile {
-  static constexpr int kKeys = FP8 ? kDecKeysFp8 : kDecKeysBf16;  // per stage
-  static constexpr int kSubs = kKeys / 16;
-  static constexpr int kKBytes = kKeys * kHeadDim * (FP8 ? 1 : 2);  // 4096
-  static_assert(kKBytes * 2 == kDecStageBytes, "stage layout");
-};
-
-// Row of the pool maps holding key `key` of KV head `kvh` of a request, or
-// rows_total (entirely outside the map: TMA fills zeros) for a bad block id.
-__device__ __forceinline__ int32_t pool_row(const int32_t *bt, int32_t key,
-                                            int32_t kvh, const DecodeParams &p,
-                                            int32_t *blk_out) {
-  const int32_t blk = __ldg(bt + key / p.bs);
-  *blk_out = blk;
-  if (blk < 0 || blk >= p.num_blocks) {
-    record_error(p.err, kErrBadBlock);
-    return p.rows_total;
-  }
-  return (blk * p.hkv + kvh) * p.bs + key % p.bs;
-}
-
-// Physical head-dim index of a row of the O^T accumulator in the E4M3 path
-// (row dr of m-tile mt): the V fragments are built from 4-byte words, so each
-// thread's 4 consecutive bytes feed rows (g, g+8) of two adjacent m-tiles.
-__device__ __forceinline__ int fp8_dmap(int mt, int dr) {
-  return 4 * ((dr & 7) + 8 * (mt >> 1)) + 2 * (mt & 1) + (dr >> 3);
-}
 
 template <bool FP8>
 __global__ void __launch_bounds__(kDecWarps * 32, FP8 ? 3 : 2)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p) {
-  using Tile = DecTile<FP8>;
-  constexpr int KS = Tile::kKeys;
-  constexpr int kDecStages = FP8 ? kDecStagesFp8 : pkv::kDecStages;  // ring depth
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(
-      smem + kDecWarps * kDecStages * kDecStageBytes);
-  int32_t *flag = reinterpret_cast<int32_t *>(bars + kDecWarps * kDecStages);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int g = lane >> 2;
-  const int t = lane & 3;
-  const pkv_work_item it = p.items[blockIdx.x];
-
-  if (threadIdx.x < kDecWarps * kDecStages) mbar_init(&bars[threadIdx.x], 1);
-  if (threadIdx.x == 0) {
-    prefetch_tmap(&kmap);
-    prefetch_tmap(&vmap);
-  }
-  fence_mbar_init();
-  __syncthreads();
-
-  const int kb = it.k_begin;
-  const int ke = it.k_end;
-  const int n_total = (ke - kb + KS - 1) / KS;
-  const int my_n = n_total > warp ? (n_total - warp + kDecWarps - 1) / kDecWarps : 0;
-  uint8_t *ring = smem + warp * kDecStages * kDecStageBytes;
-  uint64_t *full = bars + warp * kDecStages;
-  const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
-  const int br = p.bs < KS ? p.bs : KS;  // rows per TMA box
-
-  // Fill ring slot for this warp's i-th stage (lane 0 only).
-  auto issue = [&](int i) {
-    const int key0 = kb + (warp + i * kDecWarps) * KS;
-    const int slot = i % kDecStages;
-    uint8_t *kdst = ring + slot * kDecStageBytes;
-    uint8_t *vdst = kdst + Tile::kKBytes;
-    int boxes = 0;
-    for (int r = 0; r < KS; r += br)
-      if (key0 + r < ke) ++boxes;
-    mbar_arrive_expect_tx(&full[slot], boxes * br * 128 * 2 * (FP8 ? 1 : 2));
-    for (int r = 0; r < KS; r += br) {
-      const int key = key0 + r;
-      if (key >= ke) break;
-      int32_t blk;
-      const int32_t y = pool_row(bt, key, it.kv_head, p, &blk);
-      if constexpr (FP8) {
-        tma_load_2d(kdst + r * 128, &kmap, 0, y, &full[slot]);
-        tma_load_2d(vdst + r * 128, &vmap, 0, y, &full[slot]);
-      } else {
-        tma_load_2d(kdst + r * 128, &kmap, 0, y, &full[slot]);
-        tma_load_2d(kdst + KS * 128 + r * 128, &kmap, 64, y, &full[slot]);
-        tma_load_2d(vdst + r * 128, &vmap, 0, y, &full[slot]);
-        tma_load_2d(vdst + KS * 128 + r * 128, &vmap, 64, y, &full[slot]);
-      }
-    }
-  };
-
-  if (lane == 0) {
-    const int pre = my_n < kDecStages ? my_n : kDecStages;
-    for (int i = 0; i < pre; ++i) issue(i);
-  }
-
-  // Query fragments (B operand, column n = g) with the head-dim order that
-  // matches how this thread reads K rows.
-  const int group = p.group;
-  const bool col_ok = g < it.n_rows;
-  uint32_t qf[8][2];
-  // E4M3 pools: QK runs on FP8 MMAs over the stored K codes.  Each query
-  // column is scaled by a power of two sq (max |q sq| <= 448) and split into
-  // q sq = hi + lo, both E4M3 (about bf16 precision); 1/sq is folded into
-  // the score scale of that column.
-  float inv_sq0 = 1.f, inv_sq1 = 1.f;
-  if constexpr (FP8) {
-    const int r = it.row0 + g;
-    const __nv_bfloat16 *qrow =
-        p.q + (static_cast<int64_t>(it.tok0 + r / group) * p.hq +
-               it.kv_head * group + r % group) * kHeadDim + 32 * t;
-    float qv[32];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (col_ok) w = __ldg(reinterpret_cast<const uint4 *>(qrow) + i);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        qv[8 * i + 2 * k] = __uint_as_float(ww[k] << 16);
-        qv[8 * i + 2 * k + 1] = __uint_as_float(ww[k] & 0xFFFF0000u);
-      }
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qv[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const float sq = amax > 0.f ? exp2f(floorf(log2f(448.f / amax))) : 1.f;
-    uint32_t hw[8], lw[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      uint32_t hcode[2], lcode[2];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const float x0 = qv[4 * k + 2 * h2] * sq, x1 = qv[4 * k + 2 * h2 + 1] * sq;
-        hcode[h2] = e4m3x2_from_f32(x0, x1);
-        const float2 back = e4m3x2_to_f32(hcode[h2]);
-        lcode[h2] = e4m3x2_from_f32(x0 - back.x, x1 - back.y);
-      }
-      hw[k] = hcode[0] | (hcode[1] << 16);
-      lw[k] = lcode[0] | (lcode[1] << 16);
-    }
-    // step s (32 head-dim values): b0 = word 4(s>>1) + 2(s&1), b1 = next
-#pragma unroll
-    for (int st = 0; st < 4; ++st) {
-      const int w0 = 4 * (st >> 1) + 2 * (st & 1);
-      qf[st][0] = hw[w0];
-      qf[st][1] = hw[w0 + 1];
-      qf[4 + st][0] = lw[w0];
-      qf[4 + st][1] = lw[w0 + 1];
-    }
-    const float inv = 1.f / sq;
-    inv_sq0 = __shfl_sync(0xffffffffu, inv, (2 * t) * 4);
-    inv_sq1 = __shfl_sync(0xffffffffu, inv, (2 * t + 1) * 4);
-  } else {
-    const int r = it.row0 + g;
-    const __nv_bfloat16 *qrow =
-        p.q + (static_cast<int64_t>(it.tok0 + r / group) * p.hq +
-               it.kv_head * group + r % group) * kHeadDim;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int d0 = 64 * (ks >> 2) + 16 * t + 8 * ((ks >> 1) & 1) + 4 * (ks & 1);
-      uint2 v = make_uint2(0u, 0u);
-      if (col_ok) v = __ldg(reinterpret_cast<const uint2 *>(qrow + d0));
-      qf[ks][0] = v.x;
-      qf[ks][1] = v.y;
-    }
-  }
-  // causal limit of this thread's two columns (2t, 2t+1)
-  const int c0 = it.row0 + 2 * t;
-  const int pos0 = (2 * t < it.n_rows) ? it.hist + c0 / group : 0x7fffffff;
-  const int pos1 = (2 * t + 1 < it.n_rows) ? it.hist + (c0 + 1) / group : 0x7fffffff;
-
-  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
-  float acc[8][4];
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
-    acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-
-  int consumed = 0;
-  bool timed_out = false;
-  for (int i = 0; i < my_n; ++i) {
-    const int slot = i % kDecStages;
-    const bool ok = mbar_wait(&full[slot], (i / kDecStages) & 1);
-    if (!__all_sync(0xffffffffu, ok)) {  // warp-uniform way out
-      timed_out = true;
-      break;
-    }
-    const int key0 = kb + (warp + i * kDecWarps) * KS;
-    const uint32_t kbase = smem_addr(ring + slot * kDecStageBytes);
-    const uint32_t vbase = kbase + Tile::kKBytes;
-#pragma unroll
-    for (int sub = 0; sub < Tile::kSubs; ++sub) {
-      const int k16 = key0 + 16 * sub;
-      if (k16 >= ke) break;
-      // ---- S^T = K Q^T for 16 keys x 8 columns
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (FP8) {
-        // raw K codes straight into FP8 MMAs: thread t's 16 bytes of a row
-        // are steps 2h, 2h+1 (words 0,1 -> a0,a2 of step 2h; 2,3 of 2h+1)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint4 x = lds128(kbase + swz128(16 * sub + g, 2 * t + h));
-          const uint4 y = lds128(kbase + swz128(16 * sub + g + 8, 2 * t + h));
-          mma_e4m3(s, x.x, y.x, x.y, y.y, qf[2 * h][0], qf[2 * h][1]);
-          mma_e4m3(s, x.x, y.x, x.y, y.y, qf[4 + 2 * h][0], qf[4 + 2 * h][1]);
-          mma_e4m3(s, x.z, y.z, x.w, y.w, qf[2 * h + 1][0], qf[2 * h + 1][1]);
-          mma_e4m3(s, x.z, y.z, x.w, y.w, qf[4 + 2 * h + 1][0], qf[4 + 2 * h + 1][1]);
-        }
-      } else {
-#pragma unroll
-        for (int L = 0; L < 4; ++L) {
-          const uint32_t off = (L >> 1) * (KS * 128);
-          const uint32_t ch = 2 * t + (L & 1);
-          const uint4 x = lds128(kbase + off + swz128(g, ch));
-          const uint4 y = lds128(kbase + off + swz128(g + 8, ch));
-          mma_bf16(s, x.x, y.x, x.y, y.y, qf[2 * L][0], qf[2 * L][1]);
-          mma_bf16(s, x.z, y.z, x.w, y.w, qf[2 * L + 1][0], qf[2 * L + 1][1]);
-        }
-      }
-      // ---- scale, mask, online softmax per column
-      float sc0 = p.scale_log2, sc1 = p.scale_log2;
-      float pv_scale = 1.f;
-      if constexpr (FP8) {
-        const int32_t blk = __ldg(bt + k16 / p.bs);
-        float sk = 0.f, sv = 0.f;
-        if (blk >= 0 && blk < p.num_blocks) {
-          const int64_t si = static_cast<int64_t>(blk) * p.hkv + it.kv_head;
-          sk = __ldg(p.k_scale + si);
-          sv = __ldg(p.v_scale + si);
-        }
-        sc0 *= sk * inv_sq0;
-        sc1 *= sk * inv_sq1;
-        pv_scale = sv;
-      }
-      const int kr0 = k16 + g, kr1 = k16 + g + 8;
-      s[0] = (kr0 < ke && kr0 <= pos0) ? s[0] * sc0 : -CUDART_INF_F;
-      s[1] = (kr0 < ke && kr0 <= pos1) ? s[1] * sc1 : -CUDART_INF_F;
-      s[2] = (kr1 < ke && kr1 <= pos0) ? s[2] * sc0 : -CUDART_INF_F;
-      s[3] = (kr1 < ke && kr1 <= pos1) ? s[3] * sc1 : -CUDART_INF_F;
-      float tm0 = fmaxf(s[0], s[2]);
-      float tm1 = fmaxf(s[1], s[3]);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
-        tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
-      }
-      const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
-      const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
-      const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-      const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-      const float p0 = exp2f(s[0] - mu0), p1 = exp2f(s[1] - mu1);
-      const float p2 = exp2f(s[2] - mu0), p3 = exp2f(s[3] - mu1);
-      l0 = l0 * al0 + p0 + p2;
-      l1 = l1 * al1 + p1 + p3;
-      m0 = mn0;
-      m1 = mn1;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        acc[mt][0] *= al0;
-        acc[mt][1] *= al1;
-        acc[mt][2] *= al0;
-        acc[mt][3] *= al1;
-      }
-      // ---- P^T as the B operand: transpose the two 8x8 halves in registers
-      // (f16 for E4M3 pools, whose V is unpacked to f16; bf16 otherwise)
-      const uint32_t b0 = movmatrix_trans(FP8 ? pack_f16(p0 * pv_scale, p1 * pv_scale)
-                                              : pack_bf16(p0 * pv_scale, p1 * pv_scale));
-      const uint32_t b1 = movmatrix_trans(FP8 ? pack_f16(p2 * pv_scale, p3 * pv_scale)
-                                              : pack_bf16(p2 * pv_scale, p3 * pv_scale));
-      // keys of this thread's V^T fragment halves
-      const bool tail = k16 + 16 > ke;
-      const int ka = k16 + 2 * t;
-      const uint32_t mlo = tail ? ((ka < ke ? 0x0000FFFFu : 0u) | (ka + 1 < ke ? 0xFFFF0000u : 0u))
-                                : 0xFFFFFFFFu;
-      const uint32_t mhi = tail ? ((ka + 8 < ke ? 0x0000FFFFu : 0u) | (ka + 9 < ke ? 0xFFFF0000u : 0u))
-                                : 0xFFFFFFFFu;
-      // ---- O^T += V^T P^T
-      if constexpr (FP8) {
-        const int kA = 16 * sub + 2 * t;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t ch = (g >> 2) + 2 * j;
-          const uint32_t bo = 4 * (g & 3);
-          const uint32_t wA = lds32(vbase + swz128(kA, ch) + bo);
-          const uint32_t wB = lds32(vbase + swz128(kA + 1, ch) + bo);
-          const uint32_t wC = lds32(vbase + swz128(kA + 8, ch) + bo);
-          const uint32_t wD = lds32(vbase + swz128(kA + 9, ch) + bo);
-          // pair the two keys' bytes per head-dim column, then convert
-          // in hardware: [A0 B0 A1 B1] and [A2 B2 A3 B3]
-          const uint32_t x01 = __byte_perm(wA, wB, 0x5140);
-          const uint32_t x23 = __byte_perm(wA, wB, 0x7362);
-          const uint32_t y01 = __byte_perm(wC, wD, 0x5140);
-          const uint32_t y23 = __byte_perm(wC, wD, 0x7362);
-          mma_f16(acc[2 * j], mlo & e4m3x2lo_to_f16x2(x01), mlo & e4m3x2hi_to_f16x2(x01),
-                  mhi & e4m3x2lo_to_f16x2(y01), mhi & e4m3x2hi_to_f16x2(y01), b0, b1);
-          mma_f16(acc[2 * j + 1], mlo & e4m3x2lo_to_f16x2(x23), mlo & e4m3x2hi_to_f16x2(x23),
-                  mhi & e4m3x2lo_to_f16x2(y23), mhi & e4m3x2hi_to_f16x2(y23), b0, b1);
-        }
-      } else {
-        const int mi = lane >> 3;
-        const int key = (mi >> 1) * 8 + (lane & 7);
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const uint32_t ch = 2 * (mt & 3) + (mi & 1);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(vbase + (mt >> 2) * (KS * 128) + swz128(key, ch), a0, a1,
-                        a2, a3);
-          mma_bf16(acc[mt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, b0, b1);
-        }
-      }
-    }
-    __syncwarp();
-    ++consumed;
-    if (lane == 0 && i + kDecStages < my_n) {
-      fence_proxy_async();
-      issue(i + kDecStages);
-    }
-  }
-  if (timed_out) {
-    record_error(p.err, kErrTimeout);
-    // let copies already in flight land before the shared memory is reused
-    const int issued = my_n < consumed + kDecStages ? my_n : consumed + kDecStages;
-    for (int i = consumed; i < issued; ++i)
-      mbar_wait(&full[i % kDecStages], (i / kDecStages) & 1);
-  }
-
-  // ---- per-warp row sums, then merge the 4 warps through shared memory
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-  }
-  __syncthreads();  // rings are free now
-  float *red_o = reinterpret_cast<float *>(smem);           // [4][8][128]
-  float *red_m = red_o + kDecWarps * kDecCols * kHeadDim;   // [4][8]
-  float *red_l = red_m + kDecWarps * kDecCols;              // [4][8]
-  if (g == 0) {
-    red_m[warp * kDecCols + 2 * t] = m0;
-    red_m[warp * kDecCols + 2 * t + 1] = m1;
-    red_l[warp * kDecCols + 2 * t] = l0;
-    red_l[warp * kDecCols + 2 * t + 1] = l1;
-  }
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int n = 2 * t + (c & 1);
-      const int dr = g + 8 * (c >> 1);
-      const int d = FP8 ? fp8_dmap(mt, dr) : 16 * mt + dr;
-      red_o[(warp * kDecCols + n) * kHeadDim + d] = acc[mt][c];
-    }
-  }
-  __syncthreads();
-
-  const int d = threadIdx.x;  // 128 threads, one head-dim element each
-  auto write_row = [&](int n, float o, float lse2) {
-    const int r = it.row0 + n;
-    const int64_t row = static_cast<int64_t>(it.tok0 + r / group) * p.hq +
-                        it.kv_head * group + r % group;
-    p.out[row * kHeadDim + d] = __float2bfloat16_rn(o);
-    if (d == 0 && p.lse != nullptr) p.lse[row] = lse2 * kLn2;
-  };
-  for (int n = 0; n < it.n_rows; ++n) {
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red_m[w * kDecCols + n]);
-    const float Mu = M == -CUDART_INF_F ? 0.f : M;
-    float Ls = 0.f, o = 0.f;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) {
-      const float sw = exp2f(red_m[w * kDecCols + n] - Mu);
-      Ls += red_l[w * kDecCols + n] * sw;
-      o += red_o[(w * kDecCols + n) * kHeadDim + d] * sw;
-    }
-    const float lse2 = Ls > 0.f ? Mu + log2f(Ls) : -CUDART_INF_F;
-    o = Ls > 0.f ? o / Ls : 0.f;
-    if (it.part < 0) {
-      write_row(n, o, lse2);
-    } else {
-      p.part_o[(static_cast<int64_t>(it.part) * kDecCols + n) * kHeadDim + d] = o;
-      if (d == 0) p.part_lse[static_cast<int64_t>(it.part) * kDecCols + n] = lse2;
-    }
-  }
-  if (it.part < 0) return;
-
-  // ---- last range of this (request, KV head) to finish merges all ranges
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int prev = atomicAdd(p.tickets + it.pair, 1);
-    *flag = (prev == it.n_split - 1);
-  }
-  __syncthreads();
-  if (*flag == 0) return;
-  __threadfence();
-  for (int n = 0; n < it.n_rows; ++n) {
-    float M = -CUDART_INF_F;
-    for (int s2 = 0; s2 < it.n_split; ++s2)
-      M = fmaxf(M, __ldcg(p.part_lse + static_cast<int64_t>(it.pair + s2) * kDecCols + n));
-    const float Mu = M == -CUDART_INF_F ? 0.f : M;
-    float Ls = 0.f, o = 0.f;
-    for (int s2 = 0; s2 < it.n_split; ++s2) {
-      const int64_t slot = it.pair + s2;
-      const float w = exp2f(__ldcg(p.part_lse + slot * kDecCols + n) - Mu);
-      Ls += w;
-      o += w * __ldcg(p.part_o + (slot * kDecCols + n) * kHeadDim + d);
-    }
-    write_row(n, Ls > 0.f ? o / Ls : 0.f, Ls > 0.f ? Mu + log2f(Ls) : -CUDART_INF_F);
-  }
-  if (threadIdx.x == 0) p.tickets[it.pair] = 0;  // ready for the next step
+  decode_item<FP8, kDecWarps>(kmap, vmap, p, p.items[blockIdx.x], smem, threadIdx.x, 0);
 }
 
 }  // namespace

@@ -15,6 +15,7 @@ namespace pkv {
 cudaError_t configure_decode();
 cudaError_t configure_prefill();
 cudaError_t configure_prefill_tc();
+cudaError_t configure_mixed();
 }  // namespace pkv
 
 using namespace pkv;
@@ -116,6 +117,8 @@ std::string check_config(const pkv_config *c, pkv_status *st) {
     return "max_num_seqs and max_num_tokens must be > 0";
   if (c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_FP8_E4M3)
     return fmt("unknown kv_dtype %d", c->kv_dtype);
+  if (c->flags & ~static_cast<uint32_t>(PKV_FLAG_VALIDATE | PKV_FLAG_TIMING | PKV_FLAG_SEPARATE))
+    return fmt("unknown flag bits 0x%x", c->flags);
   *st = PKV_ERR_UNSUPPORTED;
   if (c->head_dim != kHeadDim) return fmt("head_dim %d is not supported (only 128)", c->head_dim);
   const int bs = c->block_size;
@@ -362,7 +365,7 @@ pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out) {
     return PKV_ERR_CUDA;
   }
   if ((e = configure_decode()) != cudaSuccess || (e = configure_prefill()) != cudaSuccess ||
-      (e = configure_prefill_tc()) != cudaSuccess) {
+      (e = configure_prefill_tc()) != cudaSuccess || (e = configure_mixed()) != cudaSuccess) {
     g_create_error = fmt("configuring kernels: %s", cudaGetErrorString(e));
     return PKV_ERR_CUDA;
   }
@@ -583,60 +586,70 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
   const float scale_log2 = c.softmax_scale * 1.4426950408889634f;
   const int G = c.num_q_heads / c.num_kv_heads;
   const int32_t rows_total = static_cast<int32_t>(c.num_blocks * c.num_kv_heads * bs);
-  if (!plan.dec.empty()) {
-    DecodeParams p{};
-    p.items = d_items;
-    p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.block_tables = block_tables;
-    p.bt_stride = block_table_stride;
-    p.k_scale = k_scale;
-    p.v_scale = v_scale;
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    p.lse = lse;
-    p.part_o = h->d_part_o;
-    p.part_lse = h->d_part_lse;
-    p.tickets = h->d_tickets;
-    p.err = h->d_err;
-    p.hq = c.num_q_heads;
-    p.hkv = c.num_kv_heads;
-    p.group = G;
-    p.bs = bs;
-    p.rows_total = rows_total;
-    p.num_blocks = c.num_blocks;
-    p.scale_log2 = scale_log2;
-    p.validate = validate;
+  DecodeParams dp{};
+  dp.items = d_items;
+  dp.q = static_cast<const __nv_bfloat16 *>(q);
+  dp.block_tables = block_tables;
+  dp.bt_stride = block_table_stride;
+  dp.k_scale = k_scale;
+  dp.v_scale = v_scale;
+  dp.out = static_cast<__nv_bfloat16 *>(out);
+  dp.lse = lse;
+  dp.part_o = h->d_part_o;
+  dp.part_lse = h->d_part_lse;
+  dp.tickets = h->d_tickets;
+  dp.err = h->d_err;
+  dp.hq = c.num_q_heads;
+  dp.hkv = c.num_kv_heads;
+  dp.group = G;
+  dp.bs = bs;
+  dp.rows_total = rows_total;
+  dp.num_blocks = c.num_blocks;
+  dp.scale_log2 = scale_log2;
+  dp.validate = validate;
+  PrefillParams pp{};
+  pp.items = d_items + plan.dec.size();
+  pp.paired = h->pf_paired ? 1 : 0;
+  pp.q = static_cast<const __nv_bfloat16 *>(q);
+  pp.block_tables = block_tables;
+  pp.bt_stride = block_table_stride;
+  pp.out = static_cast<__nv_bfloat16 *>(out);
+  pp.lse = lse;
+  pp.err = h->d_err;
+  pp.hq = c.num_q_heads;
+  pp.hkv = c.num_kv_heads;
+  pp.group = G;
+  pp.bs = bs;
+  pp.rows_total = rows_total;
+  pp.num_blocks = c.num_blocks;
+  pp.scale_log2 = scale_log2;
+  pp.validate = validate;
+  const bool tc = prefill_uses_tc(c);
+  CUtensorMap qmap;
+  if (!plan.pre.empty() && tc && !encode_q_map(&qmap, q, c.num_q_heads, G, num_tokens))
+    return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled rejected the query layout");
+  const int n_dec = static_cast<int>(plan.dec.size());
+  const int n_pre = static_cast<int>(plan.pre.size());
+  if (n_dec > 0 && n_pre > 0 && tc && !(c.flags & PKV_FLAG_SEPARATE)) {
+    // a mixed step: one launch for both kinds of work
+    timing_begin(h, PKV_KERNEL_MIXED, s);
+    e = launch_mixed(qmap, h->pf_k, h->pf_v, h->dec_k, h->dec_v, pp, dp, n_pre, n_dec, s);
+    timing_end(h, PKV_KERNEL_MIXED, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "mixed-step launch");
+    return PKV_OK;
+  }
+  if (n_dec > 0) {
     timing_begin(h, PKV_KERNEL_DECODE, s);
-    e = launch_decode(h->dec_k, h->dec_v, p, static_cast<int>(plan.dec.size()), fp8, s);
+    e = launch_decode(h->dec_k, h->dec_v, dp, n_dec, fp8, s);
     timing_end(h, PKV_KERNEL_DECODE, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
   }
-  if (!plan.pre.empty()) {
-    PrefillParams p{};
-    p.items = d_items + plan.dec.size();
-    p.paired = h->pf_paired ? 1 : 0;
-    p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.block_tables = block_tables;
-    p.bt_stride = block_table_stride;
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    p.lse = lse;
-    p.err = h->d_err;
-    p.hq = c.num_q_heads;
-    p.hkv = c.num_kv_heads;
-    p.group = G;
-    p.bs = bs;
-    p.rows_total = rows_total;
-    p.num_blocks = c.num_blocks;
-    p.scale_log2 = scale_log2;
-    p.validate = validate;
-    CUtensorMap qmap;
-    const bool tc = prefill_uses_tc(c);
-    if (tc && !encode_q_map(&qmap, q, c.num_q_heads, G, num_tokens))
-      return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled rejected the query layout");
+  if (n_pre > 0) {
     timing_begin(h, PKV_KERNEL_PREFILL, s);
     if (tc)
-      e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, p, static_cast<int>(plan.pre.size()), s);
+      e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, pp, n_pre, s);
     else
-      e = launch_prefill(h->pf_k, h->pf_v, p, static_cast<int>(plan.pre.size()), s);
+      e = launch_prefill(h->pf_k, h->pf_v, pp, n_pre, s);
     timing_end(h, PKV_KERNEL_PREFILL, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
   }

@@ -12,6 +12,8 @@
 
 namespace pkv {
 
+constexpr float kLn2 = 0.6931471805599453f;
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -24,6 +26,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 __device__ __forceinline__ void record_error(int32_t *err, int32_t bit) {
   if (err != nullptr) atomicOr(err, bit);
+}
+
+// Barrier `id` over the first `nthreads` threads of the CTA (multiple of 32).
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---- mbarrier ----------------------------------------------------------------

@@ -121,6 +121,11 @@ cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p,
                               int num_items, cudaStream_t s);
 cudaError_t launch_check(const CheckParams &p, cudaStream_t s);
+cudaError_t launch_mixed(const CUtensorMap &qmap, const CUtensorMap &kmap_pf,
+                         const CUtensorMap &vmap_pf, const CUtensorMap &kmap_dec,
+                         const CUtensorMap &vmap_dec, const PrefillParams &pp,
+                         const DecodeParams &dp, int n_prefill, int n_decode,
+                         cudaStream_t s);
 
 // Prefill tiles run on the tcgen05 kernel (128 rows) when the query group
 // size is a power of two (so a tile is a whole number of tokens) and the KV

@@ -1,0 +1,401 @@
+// Incremental-prefill work item on tcgen05 (device code shared by the
+// prefill kernel and the one-launch mixed-step kernel).  See prefill_tc.cu
+// for what it computes and how the roles divide the work.
+#pragma once
+
+#include <math_constants.h>
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+namespace {
+
+
+constexpr int kTcThreads = 320;
+constexpr int kKst = 3;                           // K ring depth
+constexpr int kVst = 2;                           // V ring depth
+constexpr uint32_t kHalf = 128 * 128;             // one 64-column half of a 128-row tile
+constexpr uint32_t kTile = 2 * kHalf;             // 32 KB: 128 rows x 128 bf16
+constexpr uint32_t kOffQ = 0;                     // 2 Q tiles
+constexpr uint32_t kOffK = 2 * kTile;             // kKst K tiles
+constexpr uint32_t kOffV = kOffK + kKst * kTile;  // kVst V tiles
+constexpr uint32_t kOffBar = kOffV + kVst * kTile;   // 229376
+constexpr uint32_t kTmemCols = 512;               // S0, S1, O0, O1
+constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);
+constexpr uint32_t kIdescQK64 = idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 0, 1);
+constexpr float kRescaleThreshold = 8.f;          // log2 units
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b,
+                                       uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+
+// Tile-local key held by S column c in the paired layout.
+__device__ __forceinline__ int paired_key(int c) {
+  return ((c & 63) >> 3) * 16 + ((c >> 6) << 3) + (c & 7);
+}
+
+// 64 consecutive fp32 TMEM columns of this thread's lane (one load, wait
+// included).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  tmem_ld64x(taddr, v);
+}
+
+// One prefill work item processed by all kTcThreads threads of the CTA;
+// `smem` is 1024-byte aligned (kTcSmemBytes - 1024 bytes).
+__device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
+                                                const CUtensorMap &kmap,
+                                                const CUtensorMap &vmap,
+                                                const PrefillParams &p,
+                                                const pkv_work_item it, uint8_t *smem) {
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  uint64_t *q_full = bars + 0;
+  uint64_t *k_full = bars + 1;               // [kKst]
+  uint64_t *k_empty = k_full + kKst;         // [kKst]
+  uint64_t *v_full = k_empty + kKst;         // [kVst]
+  uint64_t *v_empty = v_full + kVst;         // [kVst]
+  uint64_t *s_full = v_empty + kVst;         // [2] per Q tile
+  uint64_t *p_full = s_full + 2;             // [2]
+  uint64_t *o_done = p_full + 2;             // [2]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_done + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.group;
+  // Q tile t holds rows [row0 + 128 t, +n_t) and reaches keys [0, kend_t)
+  const int n0 = it.n_rows < 128 ? it.n_rows : 128;
+  const int n1 = it.n_rows - n0;
+  const bool two = n1 > 0;
+  const int kend0 = it.hist + (it.row0 + n0 - 1) / G + 1;
+  const int kend1 = two ? it.hist + (it.row0 + 128 + n1 - 1) / G + 1 : kend0;
+  const int k_end = it.k_end;                   // = kend1
+  const int nt0 = (kend0 + 127) / 128;
+  const int nt1 = two ? (kend1 + 127) / 128 : 0;
+  const int n_tiles = (k_end + 127) / 128;      // = max(nt0, nt1)
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < kKst; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < kVst; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
+    }
+    prefetch_tmap(&qmap);
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+  }
+  if (warp == 8) tmem_alloc(tmem_slot, kTmemCols);
+  fence_mbar_init();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 9) {
+    // ---------------- TMA producer (whole warp) ----------------
+    // Issue order K_0, K_1, V_0, K_2, V_1, ...: K_j waits for the QKs of tile
+    // j-3, V_i for the PVs of tile i-2, which complete in that order.  Lane b
+    // holds the row of box b of a tile (block ids read one tile ahead, so
+    // table reads never sit between TMA issues); lane 0 issues the copies.
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
+    const int br = p.bs < 128 ? p.bs : 128;
+    const int nbox = 128 / br;  // <= 8
+    const bool paired = p.paired != 0;
+    auto tile_rows = [&](int j) {
+      const int key = j * 128 + lane * br;
+      int32_t y = p.rows_total;
+      if (lane < nbox && j < n_tiles && key < k_end) {
+        const int32_t blk = __ldg(bt + key / p.bs);
+        if (blk >= 0 && blk < p.num_blocks)
+          y = (blk * p.hkv + it.kv_head) * p.bs + key % p.bs;
+        else
+          record_error(p.err, kErrBadBlock);
+      }
+      return y;
+    };
+    auto issue = [&](const CUtensorMap *map, uint8_t *dst, uint64_t *bar, int j, int32_t yv) {
+      int n = 0;
+      for (int r = 0; r < 128; r += br)
+        if (j * 128 + r < k_end) ++n;
+      if (lane == 0) mbar_arrive_expect_tx(bar, n * br * 128 * 2);
+      for (int bx = 0; bx < n; ++bx) {
+        const int32_t y = __shfl_sync(0xffffffffu, yv, bx);
+        if (lane == 0) {
+          if (paired) {
+            tma_load_3d(dst + bx * 4096, map, 0, y, 0, bar);
+          } else {
+            tma_load_2d(dst + bx * br * 128, map, 0, y, bar);
+            tma_load_2d(dst + kHalf + bx * br * 128, map, 64, y, bar);
+          }
+        }
+      }
+    };
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, two ? 2 * kTile : kTile);
+      const int t0 = it.tok0 + it.row0 / G;
+      tma_load_3d(smem + kOffQ, &qmap, 0, it.kv_head * G, t0, q_full);
+      tma_load_3d(smem + kOffQ + kHalf, &qmap, 64, it.kv_head * G, t0, q_full);
+      if (two) {
+        const int t1 = t0 + 128 / G;
+        tma_load_3d(smem + kOffQ + kTile, &qmap, 0, it.kv_head * G, t1, q_full);
+        tma_load_3d(smem + kOffQ + kTile + kHalf, &qmap, 64, it.kv_head * G, t1, q_full);
+      }
+    }
+    int32_t y_cur = tile_rows(0);   // rows of tile j (for K_j)
+    int32_t y_prev = 0;             // rows of tile j-1 (for V_{j-1})
+    for (int j = 0; j <= n_tiles; ++j) {
+      const int32_t y_next = tile_rows(j + 1);
+      if (j < n_tiles) {
+        const int s = j % kKst;
+        if (j >= kKst &&
+            !__all_sync(0xffffffffu, mbar_wait(&k_empty[s], ((j / kKst) - 1) & 1))) {
+          if (lane == 0) record_error(p.err, kErrTimeout);
+          break;
+        }
+        issue(&kmap, smem + kOffK + s * kTile, &k_full[s], j, y_cur);
+      }
+      if (j >= 1) {
+        const int i = j - 1, s = i % kVst;
+        if (i >= kVst &&
+            !__all_sync(0xffffffffu, mbar_wait(&v_empty[s], ((i / kVst) - 1) & 1))) {
+          if (lane == 0) record_error(p.err, kErrTimeout);
+          break;
+        }
+        issue(&vmap, smem + kOffV + s * kTile, &v_full[s], i, y_prev);
+      }
+      y_prev = y_cur;
+      y_cur = y_next;
+    }
+  } else if (warp == 8) {
+    // ---------------- MMA issuer (one thread) ----------------
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0);
+      auto qk = [&](int t, int j) {   // S_t = Q_t K_j^T
+        const int s = j % kKst;
+        if (!mbar_wait(&k_full[s], (j / kKst) & 1)) return false;
+        tc_fence_after();
+        const uint32_t qa = smem_addr(smem + kOffQ + t * kTile);
+        const uint32_t ka = smem_addr(smem + kOffK + s * kTile);
+        const uint32_t d = tmem + t * 128;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
+          const uint64_t ad = smem_desc_sw128(qa + off, 16, 1024);
+          if (p.paired) {
+            const uint32_t koff = (ks >> 2) * 2048 + (ks & 3) * 32;
+            tc_mma(d, ad, smem_desc_sw128(ka + koff, 16, 4096), kIdescQK64, ks > 0 ? 1u : 0u);
+            tc_mma(d + 64, ad, smem_desc_sw128(ka + koff + 1024, 16, 4096), kIdescQK64,
+                   ks > 0 ? 1u : 0u);
+          } else {
+            tc_mma(d, ad, smem_desc_sw128(ka + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
+          }
+        }
+        tc_commit(&s_full[t]);
+        return true;
+      };
+      auto pv = [&](int t, int j) {   // O_t += P_t V_j
+        const int s = j % kVst;
+        if (!mbar_wait(&p_full[t], j & 1)) return false;
+        if (!mbar_wait(&v_full[s], (j / kVst) & 1)) return false;
+        tc_fence_after();
+        const uint32_t va = smem_addr(smem + kOffV + s * kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd =
+              p.paired ? smem_desc_sw128(va + (kk >> 2) * 1024 + (kk & 3) * 8192, 2048, 4096)
+                       : smem_desc_sw128(va + kk * 2048, kHalf, 1024);
+          tc_mma_tmem_a(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, bd, kIdescPV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&o_done[t]);
+        return true;
+      };
+      // prologue: QK of tile 0 for both Q tiles
+      if (ok) ok = qk(0, 0);
+      if (ok && two) ok = qk(1, 0);
+      if (ok) tc_commit(&k_empty[0]);
+      // P_t(j) lives where QK_t(j+1) writes: QK_t(j+1) is issued after
+      // PV_t(j) (tcgen05.mma of one thread execute in order).
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j < nt0) {
+          ok = pv(0, j);
+          if (ok && j + 1 < nt0) ok = qk(0, j + 1);
+        }
+        if (ok && two && j < nt1) {
+          ok = pv(1, j);
+          if (ok && j + 1 < nt1) ok = qk(1, j + 1);
+        }
+        if (!ok) break;
+        tc_commit(&v_empty[j % kVst]);
+        if (j + 1 < n_tiles) tc_commit(&k_empty[(j + 1) % kKst]);
+      }
+      if (!ok) record_error(p.err, kErrTimeout);
+    }
+  } else {
+    // ---------------- softmax / epilogue: thread r of tile t owns row r ----
+    const int t = warp >> 2;                   // Q tile of this warpgroup
+    const int r = threadIdx.x & 127;
+    const int nrow = t == 0 ? n0 : n1;
+    const int ntl = t == 0 ? nt0 : nt1;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t col_s = t * 128, col_o = 256 + t * 128;
+    const int rowg = it.row0 + 128 * t + r;
+    const bool row_ok = r < nrow;
+    const int pos = it.hist + rowg / G;   // padded rows see every key
+    const float c = p.scale_log2;
+    float m = -CUDART_INF_F;              // running max, log2 units
+    float l = 0.f;
+    bool ok = true;
+    // TMEM loads and stores are .sync.aligned: every decision that guards
+    // one is warp-uniform (__all_sync / __any_sync).
+    for (int j = 0; j < ntl; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int key0 = j * 128;
+      // one pass: the whole S row in registers (one TMEM load)
+      float s[128];
+      tmem_ld128(lane_addr + col_s, s);
+      if (key0 + 127 > pos) {   // diagonal tile: causal mask
+#pragma unroll
+        for (int k = 0; k < 128; ++k) {
+          const int key = key0 + (p.paired ? paired_key(k) : k);
+          s[k] = key > pos ? -CUDART_INF_F : s[k];
+        }
+      }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int k = 8; k < 128; k += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[k + i]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float mt2 = mt * c;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (mt2 > m + kRescaleThreshold) {
+        alpha = ex2(m - mt2);
+        rescale = j > 0;
+        m = mt2;
+      }
+      // P = 2^(s c - m) as bf16 pairs over the S columns, in two 64-column
+      // chunks (chunk 0's P lands on S columns 0-31, already in registers)
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float e0 = ex2(fmaf(s[64 * hh + 2 * k], c, -m));
+          const float e1 = ex2(fmaf(s[64 * hh + 2 * k + 1], c, -m));
+          acc[(2 * k) & 7] += e0;
+          acc[(2 * k + 1) & 7] += e1;
+          pk[k] = pack_bf16(e0, e1);
+        }
+        tmem_st32u(lane_addr + col_s + 32 * hh, pk);
+      }
+      const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
+                        ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+      l = l * alpha + sum;
+      if (__any_sync(0xffffffffu, rescale)) {
+        // the whole warp rescales (alpha is 1 on rows whose max held); O
+        // must not be written by PV of tile j-1 meanwhile
+        if (!rescale) alpha = 1.f;
+        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[t], (j - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_ld128(lane_addr + col_o, s);
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] *= alpha;
+        tmem_st128(lane_addr + col_o, s);
+      }
+      // The last K/V tile may carry V rows past the item's last key (rows
+      // of other requests or never loaded): zero them before any PV reads
+      // them.  Q tile 0 does it when it reaches that tile (its PV comes
+      // first), otherwise Q tile 1.
+      if (j == n_tiles - 1 && k_end - key0 < 128 && (t == 0 || nt0 < n_tiles)) {
+        const int vvalid = k_end - key0;
+        const int vs = j % kVst;
+        if (!__all_sync(0xffffffffu, mbar_wait(&v_full[vs], (j / kVst) & 1))) {
+          ok = false;
+          break;
+        }
+        if (r >= vvalid) {   // thread r clears the V row of tile-local key r
+          const uint32_t vt = smem_addr(smem + kOffV + vs * kTile);
+          const uint32_t vrow = p.paired ? vt + (r >> 4) * 4096 + (r & 15) * 128 : vt + r * 128;
+          const uint32_t hstep = p.paired ? 2048u : kHalf;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)   // rotate chunks across rows: no bank conflicts
+              sts128(vrow + h * hstep + 16 * ((q + r) & 7), 0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async();
+      }
+      tc_fence_before();
+      mbar_arrive(&p_full[t]);
+    }
+    // ---- epilogue: O / l -> bf16
+    if (ntl > 0) {
+      const int J = ntl - 1;
+      if (__all_sync(0xffffffffu, ok && mbar_wait(&o_done[t], J & 1))) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int64_t orow = static_cast<int64_t>(it.tok0 + rowg / G) * p.hq +
+                             it.kv_head * G + rowg % G;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kHeadDim);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[64];
+          tmem_ld64(lane_addr + col_o + 64 * hh, v);
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[8 * hh + i] = make_uint4(pack_bf16(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                           pack_bf16(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                           pack_bf16(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                           pack_bf16(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+          }
+        }
+        if (row_ok && p.lse != nullptr)
+          p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
+      } else {
+        record_error(p.err, kErrTimeout);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 8) tmem_dealloc(tmem, kTmemCols);
+}
+
+
+constexpr uint32_t kTcSmemBytes = kOffBar + 256 + 1024;
+
+}  // namespace
+}  // namespace pkv

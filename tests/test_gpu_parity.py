@@ -89,6 +89,29 @@ def test_small_cases_every_row(case, q_scale):
     U.full_parity(b, what=name, peaked=q_scale > 1.0)
 
 
+@pytest.mark.parametrize("separate", [False, True], ids=["one_launch", "separate"])
+def test_mixed_step_launch_modes(separate):
+    """A step with decodes and prefill chunks runs as one mixed launch, or
+    with PKV_FLAG_SEPARATE as a decode and a prefill launch; both match the
+    oracle on every row."""
+    s = spec("mixed_modes", 32, 4, 16, [1, 1, 300, 1, 77, 1], [40, 3000, 1300, 1, 77, 700])
+    b = W.generate(s, DEV)
+    flags = pkv.FLAG_VALIDATE | pkv.FLAG_TIMING | (pkv.FLAG_SEPARATE if separate else 0)
+    h = U.make_handle(b, flags)
+    sub = W.subset(b, list(range(s.num_seqs)))
+    out, lse = U.gpu_step(b, handle=h)
+    counts = {k: h.timing_read(k)[0] for k in
+              (pkv.KERNEL_DECODE, pkv.KERNEL_PREFILL, pkv.KERNEL_MIXED)}
+    h.close()
+    ref, ref_lse = U.oracle_subset(sub, s)
+    got, got_lse = U.gpu_rows(out, lse, sub)
+    U.check(got, ref, got_lse, ref_lse, "bf16", "mixed_modes")
+    if separate:
+        assert counts == {pkv.KERNEL_DECODE: 1, pkv.KERNEL_PREFILL: 1, pkv.KERNEL_MIXED: 0}
+    else:
+        assert counts == {pkv.KERNEL_DECODE: 0, pkv.KERNEL_PREFILL: 0, pkv.KERNEL_MIXED: 1}
+
+
 def test_tiny_incremental_prefill_config():
     """1 sequence, l_hist 1000 + l_incr 64, 8q/2kv heads, 128-block pool."""
     b = W.generate(W.config_spec(0), DEV)
