@@ -141,20 +141,31 @@ class ClockSampler:
                 "samples": len(inside)}
 
 
-def traffic_from_profile(kernel_file: str, summary: str):
+def traffic_from_profile(summary: str):
     """DRAM bytes per launch recorded by an ncu capture, if the kernel's
-    source is unchanged since (matched by the sha256 noted in the summary)."""
+    sources are unchanged since: the summary lists them (`sources:`) and the
+    sha256 of their concatenation (`source_sha256:`)."""
     path = os.path.join(ROOT, "profiles", summary)
-    src = os.path.join(ROOT, "paged_kv_attention_pkv_gb300", "csrc", kernel_file)
-    if not os.path.exists(path) or not os.path.exists(src):
+    if not os.path.exists(path):
         return None
     text = open(path).read()
+    m_src = re.search(r"^sources:\s*(.+)$", text, re.M)
     m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     m_tr = re.search(r"traffic_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_tr:
+    if not m_src or not m_sha or not m_tr:
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return float(m_tr.group(1)) if sha == m_sha.group(1) else None
+    return float(m_tr.group(1)) if sources_sha256(m_src.group(1).split()) == m_sha.group(1) \
+        else None
+
+
+def sources_sha256(names) -> str | None:
+    h = hashlib.sha256()
+    for n in names:
+        f = os.path.join(ROOT, "paged_kv_attention_pkv_gb300", "csrc", n)
+        if not os.path.exists(f):
+            return None
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
 
 
 def barrier(world):
@@ -357,7 +368,7 @@ def run_ours(args, rank, world, local_rank):
     value = world * bytes_step / (ms_step * 1e-3) / 1e9
     e2e = prim["e2e"]
     e2e_value = world * bytes_step / (e2e["ms_per_step"] * 1e-3) / 1e9
-    traffic = traffic_from_profile("decode.cu", "ncu_decode_c2.md")
+    traffic = traffic_from_profile("ncu_decode_c2.md")
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),

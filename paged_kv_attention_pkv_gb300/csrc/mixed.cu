@@ -5,10 +5,10 @@
 //
 // The grid is the prefill tiles (longest first) followed by the split-KV
 // decode items (longest first).  A CTA whose index falls on a prefill tile
-// runs the tcgen05 prefill item with all 10 warps; a CTA on a decode item
+// runs the tcgen05 prefill item with all 12 warps; a CTA on a decode item
 // runs the decode item with 8 warps (8 rings of 3 stages in the same shared
 // memory, so an SM keeps as many K/V bytes in flight as two 4-warp decode
-// CTAs) and lets the other 2 warps exit.  Decode CTAs are scheduled last and
+// CTAs) and lets the other 4 warps exit.  Decode CTAs are scheduled last and
 // fill the SMs that prefill tiles free at different times, so the tail of
 // the prefill work overlaps the memory-bound decode work.  Decode ranges of
 // one (request, KV head) are merged by the last CTA to finish, as in the
@@ -57,6 +57,13 @@ cudaError_t launch_mixed(const CUtensorMap &qmap, const CUtensorMap &kmap_pf,
 }
 
 cudaError_t configure_mixed() {
+  // setmaxnreg moves registers within the CTA's launch allotment: the split
+  // must not ask for more than the kernel was compiled (and launched) with
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, mixed_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * kTcThreads < static_cast<int>(2 * 128 * kRegsSoftmax + 128 * kRegsCtl))
+    return cudaErrorInvalidConfiguration;
   return cudaFuncSetAttribute(mixed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kTcSmemBytes);
 }

@@ -87,7 +87,6 @@ struct pkv_handle {
   // cached pool descriptors
   const void *map_k_ptr = nullptr, *map_v_ptr = nullptr;
   CUtensorMap dec_k{}, dec_v{}, pf_k{}, pf_v{};
-  bool pf_paired = false;   // pf_k / pf_v hold the 16-token 3D-box view
 };
 
 namespace {
@@ -287,19 +286,6 @@ bool encode_q_map(CUtensorMap *m, const void *q, int hq, int group, int64_t toke
 // 16-token pools viewed as [2 halves][rows][64 columns] (the halves 128 B
 // apart, rows 256 B apart) with boxes of {64, 16, 2}: one box carries a whole
 // (block, KV head) tile of 4 KB as [half][16 rows][64], 128-byte swizzled.
-bool encode_pool_map_paired(CUtensorMap *m, const void *base, int64_t rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[3] = {64, cuuint64_t(rows), 2};
-  const cuuint64_t strides[2] = {cuuint64_t(kHeadDim * 2), 128};
-  const cuuint32_t box[3] = {64, 16, 2};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 size_t items_bytes(int max_items) { return sizeof(pkv_work_item) * size_t(max_items); }
 
 void timing_begin(pkv_handle *h, int kind, cudaStream_t s) {
@@ -528,12 +514,7 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
     const int pf_box = std::min(bs, prefill_uses_tc(c) ? 128 : kPfKeys);
     bool ok = encode_pool_map(&h->dec_k, k_cache, fp8, rows, dec_box) &&
               encode_pool_map(&h->dec_v, v_cache, fp8, rows, dec_box);
-    h->pf_paired = false;
-    if (ok && !fp8 && prefill_uses_tc(c) && bs == 16) {
-      h->pf_paired = encode_pool_map_paired(&h->pf_k, k_cache, rows) &&
-                     encode_pool_map_paired(&h->pf_v, v_cache, rows);
-    }
-    if (ok && !fp8 && !h->pf_paired)
+    if (ok && !fp8)
       ok = encode_pool_map(&h->pf_k, k_cache, false, rows, pf_box) &&
            encode_pool_map(&h->pf_v, v_cache, false, rows, pf_box);
     if (!ok) {
@@ -609,7 +590,6 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
   dp.validate = validate;
   PrefillParams pp{};
   pp.items = d_items + plan.dec.size();
-  pp.paired = h->pf_paired ? 1 : 0;
   pp.q = static_cast<const __nv_bfloat16 *>(q);
   pp.block_tables = block_tables;
   pp.bt_stride = block_table_stride;

@@ -67,7 +67,6 @@ struct DecodeParams {
 
 struct PrefillParams {
   const pkv_work_item *items;
-  int32_t paired;    // tcgen05 kernel: 16-token blocks in one 3D box each
   const __nv_bfloat16 *q;
   const int32_t *block_tables;
   int32_t bt_stride;

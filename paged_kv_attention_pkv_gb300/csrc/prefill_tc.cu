@@ -9,17 +9,15 @@
 // 4.3.1).  The rows form two 128-row Q tiles that share every 128-key K/V
 // tile, so each byte brought into shared memory feeds 256 rows.
 //
-// Roles (320 threads, one CTA per SM):
-//   warp 9      TMA producer: Q tiles (one 3D box per 64-column half) and K
-//               and V tiles of 128 keys into a 3-stage K ring and a 2-stage V
-//               ring, 128-byte swizzled; K of tile j is released once both
-//               QKs of tile j are done, V once both PVs are done.  16-token
-//               blocks come in one 4 KB 3D box per block holding both
-//               64-column halves ([half][16 rows][64]; "paired" layout: the
-//               8-row groups of a half are 4 KB apart with even and odd groups
-//               interleaved, so QK runs as two N = 64 MMAs and PV reads V in
-//               the same key order); larger blocks use one 2D box per block
-//               and half, laid out [half][128 rows][64].
+// Roles (384 threads, one CTA per SM; warp 11 only completes the third
+// warpgroup, whose registers move to the softmax warpgroups):
+//   warps 9-10  TMA producers, warp 9 for the Q tiles (one 3D box per
+//               64-column half) and a 2-stage K ring, warp 10 for a 3-stage
+//               V ring, tiles of 128 keys laid out [half][128 rows][64],
+//               128-byte swizzled, one 2D box per block and half (16 copies
+//               per tile for 16-token blocks: one issuing thread cannot keep
+//               up with both rings); K of tile j is released once both QKs
+//               of tile j are done, V once both PVs are done.
 //   warp 8      one thread issues tcgen05.mma in the order
 //                 PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1), ...
 //               so the tensor core works on one Q tile while the softmax of
@@ -60,8 +58,14 @@ cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
 }
 
 cudaError_t configure_prefill_tc() {
-  return cudaFuncSetAttribute(prefill_tc_kernel,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // setmaxnreg moves registers within the CTA's launch allotment: the split
+  // must not ask for more than the kernel was compiled (and launched) with
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * kTcThreads < static_cast<int>(2 * 128 * kRegsSoftmax + 128 * kRegsCtl))
+    return cudaErrorInvalidConfiguration;
+  return cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kTcSmemBytes);
 }
 

@@ -11,15 +11,27 @@ namespace pkv {
 namespace {
 
 
-constexpr int kTcThreads = 320;
-constexpr int kKst = 3;                           // K ring depth
-constexpr int kVst = 2;                           // V ring depth
+// 12 warps: softmax warpgroups 0-1 (warps 0-7), then warp 8 (MMA issue,
+// TMEM owner), warp 9 (TMA producer) and two idle warps completing
+// warpgroup 2, so registers can move between warpgroups (setmaxnreg): the
+// launch gives every thread 168; warpgroup 2 drops to kRegsCtl and the
+// softmax warpgroups rise to kRegsSoftmax (2 x 128 x 208 + 128 x 88 =
+// 384 x 168, the registers the CTA was launched with; neither side spills).
+constexpr int kTcThreads = 384;
+constexpr uint32_t kRegsLaunch = 168;
+constexpr uint32_t kRegsCtl = 88;
+constexpr uint32_t kRegsSoftmax = 208;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsCtl == kTcThreads * kRegsLaunch,
+              "register split must use exactly the launch's registers");
+constexpr int kKst = 2;                           // K ring depth
+constexpr int kVst = 3;                           // V ring depth
 constexpr uint32_t kHalf = 128 * 128;             // one 64-column half of a 128-row tile
 constexpr uint32_t kTile = 2 * kHalf;             // 32 KB: 128 rows x 128 bf16
 constexpr uint32_t kOffQ = 0;                     // 2 Q tiles
 constexpr uint32_t kOffK = 2 * kTile;             // kKst K tiles
 constexpr uint32_t kOffV = kOffK + kKst * kTile;  // kVst V tiles
 constexpr uint32_t kOffBar = kOffV + kVst * kTile;   // 229376
+static_assert(kOffBar == 229376, "Q, K and V tiles fill 224 KB");
 constexpr uint32_t kTmemCols = 512;               // S0, S1, O0, O1
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);
 constexpr uint32_t kIdescQK64 = idesc_bf16(128, 64, 0, 0);
@@ -37,11 +49,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b,
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b),
                "r"(c), "r"(d)
                : "memory");
-}
-
-// Tile-local key held by S column c in the paired layout.
-__device__ __forceinline__ int paired_key(int c) {
-  return ((c & 63) >> 3) * 16 + ((c >> 6) << 3) + (c & 7);
 }
 
 // 64 consecutive fp32 TMEM columns of this thread's lane (one load, wait
@@ -108,16 +115,25 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 9) {
-    // ---------------- TMA producer (whole warp) ----------------
-    // Issue order K_0, K_1, V_0, K_2, V_1, ...: K_j waits for the QKs of tile
-    // j-3, V_i for the PVs of tile i-2, which complete in that order.  Lane b
-    // holds the row of box b of a tile (block ids read one tile ahead, so
-    // table reads never sit between TMA issues); lane 0 issues the copies.
+  if (warp >= 8) {
+   setmaxnreg_dec<kRegsCtl>();
+   if (warp == 9 || warp == 10) {
+    // ---------------- TMA producers: warp 9 loads Q and K, warp 10 V ----
+    // Each ring is filled in tile order; K_j waits for the QKs of tile
+    // j - kKst, V_j for the PVs of tile j - kVst.  Small blocks take one box
+    // per block and 64-column half (16 copies per 128-key tile for 16-token
+    // blocks), so K and V are issued by separate warps.  Lane b holds the
+    // row of box b of a tile (block ids are read one tile ahead, so table
+    // reads never sit between copies); lane 0 issues the copies.
+    const bool is_k = warp == 9;
+    const CUtensorMap *map = is_k ? &kmap : &vmap;
+    const int nst = is_k ? kKst : kVst;
+    uint8_t *ring = smem + (is_k ? kOffK : kOffV);
+    uint64_t *full = is_k ? k_full : v_full;
+    uint64_t *empty = is_k ? k_empty : v_empty;
     const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
     const int br = p.bs < 128 ? p.bs : 128;
     const int nbox = 128 / br;  // <= 8
-    const bool paired = p.paired != 0;
     auto tile_rows = [&](int j) {
       const int key = j * 128 + lane * br;
       int32_t y = p.rows_total;
@@ -125,29 +141,12 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         const int32_t blk = __ldg(bt + key / p.bs);
         if (blk >= 0 && blk < p.num_blocks)
           y = (blk * p.hkv + it.kv_head) * p.bs + key % p.bs;
-        else
+        else if (is_k)
           record_error(p.err, kErrBadBlock);
       }
       return y;
     };
-    auto issue = [&](const CUtensorMap *map, uint8_t *dst, uint64_t *bar, int j, int32_t yv) {
-      int n = 0;
-      for (int r = 0; r < 128; r += br)
-        if (j * 128 + r < k_end) ++n;
-      if (lane == 0) mbar_arrive_expect_tx(bar, n * br * 128 * 2);
-      for (int bx = 0; bx < n; ++bx) {
-        const int32_t y = __shfl_sync(0xffffffffu, yv, bx);
-        if (lane == 0) {
-          if (paired) {
-            tma_load_3d(dst + bx * 4096, map, 0, y, 0, bar);
-          } else {
-            tma_load_2d(dst + bx * br * 128, map, 0, y, bar);
-            tma_load_2d(dst + kHalf + bx * br * 128, map, 64, y, bar);
-          }
-        }
-      }
-    };
-    if (lane == 0) {
+    if (is_k && lane == 0) {
       mbar_arrive_expect_tx(q_full, two ? 2 * kTile : kTile);
       const int t0 = it.tok0 + it.row0 / G;
       tma_load_3d(smem + kOffQ, &qmap, 0, it.kv_head * G, t0, q_full);
@@ -158,39 +157,38 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         tma_load_3d(smem + kOffQ + kTile + kHalf, &qmap, 64, it.kv_head * G, t1, q_full);
       }
     }
-    int32_t y_cur = tile_rows(0);   // rows of tile j (for K_j)
-    int32_t y_prev = 0;             // rows of tile j-1 (for V_{j-1})
-    for (int j = 0; j <= n_tiles; ++j) {
+    int32_t y_cur = tile_rows(0);
+    for (int j = 0; j < n_tiles; ++j) {
       const int32_t y_next = tile_rows(j + 1);
-      if (j < n_tiles) {
-        const int s = j % kKst;
-        if (j >= kKst &&
-            !__all_sync(0xffffffffu, mbar_wait(&k_empty[s], ((j / kKst) - 1) & 1))) {
-          if (lane == 0) record_error(p.err, kErrTimeout);
-          break;
-        }
-        issue(&kmap, smem + kOffK + s * kTile, &k_full[s], j, y_cur);
+      const int s = j % nst;
+      if (j >= nst &&
+          !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((j / nst) - 1) & 1))) {
+        if (lane == 0) record_error(p.err, kErrTimeout);
+        break;
       }
-      if (j >= 1) {
-        const int i = j - 1, s = i % kVst;
-        if (i >= kVst &&
-            !__all_sync(0xffffffffu, mbar_wait(&v_empty[s], ((i / kVst) - 1) & 1))) {
-          if (lane == 0) record_error(p.err, kErrTimeout);
-          break;
+      uint8_t *dst = ring + s * kTile;
+      int n = 0;
+      for (int r = 0; r < 128; r += br)
+        if (j * 128 + r < k_end) ++n;
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], n * br * 128 * 2);
+      for (int bx = 0; bx < n; ++bx) {
+        const int32_t y = __shfl_sync(0xffffffffu, y_cur, bx);
+        if (lane == 0) {
+          tma_load_2d(dst + bx * br * 128, map, 0, y, &full[s]);
+          tma_load_2d(dst + kHalf + bx * br * 128, map, 64, y, &full[s]);
         }
-        issue(&vmap, smem + kOffV + s * kTile, &v_full[s], i, y_prev);
       }
-      y_prev = y_cur;
       y_cur = y_next;
     }
-  } else if (warp == 8) {
+   } else if (warp == 8) {
     // ---------------- MMA issuer (one thread) ----------------
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0);
       auto qk = [&](int t, int j) {   // S_t = Q_t K_j^T
         const int s = j % kKst;
+        // K arrives by TMA (async proxy, like the MMA): the mbarrier alone
+        // orders it, and a tcgen05 fence here would drain the MMA pipe
         if (!mbar_wait(&k_full[s], (j / kKst) & 1)) return false;
-        tc_fence_after();
         const uint32_t qa = smem_addr(smem + kOffQ + t * kTile);
         const uint32_t ka = smem_addr(smem + kOffK + s * kTile);
         const uint32_t d = tmem + t * 128;
@@ -198,14 +196,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
           const uint64_t ad = smem_desc_sw128(qa + off, 16, 1024);
-          if (p.paired) {
-            const uint32_t koff = (ks >> 2) * 2048 + (ks & 3) * 32;
-            tc_mma(d, ad, smem_desc_sw128(ka + koff, 16, 4096), kIdescQK64, ks > 0 ? 1u : 0u);
-            tc_mma(d + 64, ad, smem_desc_sw128(ka + koff + 1024, 16, 4096), kIdescQK64,
-                   ks > 0 ? 1u : 0u);
-          } else {
-            tc_mma(d, ad, smem_desc_sw128(ka + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
-          }
+          tc_mma(d, ad, smem_desc_sw128(ka + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[t]);
         return true;
@@ -218,9 +209,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         const uint32_t va = smem_addr(smem + kOffV + s * kTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd =
-              p.paired ? smem_desc_sw128(va + (kk >> 2) * 1024 + (kk & 3) * 8192, 2048, 4096)
-                       : smem_desc_sw128(va + kk * 2048, kHalf, 1024);
+          const uint64_t bd = smem_desc_sw128(va + kk * 2048, kHalf, 1024);
           tc_mma_tmem_a(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, bd, kIdescPV,
                         (j > 0 || kk > 0) ? 1u : 0u);
         }
@@ -233,22 +222,26 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       if (ok) tc_commit(&k_empty[0]);
       // P_t(j) lives where QK_t(j+1) writes: QK_t(j+1) is issued after
       // PV_t(j) (tcgen05.mma of one thread execute in order).
+      // V_j is released as soon as its last PV is issued, K_{j+1} after its
+      // last QK.
       for (int j = 0; ok && j < n_tiles; ++j) {
         if (j < nt0) {
           ok = pv(0, j);
           if (ok && j + 1 < nt0) ok = qk(0, j + 1);
         }
-        if (ok && two && j < nt1) {
-          ok = pv(1, j);
-          if (ok && j + 1 < nt1) ok = qk(1, j + 1);
-        }
+        const bool t1 = two && j < nt1;
+        if (ok && t1) ok = pv(1, j);
         if (!ok) break;
         tc_commit(&v_empty[j % kVst]);
+        if (t1 && j + 1 < nt1) ok = qk(1, j + 1);
+        if (!ok) break;
         if (j + 1 < n_tiles) tc_commit(&k_empty[(j + 1) % kKst]);
       }
       if (!ok) record_error(p.err, kErrTimeout);
     }
+   }
   } else {
+    setmaxnreg_inc<kRegsSoftmax>();
     // ---------------- softmax / epilogue: thread r of tile t owns row r ----
     const int t = warp >> 2;                   // Q tile of this warpgroup
     const int r = threadIdx.x & 127;
@@ -278,7 +271,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       if (key0 + 127 > pos) {   // diagonal tile: causal mask
 #pragma unroll
         for (int k = 0; k < 128; ++k) {
-          const int key = key0 + (p.paired ? paired_key(k) : k);
+          const int key = key0 + k;
           s[k] = key > pos ? -CUDART_INF_F : s[k];
         }
       }
@@ -345,8 +338,8 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         }
         if (r >= vvalid) {   // thread r clears the V row of tile-local key r
           const uint32_t vt = smem_addr(smem + kOffV + vs * kTile);
-          const uint32_t vrow = p.paired ? vt + (r >> 4) * 4096 + (r & 15) * 128 : vt + r * 128;
-          const uint32_t hstep = p.paired ? 2048u : kHalf;
+          const uint32_t vrow = vt + r * 128;
+          const uint32_t hstep = kHalf;
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
