@@ -44,6 +44,31 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (d0, d1) = (a0 b + c, a1 b + c) and (d0, d1) += (a0, a1) as packed f32x2
+// operations (each lane rounds like fmaf / a plain add).
+__device__ __forceinline__ void fma2_bc(float &d0, float &d1, float a0, float a1, float b,
+                                        float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
+      "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b,
                                        uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b),
@@ -277,13 +302,13 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       }
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[8 + i]);
 #pragma unroll
-      for (int k = 8; k < 128; k += 8)
+      for (int k = 16; k < 128; k += 16)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[k + i]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[k + i], s[k + 8 + i]);
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                             fmaxf(mx[6], mx[7]));
       const float mt2 = mt * c;
       float alpha = 1.f;
       bool rescale = false;
@@ -300,10 +325,10 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float e0 = ex2(fmaf(s[64 * hh + 2 * k], c, -m));
-          const float e1 = ex2(fmaf(s[64 * hh + 2 * k + 1], c, -m));
-          acc[(2 * k) & 7] += e0;
-          acc[(2 * k + 1) & 7] += e1;
+          float x0, x1;
+          fma2_bc(x0, x1, s[64 * hh + 2 * k], s[64 * hh + 2 * k + 1], c, -m);
+          const float e0 = ex2(x0), e1 = ex2(x1);
+          add2(acc[(2 * k) & 7], acc[(2 * k + 1) & 7], e0, e1);
           pk[k] = pack_bf16(e0, e1);
         }
         tmem_st32u(lane_addr + col_s + 32 * hh, pk);
