@@ -159,6 +159,26 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q,
                                 void *stream);
 
 /*
+ * Prepare a step for CUDA-graph capture.  Small steps are dominated by
+ * launch overhead unless captured in a CUDA graph (page "vLLM 优化
+ * DeepSeek-V4.1-Flash：智能体吞吐提升 5 倍", section "裁剪层的 CUDA graphs");
+ * the calls of this library can be captured the same way.  This call plans the
+ * step from the host mirrors (same meaning as in pkv_attention_varlen) and
+ * copies the work list into a device buffer kept for captured steps; it is
+ * synchronous and may allocate that buffer (once per handle), so call it
+ * before cudaStreamBeginCapture.  While `stream` is capturing,
+ * pkv_attention_varlen enqueues kernels only, reading this prepared work
+ * list: its host mirrors must equal the prepared ones (else
+ * PKV_ERR_INVALID_ARG and nothing is enqueued), and the graph replays that
+ * plan as long as the handle lives and no later pkv_graph_prepare replaces
+ * it.  pkv_write_slots needs no preparation.  Timing (PKV_FLAG_TIMING)
+ * records nothing for captured calls.
+ */
+pkv_status pkv_graph_prepare(pkv_handle *h, const int32_t *query_start_loc_host,
+                             const int32_t *seq_lens_host, int32_t num_seqs,
+                             int32_t num_tokens);
+
+/*
  * Wait for the handle's device (cudaDeviceSynchronize) and read the device
  * error word, clearing it.  Returns PKV_OK, PKV_ERR_DEVICE_CHECK (validate
  * mode found a bad block id, slot or host-mirror mismatch),

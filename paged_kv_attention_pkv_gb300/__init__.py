@@ -31,7 +31,7 @@ KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL, KERNEL_MIXED = 0, 1, 2, 3
 EXPORTS = ["pkv_create", "pkv_write_slots", "pkv_attention_varlen",
            "pkv_check_device_errors", "pkv_status_string", "pkv_last_error",
            "pkv_destroy", "pkv_plan", "pkv_timing_reset", "pkv_timing_read",
-           "pkv_decode_static"]
+           "pkv_decode_static", "pkv_graph_prepare"]
 
 
 class PkvError(RuntimeError):
@@ -78,6 +78,8 @@ def load(path: str | None = None):
                                          vp, vp, i32, i32, vp, vp, vp]
     lib.pkv_check_device_errors.restype = ctypes.c_int
     lib.pkv_check_device_errors.argtypes = [vp]
+    lib.pkv_graph_prepare.restype = ctypes.c_int
+    lib.pkv_graph_prepare.argtypes = [vp, vp, vp, i32, i32]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_last_error.restype = ctypes.c_char_p
@@ -204,6 +206,15 @@ class Handle:
             int(block_tables.shape[1]), _ptr(qslh), _ptr(lenh), int(lenh.shape[0]),
             int(q.shape[0]), _ptr(out), _ptr(lse), _stream(stream, self.device)))
         return out, lse
+
+    def graph_prepare(self, query_start_loc_host, seq_lens_host, num_tokens=None) -> None:
+        """pkv_graph_prepare: plan a step for CUDA-graph capture (synchronous;
+        call before capturing attention_varlen with the same host mirrors)."""
+        qslh = _host_i32(query_start_loc_host)
+        lenh = _host_i32(seq_lens_host)
+        nt = int(qslh[-1]) if num_tokens is None else int(num_tokens)
+        self._check(self._lib.pkv_graph_prepare(self._h, _ptr(qslh), _ptr(lenh),
+                                                int(lenh.shape[0]), nt))
 
     def check_device_errors(self) -> None:
         """pkv_check_device_errors: raise PkvError if the device recorded one."""

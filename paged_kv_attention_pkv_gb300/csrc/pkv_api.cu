@@ -87,6 +87,12 @@ struct pkv_handle {
   // cached pool descriptors
   const void *map_k_ptr = nullptr, *map_v_ptr = nullptr;
   CUtensorMap dec_k{}, dec_v{}, pf_k{}, pf_v{};
+  // CUDA-graph capture: a step prepared by pkv_graph_prepare (work list and
+  // mirrors in their own device buffer, lengths kept to check the capture)
+  uint8_t *d_graph_work = nullptr;
+  bool graph_ready = false;
+  std::vector<int32_t> graph_qsl, graph_lens;
+  bool capturing = false;   // set while a call enqueues onto a capturing stream
 };
 
 namespace {
@@ -288,13 +294,28 @@ bool encode_q_map(CUtensorMap *m, const void *q, int hq, int group, int64_t toke
 // (block, KV head) tile of 4 KB as [half][16 rows][64], 128-byte swizzled.
 size_t items_bytes(int max_items) { return sizeof(pkv_work_item) * size_t(max_items); }
 
+// Lays out a plan's work items (decode items, then prefill tiles) at `dst`,
+// and the host mirrors at dst + mirror_off in validate mode; returns the
+// bytes of the work items.
+size_t stage_plan(const Plan &plan, const int32_t *qsl_host, const int32_t *lens_host,
+                  int num_seqs, bool validate, size_t mirror_off, uint8_t *dst) {
+  std::memcpy(dst, plan.dec.data(), items_bytes(plan.dec.size()));
+  std::memcpy(dst + items_bytes(plan.dec.size()), plan.pre.data(), items_bytes(plan.pre.size()));
+  if (validate) {
+    std::memcpy(dst + mirror_off, qsl_host, sizeof(int32_t) * (num_seqs + 1));
+    std::memcpy(dst + mirror_off + sizeof(int32_t) * (num_seqs + 1), lens_host,
+                sizeof(int32_t) * num_seqs);
+  }
+  return items_bytes(plan.dec.size() + plan.pre.size());
+}
+
 void timing_begin(pkv_handle *h, int kind, cudaStream_t s) {
-  if (!h->timing) return;
+  if (!h->timing || h->capturing) return;
   TimingRing &r = h->rings[kind];
   cudaEventRecord(r.start[r.count % kTimingSlots], s);
 }
 void timing_end(pkv_handle *h, int kind, cudaStream_t s) {
-  if (!h->timing) return;
+  if (!h->timing || h->capturing) return;
   TimingRing &r = h->rings[kind];
   cudaEventRecord(r.stop[r.count % kTimingSlots], s);
   ++r.count;
@@ -400,6 +421,7 @@ pkv_status pkv_destroy(pkv_handle *h) {
   cudaSetDevice(h->device);
   cudaDeviceSynchronize();
   cudaFree(h->d_work);
+  cudaFree(h->d_graph_work);
   cudaFree(h->d_part_o);
   cudaFree(h->d_part_lse);
   cudaFree(h->d_tickets);
@@ -453,6 +475,9 @@ pkv_status pkv_write_slots(pkv_handle *h, const void *k_new, const void *v_new,
   p.num_blocks = h->cfg.num_blocks;
   p.validate = (h->cfg.flags & PKV_FLAG_VALIDATE) != 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if ((e = cudaStreamIsCapturing(s, &cap)) != cudaSuccess) return cuda_fail(h, e, "capture query");
+  h->capturing = cap != cudaStreamCaptureStatusNone;
   timing_begin(h, PKV_KERNEL_APPEND, s);
   e = launch_append(p, fp8, s);
   timing_end(h, PKV_KERNEL_APPEND, s);
@@ -506,6 +531,16 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
   cudaError_t e = cudaSetDevice(h->device);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if ((e = cudaStreamIsCapturing(s, &cap)) != cudaSuccess) return cuda_fail(h, e, "capture query");
+  h->capturing = cap != cudaStreamCaptureStatusNone;
+  if (h->capturing &&
+      !(h->graph_ready && int(h->graph_lens.size()) == num_seqs &&
+        std::equal(h->graph_lens.begin(), h->graph_lens.end(), lens_host) &&
+        std::equal(h->graph_qsl.begin(), h->graph_qsl.end(), qsl_host)))
+    return fail(h, PKV_ERR_INVALID_ARG,
+                "a captured step needs pkv_graph_prepare with the same query_start_loc and "
+                "seq_lens first");
 
   // pool descriptors (re-encoded when the pools move)
   if (k_cache != h->map_k_ptr || v_cache != h->map_v_ptr) {
@@ -525,36 +560,34 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
     h->map_v_ptr = v_cache;
   }
 
-  // stage the work list (+ host mirrors for validate mode) and upload it
-  const int cur = h->stage_cur;
-  h->stage_cur ^= 1;
-  e = cudaEventSynchronize(h->staged[cur]);   // this buffer's previous copy is done
-  if (e != cudaSuccess) return cuda_fail(h, e, "staging event");
-  uint8_t *hs = h->h_stage[cur];
-  size_t nbytes = items_bytes(n_items);
-  std::memcpy(hs, plan.dec.data(), items_bytes(plan.dec.size()));
-  std::memcpy(hs + items_bytes(plan.dec.size()), plan.pre.data(), items_bytes(plan.pre.size()));
+  // the work list (+ host mirrors for validate mode) in device memory
   const bool validate = (c.flags & PKV_FLAG_VALIDATE) != 0;
   const size_t mirror_off = items_bytes(h->max_items);
-  if (validate) {
-    std::memcpy(hs + mirror_off, qsl_host, sizeof(int32_t) * (num_seqs + 1));
-    std::memcpy(hs + mirror_off + sizeof(int32_t) * (num_seqs + 1), lens_host,
-                sizeof(int32_t) * num_seqs);
+  uint8_t *work = h->d_work;
+  if (h->capturing) {
+    work = h->d_graph_work;   // uploaded by pkv_graph_prepare: nothing to copy
+  } else {
+    const int cur = h->stage_cur;
+    h->stage_cur ^= 1;
+    e = cudaEventSynchronize(h->staged[cur]);   // this buffer's previous copy is done
+    if (e != cudaSuccess) return cuda_fail(h, e, "staging event");
+    uint8_t *hs = h->h_stage[cur];
+    const size_t nbytes = stage_plan(plan, qsl_host, lens_host, num_seqs, validate, mirror_off, hs);
+    e = cudaMemcpyAsync(h->d_work, hs, nbytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && validate)
+      e = cudaMemcpyAsync(h->d_work + mirror_off, hs + mirror_off,
+                          sizeof(int32_t) * (2 * num_seqs + 1), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaEventRecord(h->staged[cur], s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "work-list upload");
   }
-  e = cudaMemcpyAsync(h->d_work, hs, nbytes, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess && validate)
-    e = cudaMemcpyAsync(h->d_work + mirror_off, hs + mirror_off,
-                        sizeof(int32_t) * (2 * num_seqs + 1), cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaEventRecord(h->staged[cur], s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "work-list upload");
-  const pkv_work_item *d_items = reinterpret_cast<const pkv_work_item *>(h->d_work);
+  const pkv_work_item *d_items = reinterpret_cast<const pkv_work_item *>(work);
 
   if (validate) {
     CheckParams cp{};
     cp.qsl = query_start_loc;
     cp.seq_lens = seq_lens;
     cp.block_tables = block_tables;
-    cp.qsl_expect = reinterpret_cast<const int32_t *>(h->d_work + mirror_off);
+    cp.qsl_expect = reinterpret_cast<const int32_t *>(work + mirror_off);
     cp.seq_lens_expect = cp.qsl_expect + num_seqs + 1;
     cp.bt_stride = block_table_stride;
     cp.num_seqs = num_seqs;
@@ -633,6 +666,39 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
     timing_end(h, PKV_KERNEL_PREFILL, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
   }
+  return PKV_OK;
+}
+
+pkv_status pkv_graph_prepare(pkv_handle *h, const int32_t *qsl_host,
+                             const int32_t *lens_host, int32_t num_seqs,
+                             int32_t num_tokens) {
+  if (h == nullptr) return PKV_ERR_INVALID_ARG;
+  h->last_error.clear();
+  const pkv_config &c = h->cfg;
+  if (num_seqs > c.max_num_seqs || num_tokens > c.max_num_tokens)
+    return fail(h, PKV_ERR_INVALID_ARG, "step larger than the handle serves");
+  Plan plan;
+  pkv_status st;
+  std::string msg = make_plan(c, qsl_host, lens_host, num_seqs, num_tokens, h->num_sms,
+                              kMaxPartials, &plan, &st);
+  if (st != PKV_OK) return fail(h, st, msg);
+  const int n_items = static_cast<int>(plan.dec.size() + plan.pre.size());
+  if (n_items > h->max_items)
+    return fail(h, PKV_ERR_WORKSPACE, fmt("step needs %d work items, workspace holds %d", n_items, h->max_items));
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  h->graph_ready = false;
+  if (h->d_graph_work == nullptr && (e = cudaMalloc(&h->d_graph_work, h->work_bytes)) != cudaSuccess)
+    return fail(h, PKV_ERR_OUT_OF_MEMORY, fmt("graph work list: %s", cudaGetErrorString(e)));
+  std::vector<uint8_t> host(h->work_bytes, 0);
+  const size_t mirror_off = items_bytes(h->max_items);
+  stage_plan(plan, qsl_host, lens_host, num_seqs, true, mirror_off, host.data());
+  // synchronous on purpose: the buffer must hold this plan before any replay
+  if ((e = cudaMemcpy(h->d_graph_work, host.data(), h->work_bytes, cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail(h, e, "graph work-list upload");
+  h->graph_qsl.assign(qsl_host, qsl_host + num_seqs + 1);
+  h->graph_lens.assign(lens_host, lens_host + num_seqs);
+  h->graph_ready = true;
   return PKV_OK;
 }
 
