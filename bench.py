@@ -396,8 +396,54 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def time_graph(index, steps: int, device: str) -> dict:
+    """One step (append + attention) of a workload issued eagerly `steps`
+    times back to back, against the same step captured once in a CUDA graph
+    and replayed `steps` times; CUDA events around each whole loop, so host
+    enqueue time shows wherever it exceeds the GPU time."""
+    import paged_kv_attention_pkv_gb300 as pkv
+    spec = W.config_spec(index)
+    batch = W.generate(spec, device)
+    h = make_handle(batch, 0)
+    m = device_meta(batch)
+    out = torch.empty_like(batch.q)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        h.write_slots(batch.k_new, batch.v_new, m["slots"], batch.k_cache,
+                      batch.v_cache, batch.k_scale, batch.v_scale)
+        h.attention_varlen(batch.q, batch.k_cache, batch.v_cache, m["qsl"], m["lens"],
+                           m["bt"], batch.qsl, batch.seq_lens, out=out,
+                           k_scale=batch.k_scale, v_scale=batch.v_scale)
+
+    def loop(fn):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    eager_ms = loop(step)
+    h.graph_prepare(batch.qsl, batch.seq_lens)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    graph_ms = loop(g.replay)
+    h.close()
+    del g, batch
+    torch.cuda.empty_cache()
+    return {"workload": spec.name, "steps": steps, "eager_ms_per_step": round(eager_ms, 5),
+            "graph_ms_per_step": round(graph_ms, 5), "speedup": round(eager_ms / graph_ms, 3)}
+
+
 def secondary(args, world, peaks, device):
     out = []
+    out.append({"cuda_graph": [time_graph(0, 500, device), time_graph(1, 200, device)]})
     for idx, steps in ((2, 10), (3, 10), (4, 50)):
         r = time_workload(idx, steps, 3, world, peaks, device)
         spec, work = r["spec"], r["work"]
