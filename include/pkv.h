@@ -159,6 +159,56 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q,
                                 void *stream);
 
 /*
+ * Decode context parallelism, emulated on one GPU.  DCP deals a request's KV
+ * tokens out to N ranks in runs of `interleave` tokens (run j to rank j % N);
+ * each rank attends with all query heads to its own share, producing a
+ * partial output and its log-sum-exp, and the partials are exchanged and
+ * merged with log-sum-exp weights (page "vLLM Agentic 推理｜面向 Agent 负载的
+ * 推理优化", sections 4.3.1 and 4.3.3).  Here every shard reads its share
+ * from the one shared pool.
+ *
+ * pkv_attention_partial: shard `shard` (0 <= shard < num_shards) of one step,
+ * decode rows only (q_i * G <= 8; a request with more rows returns
+ * PKV_ERR_UNSUPPORTED).  Arguments as for pkv_attention_varlen, except:
+ *  interleave  tokens per run, a positive multiple of the decode stage (16
+ *              keys for bf16 pools, 32 for E4M3; the pages' default of 1 is
+ *              not supported on the GPU and returns PKV_ERR_UNSUPPORTED);
+ *  out         [num_tokens][Hq][128] fp32, device: the shard's softmax-
+ *              normalised partial output (0 where the shard owns no visible
+ *              key);
+ *  lse         [num_tokens][Hq] fp32, device: its natural-log log-sum-exp
+ *              (-inf where the shard owns no visible key).  Required.
+ * Not capturable in a CUDA graph (PKV_ERR_UNSUPPORTED while capturing).
+ */
+pkv_status pkv_attention_partial(pkv_handle *h, const void *q,
+                                 const void *k_cache, const void *v_cache,
+                                 const float *k_scale, const float *v_scale,
+                                 const int32_t *query_start_loc,
+                                 const int32_t *seq_lens,
+                                 const int32_t *block_tables,
+                                 int32_t block_table_stride,
+                                 const int32_t *query_start_loc_host,
+                                 const int32_t *seq_lens_host, int32_t num_seqs,
+                                 int32_t num_tokens, int32_t shard,
+                                 int32_t num_shards, int32_t interleave,
+                                 float *out, float *lse, void *stream);
+
+/*
+ * The merge step: for each of num_rows rows, lse = ln sum_s exp(lse_s) and
+ * out = sum_s exp(lse_s - lse) * o_s over the num_parts partials (parts with
+ * lse_s = -inf contribute nothing; a row with no part gets 0 and -inf).
+ *  parts_o    [num_parts][num_rows][128] fp32, device, 16-byte aligned;
+ *  parts_lse  [num_parts][num_rows] fp32, device (natural log);
+ *  out        [num_rows][128] bf16, device (written);
+ *  lse        NULL or [num_rows] fp32, device (written).
+ * With the rows of pkv_attention_partial (num_rows = num_tokens * Hq) this
+ * is the exchange-then-merge of DCP; the partials may come from any source.
+ */
+pkv_status pkv_lse_merge(pkv_handle *h, const float *parts_o,
+                         const float *parts_lse, int32_t num_parts,
+                         int64_t num_rows, void *out, float *lse, void *stream);
+
+/*
  * Prepare a step for CUDA-graph capture.  Small steps are dominated by
  * launch overhead unless captured in a CUDA graph (page "vLLM 优化
  * DeepSeek-V4.1-Flash：智能体吞吐提升 5 倍", section "裁剪层的 CUDA graphs");

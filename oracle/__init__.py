@@ -56,6 +56,7 @@ def load(path: str | None = None):
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, _u16p, _i32p, _i32p, _i32p, ctypes.c_int64, ctypes.c_int,
         ctypes.c_int64, ctypes.c_double, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_void_p, ctypes.c_int64, _f64p, _f64p]
     lib.pko_lse_merge.restype = None
     lib.pko_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p,
@@ -119,13 +120,16 @@ def attention(k_cache: np.ndarray, v_cache: np.ndarray, q: np.ndarray,
               qsl: np.ndarray, seq_lens: np.ndarray, block_tables: np.ndarray,
               softmax_scale: float, k_scale: np.ndarray | None = None,
               v_scale: np.ndarray | None = None, rows: np.ndarray | None = None,
-              k_range: tuple[int, int] | None = None, lib=None):
+              k_range: tuple[int, int] | None = None,
+              shard: tuple[int, int, int] | None = None, lib=None):
     """Paged varlen attention in fp64.
 
     ``q`` is ``[T, Hq, D]`` uint16 (bf16 bits).  Returns ``(out, lse)``:
     ``out`` is ``[nrows, D]`` float64 and ``lse`` ``[nrows]`` float64, where
     the rows are ``rows`` (indices ``token * Hq + head``) or all ``T * Hq``.
-    ``k_range`` restricts keys to logical positions ``[lo, hi)``.
+    ``k_range`` restricts keys to logical positions ``[lo, hi)``; ``shard =
+    (n, r, k)`` to the keys context-parallel rank ``r`` of ``n`` owns when
+    tokens are dealt out in runs of ``k`` (run ``j`` to rank ``j % n``).
     """
     lib = lib or load()
     fp8 = k_cache.dtype == np.uint8
@@ -150,6 +154,7 @@ def attention(k_cache: np.ndarray, v_cache: np.ndarray, q: np.ndarray,
         int(fp8), _ptr(k_cache), _ptr(v_cache), _ptr(ks), _ptr(vs), nb, hkv, d,
         bs, hq, np.ascontiguousarray(q), qsl, seq_lens, bt, bt.shape[1],
         int(seq_lens.shape[0]), t, float(softmax_scale), int(lo), int(hi),
+        *((1, 0, 1) if shard is None else tuple(int(x) for x in shard)),
         _ptr(rows), nrows, out, lse)
     if st != 0:
         raise ValueError(f"oracle attention rejected its arguments ({st})")

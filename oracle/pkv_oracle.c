@@ -22,6 +22,10 @@
  *    Agentic 推理", section 4.3.1.
  *  - Partial results over disjoint key sets merge through their log-sum-exp.
  *    Page "vLLM Agentic 推理", section 4.3.3 (step 4, online-softmax merge).
+ *  - Decode context parallelism: a request's KV tokens are dealt out to N
+ *    ranks in runs of `interleave` tokens (interleave 1: token i on rank
+ *    i % N); each rank attends to its own tokens only.  Page "vLLM Agentic
+ *    推理", sections 4.3.1 and 4.3.3 (step 3).
  *
  * The pages never print the attention formula.  The reading taken here is
  * the plain one: scaled dot-product softmax attention, key j visible to the
@@ -210,9 +214,17 @@ static double pool_elem(const pool_t *p, int is_v, const int32_t *bt,
  * log-sum-exp of the scaled scores to *lse.  With no visible key the result
  * is out = 0, lse = -inf (the identity of the merge).
  */
+/* Does context-parallel rank r of n own key j (runs of k tokens dealt out
+ * in turn)?  n <= 1: every key. */
+static int owns_key(int64_t j, int64_t n, int64_t r, int64_t k)
+{
+    return n <= 1 || (j / k) % n == r;
+}
+
 static int attend_one(const pool_t *p, const uint16_t *qrow, const int32_t *bt,
                       int64_t pos, int kvh, double softmax_scale, int64_t k_lo,
-                      int64_t k_hi, double *scores, double *out, double *lse)
+                      int64_t k_hi, int64_t sn, int64_t sr, int64_t sk,
+                      double *scores, double *out, double *lse)
 {
     int64_t hi = k_hi < pos + 1 ? k_hi : pos + 1; /* causal: j <= pos */
     int d = p->d;
@@ -224,6 +236,8 @@ static int attend_one(const pool_t *p, const uint16_t *qrow, const int32_t *bt,
     }
     double m = -INFINITY;
     for (int64_t j = k_lo; j < hi; ++j) {
+        if (!owns_key(j, sn, sr, sk))
+            continue;
         double s = 0.0;
         for (int i = 0; i < d; ++i)
             s += pko_bf16_value(qrow[i]) * pool_elem(p, 0, bt, j, kvh, i);
@@ -232,8 +246,14 @@ static int attend_one(const pool_t *p, const uint16_t *qrow, const int32_t *bt,
         if (s > m)
             m = s;
     }
+    if (m == -INFINITY) { /* no owned key is visible */
+        *lse = -INFINITY;
+        return 0;
+    }
     double l = 0.0;
     for (int64_t j = k_lo; j < hi; ++j) {
+        if (!owns_key(j, sn, sr, sk))
+            continue;
         double w = exp(scores[j - k_lo] - m);
         l += w;
         for (int i = 0; i < d; ++i)
@@ -250,7 +270,9 @@ static int attend_one(const pool_t *p, const uint16_t *qrow, const int32_t *bt,
  * [qsl[i], qsl[i+1]) of q ([T][hq][d] bf16 bits) and has seq_lens[i] context
  * tokens including those new ones; its block table is
  * block_tables[i * bt_stride ...].  Keys are restricted to [k_lo, k_hi) in
- * logical position (k_lo = 0, k_hi = INT64_MAX for full attention).
+ * logical position (k_lo = 0, k_hi = INT64_MAX for full attention), and to
+ * the keys context-parallel rank shard_r of shard_n owns with runs of
+ * shard_k tokens (shard_n <= 1: no restriction).
  *
  * rows: indices (token * hq + head) to evaluate, or NULL for all T*hq rows in
  * order.  out receives nrows * d doubles, lse nrows doubles.
@@ -262,11 +284,14 @@ int pko_attention(int kv_fp8, const void *k_cache, const void *v_cache,
                   const int32_t *seq_lens, const int32_t *block_tables,
                   int64_t bt_stride, int num_seqs, int64_t num_tokens,
                   double softmax_scale, int64_t k_lo, int64_t k_hi,
+                  int64_t shard_n, int64_t shard_r, int64_t shard_k,
                   const int64_t *rows, int64_t nrows, double *out,
                   double *lse)
 {
     if (hkv <= 0 || hq <= 0 || hq % hkv != 0 || d <= 0 || bs <= 0 ||
         num_seqs < 0 || num_tokens < 0)
+        return PKO_BAD_ARG;
+    if (shard_n > 1 && (shard_r < 0 || shard_r >= shard_n || shard_k < 1))
         return PKO_BAD_ARG;
     if (qsl[0] != 0 || qsl[num_seqs] != num_tokens)
         return PKO_BAD_ARG;
@@ -317,7 +342,8 @@ int pko_attention(int kv_fp8, const void *k_cache, const void *v_cache,
             int64_t pos = hist + t;
             attend_one(&p, q + ((size_t)tok * hq + head) * d,
                        block_tables + (size_t)i * bt_stride, pos, head / group,
-                       softmax_scale, k_lo, k_hi, scores, out + (size_t)r * d,
+                       softmax_scale, k_lo, k_hi, shard_n, shard_r, shard_k,
+                       scores, out + (size_t)r * d,
                        lse + r);
         }
         free(scores);

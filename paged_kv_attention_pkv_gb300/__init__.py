@@ -31,7 +31,8 @@ KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL, KERNEL_MIXED = 0, 1, 2, 3
 EXPORTS = ["pkv_create", "pkv_write_slots", "pkv_attention_varlen",
            "pkv_check_device_errors", "pkv_status_string", "pkv_last_error",
            "pkv_destroy", "pkv_plan", "pkv_timing_reset", "pkv_timing_read",
-           "pkv_decode_static", "pkv_graph_prepare"]
+           "pkv_decode_static", "pkv_graph_prepare", "pkv_attention_partial",
+           "pkv_lse_merge"]
 
 
 class PkvError(RuntimeError):
@@ -78,6 +79,11 @@ def load(path: str | None = None):
                                          vp, vp, i32, i32, vp, vp, vp]
     lib.pkv_check_device_errors.restype = ctypes.c_int
     lib.pkv_check_device_errors.argtypes = [vp]
+    lib.pkv_attention_partial.restype = ctypes.c_int
+    lib.pkv_attention_partial.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                          vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.pkv_lse_merge.restype = ctypes.c_int
+    lib.pkv_lse_merge.argtypes = [vp, vp, vp, i32, i64, vp, vp, vp]
     lib.pkv_graph_prepare.restype = ctypes.c_int
     lib.pkv_graph_prepare.argtypes = [vp, vp, vp, i32, i32]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -205,6 +211,40 @@ class Handle:
             _ptr(v_scale), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_tables),
             int(block_tables.shape[1]), _ptr(qslh), _ptr(lenh), int(lenh.shape[0]),
             int(q.shape[0]), _ptr(out), _ptr(lse), _stream(stream, self.device)))
+        return out, lse
+
+    def attention_partial(self, q, k_cache, v_cache, query_start_loc, seq_lens,
+                          block_tables, query_start_loc_host, seq_lens_host, shard,
+                          num_shards, interleave, out=None, lse=None, k_scale=None,
+                          v_scale=None, stream=None):
+        """pkv_attention_partial: one context-parallel shard's partial output
+        (fp32, ``[T, Hq, 128]``) and log-sum-exp (``[T, Hq]``)."""
+        qslh = _host_i32(query_start_loc_host)
+        lenh = _host_i32(seq_lens_host)
+        T, hq = q.shape[0], q.shape[1]
+        if out is None:
+            out = torch.empty((T, hq, q.shape[2]), dtype=torch.float32, device=q.device)
+        if lse is None:
+            lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
+        self._check(self._lib.pkv_attention_partial(
+            self._h, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+            _ptr(v_scale), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_tables),
+            int(block_tables.shape[1]), _ptr(qslh), _ptr(lenh), int(lenh.shape[0]),
+            int(T), int(shard), int(num_shards), int(interleave), _ptr(out), _ptr(lse),
+            _stream(stream, self.device)))
+        return out, lse
+
+    def lse_merge(self, parts_o, parts_lse, out=None, lse=None, stream=None):
+        """pkv_lse_merge: ``parts_o`` ``[N, rows..., 128]`` fp32 and
+        ``parts_lse`` ``[N, rows...]`` fp32 -> bf16 ``out`` ``[rows..., 128]``
+        (and ``lse`` if given)."""
+        n = parts_o.shape[0]
+        rows = parts_lse[0].numel()
+        if out is None:
+            out = torch.empty(parts_o.shape[1:], dtype=torch.bfloat16, device=parts_o.device)
+        self._check(self._lib.pkv_lse_merge(self._h, _ptr(parts_o), _ptr(parts_lse), int(n),
+                                            int(rows), _ptr(out), _ptr(lse),
+                                            _stream(stream, self.device)))
         return out, lse
 
     def graph_prepare(self, query_start_loc_host, seq_lens_host, num_tokens=None) -> None:

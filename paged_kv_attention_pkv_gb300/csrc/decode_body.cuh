@@ -32,6 +32,13 @@ __device__ __forceinline__ int32_t pool_row(const int32_t *bt, int32_t key,
   return (blk * p.hkv + kvh) * p.bs + key % p.bs;
 }
 
+// Global key of an item-local key: the identity, or the shard view (see
+// DecodeParams).  Keys of one stage stay consecutive.
+__device__ __forceinline__ int32_t global_key(const DecodeParams &p, int32_t x) {
+  if (p.dcp_n <= 1) return x;
+  return ((x / p.dcp_k) * p.dcp_n + p.dcp_r) * p.dcp_k + x % p.dcp_k;
+}
+
 // Physical head-dim index of a row of the O^T accumulator in the E4M3 path
 // (row dr of m-tile mt): the V fragments are built from 4-byte words, so each
 // thread's 4 consecutive bytes feed rows (g, g+8) of two adjacent m-tiles.
@@ -83,15 +90,15 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
     const int slot = i % kDecStages;
     uint8_t *kdst = ring + slot * kDecStageBytes;
     uint8_t *vdst = kdst + Tile::kKBytes;
+    const int gkey0 = global_key(p, key0);
     int boxes = 0;
     for (int r = 0; r < KS; r += br)
       if (key0 + r < ke) ++boxes;
     mbar_arrive_expect_tx(&full[slot], boxes * br * 128 * 2 * (FP8 ? 1 : 2));
     for (int r = 0; r < KS; r += br) {
-      const int key = key0 + r;
-      if (key >= ke) break;
+      if (key0 + r >= ke) break;
       int32_t blk;
-      const int32_t y = pool_row(bt, key, it.kv_head, p, &blk);
+      const int32_t y = pool_row(bt, gkey0 + r, it.kv_head, p, &blk);
       if constexpr (FP8) {
         tma_load_2d(kdst + r * 128, &kmap, 0, y, &full[slot]);
         tma_load_2d(vdst + r * 128, &vmap, 0, y, &full[slot]);
@@ -209,6 +216,7 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
     for (int sub = 0; sub < Tile::kSubs; ++sub) {
       const int k16 = key0 + 16 * sub;
       if (k16 >= ke) break;
+      const int g16 = global_key(p, key0) + 16 * sub;   // global key of k16
       // ---- S^T = K Q^T for 16 keys x 8 columns
       float s[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (FP8) {
@@ -238,7 +246,7 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       float sc0 = p.scale_log2, sc1 = p.scale_log2;
       float pv_scale = 1.f;
       if constexpr (FP8) {
-        const int32_t blk = __ldg(bt + k16 / p.bs);
+        const int32_t blk = __ldg(bt + g16 / p.bs);
         float sk = 0.f, sv = 0.f;
         if (blk >= 0 && blk < p.num_blocks) {
           const int64_t si = static_cast<int64_t>(blk) * p.hkv + it.kv_head;
@@ -249,11 +257,13 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
         sc1 *= sk * inv_sq1;
         pv_scale = sv;
       }
+      // validity on item-local keys, causality on global positions
       const int kr0 = k16 + g, kr1 = k16 + g + 8;
-      s[0] = (kr0 < ke && kr0 <= pos0) ? s[0] * sc0 : -CUDART_INF_F;
-      s[1] = (kr0 < ke && kr0 <= pos1) ? s[1] * sc1 : -CUDART_INF_F;
-      s[2] = (kr1 < ke && kr1 <= pos0) ? s[2] * sc0 : -CUDART_INF_F;
-      s[3] = (kr1 < ke && kr1 <= pos1) ? s[3] * sc1 : -CUDART_INF_F;
+      const int gr0 = g16 + g, gr1 = g16 + g + 8;
+      s[0] = (kr0 < ke && gr0 <= pos0) ? s[0] * sc0 : -CUDART_INF_F;
+      s[1] = (kr0 < ke && gr0 <= pos1) ? s[1] * sc1 : -CUDART_INF_F;
+      s[2] = (kr1 < ke && gr1 <= pos0) ? s[2] * sc0 : -CUDART_INF_F;
+      s[3] = (kr1 < ke && gr1 <= pos1) ? s[3] * sc1 : -CUDART_INF_F;
       float tm0 = fmaxf(s[0], s[2]);
       float tm1 = fmaxf(s[1], s[3]);
 #pragma unroll
@@ -376,7 +386,10 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
     const int r = it.row0 + n;
     const int64_t row = static_cast<int64_t>(it.tok0 + r / group) * p.hq +
                         it.kv_head * group + r % group;
-    p.out[row * kHeadDim + d] = __float2bfloat16_rn(o);
+    if (p.out_f32 != nullptr)
+      p.out_f32[row * kHeadDim + d] = o;
+    else
+      p.out[row * kHeadDim + d] = __float2bfloat16_rn(o);
     if (d == 0 && p.lse != nullptr) p.lse[row] = lse2 * kLn2;
   };
   for (int n = n_first; n < it.n_rows; n += n_step) {

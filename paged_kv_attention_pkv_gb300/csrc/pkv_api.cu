@@ -141,9 +141,18 @@ struct Plan {
   int partials = 0;
 };
 
+// Keys of a sequence of L keys that context-parallel shard r of n owns when
+// tokens are dealt out in runs of k: run j goes to shard j % n.
+int64_t shard_keys(int64_t L, const int32_t *dcp) {
+  if (dcp == nullptr || dcp[0] <= 1) return L;
+  const int64_t n = dcp[0], r = dcp[1], k = dcp[2];
+  const int64_t runs = L / k, rem = L % k;
+  return (runs / n) * k + (runs % n > r ? k : 0) + (runs % n == r ? rem : 0);
+}
+
 std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *lens,
                       int32_t B, int32_t T, int num_sms, int max_partials, Plan *plan,
-                      pkv_status *st) {
+                      pkv_status *st, const int32_t *dcp = nullptr) {
   *st = PKV_ERR_INVALID_ARG;
   if (B < 0 || T < 0) return "num_seqs and num_tokens must be >= 0";
   if (B > 0 && (qsl == nullptr || lens == nullptr))
@@ -163,7 +172,12 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
     const int64_t q = int64_t(qsl[i + 1]) - qsl[i];
     if (q < 0) return fmt("query_start_loc_host decreases at %d", i);
     if (lens[i] < q) return fmt("seq_lens_host[%d] = %d is less than its %lld new tokens", i, lens[i], (long long)q);
-    if (q > 0 && q * G <= kDecCols) dec_keys += int64_t(lens[i]) * H;
+    if (q > 0 && q * G <= kDecCols) dec_keys += shard_keys(lens[i], dcp) * H;
+    if (dcp != nullptr && q * G > kDecCols) {
+      *st = PKV_ERR_UNSUPPORTED;
+      return fmt("request %d has %lld query rows per KV head; shard partials cover decode "
+                 "rows (q * G <= %d) only", i, (long long)(q * G), kDecCols);
+    }
   }
   // decode split size: ~4 waves of 2 CTAs per SM, at least 1024 keys
   const int64_t target = int64_t(8) * std::max(num_sms, 1);
@@ -173,7 +187,7 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
     for (int i = 0; i < B; ++i) {
       const int64_t q = int64_t(qsl[i + 1]) - qsl[i];
       if (q > 0 && q * G <= kDecCols) {
-        const int64_t ns = (lens[i] + chunk - 1) / chunk;
+        const int64_t ns = (shard_keys(lens[i], dcp) + chunk - 1) / chunk;
         if (ns > 1) parts += ns * H;
       }
     }
@@ -189,7 +203,9 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
     const int L = lens[i];
     const int hist = L - q;
     if (q * G <= kDecCols) {
-      const int ns = static_cast<int>((L + chunk - 1) / chunk);
+      // a shard may own no key of a short request: it still writes (0, -inf)
+      const int64_t Ls = shard_keys(L, dcp);
+      const int ns = std::max(1, static_cast<int>((Ls + chunk - 1) / chunk));
       for (int h = 0; h < H; ++h) {
         const int base = ns > 1 ? part : -1;
         for (int s = 0; s < ns; ++s) {
@@ -202,7 +218,7 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
           w.n_rows = q * G;
           w.hist = hist;
           w.k_begin = static_cast<int32_t>(s * chunk);
-          w.k_end = static_cast<int32_t>(std::min<int64_t>(L, (s + 1) * chunk));
+          w.k_end = static_cast<int32_t>(std::min<int64_t>(Ls, (s + 1) * chunk));
           w.part = ns > 1 ? part++ : -1;
           w.pair = base;
           w.n_split = ns;
@@ -485,14 +501,20 @@ pkv_status pkv_write_slots(pkv_handle *h, const void *k_new, const void *v_new,
   return PKV_OK;
 }
 
-pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cache,
-                                const void *v_cache, const float *k_scale,
-                                const float *v_scale, const int32_t *query_start_loc,
-                                const int32_t *seq_lens, const int32_t *block_tables,
-                                int32_t block_table_stride,
-                                const int32_t *qsl_host, const int32_t *lens_host,
-                                int32_t num_seqs, int32_t num_tokens, void *out,
-                                float *lse, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// One attention step: the whole batch (dcp == NULL, bf16 out), or one
+// context-parallel shard's partial (dcp = {n, r, k}: decode rows only, the
+// shard's own keys, fp32 out_f32 and lse).
+pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
+                          const void *v_cache, const float *k_scale, const float *v_scale,
+                          const int32_t *query_start_loc, const int32_t *seq_lens,
+                          const int32_t *block_tables, int32_t block_table_stride,
+                          const int32_t *qsl_host, const int32_t *lens_host,
+                          int32_t num_seqs, int32_t num_tokens, void *out, float *lse,
+                          void *stream, const int32_t *dcp, float *out_f32) {
   if (h == nullptr) return PKV_ERR_INVALID_ARG;
   h->last_error.clear();
   const pkv_config &c = h->cfg;
@@ -503,10 +525,11 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
   Plan plan;
   pkv_status st;
   std::string msg = make_plan(c, qsl_host, lens_host, num_seqs, num_tokens, h->num_sms,
-                              kMaxPartials, &plan, &st);
+                              kMaxPartials, &plan, &st, dcp);
   if (st != PKV_OK) return fail(h, st, msg);
   if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
-  if (!q || !k_cache || !v_cache || !query_start_loc || !seq_lens || !block_tables || !out)
+  if (!q || !k_cache || !v_cache || !query_start_loc || !seq_lens || !block_tables ||
+      !(out || out_f32))
     return fail(h, PKV_ERR_INVALID_ARG, "NULL buffer");
   const bool fp8 = c.kv_dtype == PKV_KV_FP8_E4M3;
   if (fp8 && (!k_scale || !v_scale))
@@ -514,7 +537,8 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
   if (fp8 && !plan.pre.empty())
     return fail(h, PKV_ERR_UNSUPPORTED,
                 "prefill rows (q * G > 8) over FP8 pools are not supported");
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(out_f32))
     return fail(h, PKV_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
   const int bs = c.block_size;
   for (int i = 0; i < num_seqs; ++i) {
@@ -534,6 +558,8 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if ((e = cudaStreamIsCapturing(s, &cap)) != cudaSuccess) return cuda_fail(h, e, "capture query");
   h->capturing = cap != cudaStreamCaptureStatusNone;
+  if (h->capturing && dcp != nullptr)
+    return fail(h, PKV_ERR_UNSUPPORTED, "shard partials are not captured in CUDA graphs");
   if (h->capturing &&
       !(h->graph_ready && int(h->graph_lens.size()) == num_seqs &&
         std::equal(h->graph_lens.begin(), h->graph_lens.end(), lens_host) &&
@@ -621,6 +647,12 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
   dp.num_blocks = c.num_blocks;
   dp.scale_log2 = scale_log2;
   dp.validate = validate;
+  if (dcp != nullptr) {
+    dp.dcp_n = dcp[0];
+    dp.dcp_r = dcp[1];
+    dp.dcp_k = dcp[2];
+  }
+  dp.out_f32 = out_f32;
   PrefillParams pp{};
   pp.items = d_items + plan.dec.size();
   pp.q = static_cast<const __nv_bfloat16 *>(q);
@@ -666,6 +698,67 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cach
     timing_end(h, PKV_KERNEL_PREFILL, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
   }
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_attention_varlen(pkv_handle *h, const void *q, const void *k_cache,
+                                const void *v_cache, const float *k_scale,
+                                const float *v_scale, const int32_t *query_start_loc,
+                                const int32_t *seq_lens, const int32_t *block_tables,
+                                int32_t block_table_stride,
+                                const int32_t *qsl_host, const int32_t *lens_host,
+                                int32_t num_seqs, int32_t num_tokens, void *out,
+                                float *lse, void *stream) {
+  return attention_step(h, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens,
+                        block_tables, block_table_stride, qsl_host, lens_host, num_seqs,
+                        num_tokens, out, lse, stream, nullptr, nullptr);
+}
+
+pkv_status pkv_attention_partial(pkv_handle *h, const void *q, const void *k_cache,
+                                 const void *v_cache, const float *k_scale,
+                                 const float *v_scale, const int32_t *query_start_loc,
+                                 const int32_t *seq_lens, const int32_t *block_tables,
+                                 int32_t block_table_stride, const int32_t *qsl_host,
+                                 const int32_t *lens_host, int32_t num_seqs,
+                                 int32_t num_tokens, int32_t shard, int32_t num_shards,
+                                 int32_t interleave, float *out, float *lse, void *stream) {
+  if (h == nullptr) return PKV_ERR_INVALID_ARG;
+  h->last_error.clear();
+  const int stage = h->cfg.kv_dtype == PKV_KV_FP8_E4M3 ? kDecKeysFp8 : kDecKeysBf16;
+  if (num_shards < 1 || shard < 0 || shard >= num_shards)
+    return fail(h, PKV_ERR_INVALID_ARG, fmt("shard %d of %d", shard, num_shards));
+  if (interleave < stage || interleave % stage != 0)
+    return fail(h, PKV_ERR_UNSUPPORTED,
+                fmt("interleave %d: must be a positive multiple of %d keys", interleave, stage));
+  if (out == nullptr || lse == nullptr)
+    return fail(h, PKV_ERR_INVALID_ARG, "a partial needs out and lse");
+  const int32_t dcp[3] = {num_shards, shard, interleave};
+  return attention_step(h, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens,
+                        block_tables, block_table_stride, qsl_host, lens_host, num_seqs,
+                        num_tokens, nullptr, lse, stream, dcp, out);
+}
+
+pkv_status pkv_lse_merge(pkv_handle *h, const float *parts_o, const float *parts_lse,
+                         int32_t num_parts, int64_t num_rows, void *out, float *lse,
+                         void *stream) {
+  if (h == nullptr) return PKV_ERR_INVALID_ARG;
+  h->last_error.clear();
+  if (num_parts < 1 || num_rows < 0)
+    return fail(h, PKV_ERR_INVALID_ARG, fmt("num_parts %d, num_rows %lld", num_parts, (long long)num_rows));
+  if (num_rows == 0) return PKV_OK;
+  if (!parts_o || !parts_lse || !out)
+    return fail(h, PKV_ERR_INVALID_ARG, "NULL buffer");
+  if (!aligned16(parts_o) || !aligned16(out))
+    return fail(h, PKV_ERR_INVALID_ARG, "parts_o and out must be 16-byte aligned");
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  e = launch_lse_merge(parts_o, parts_lse, num_parts, num_rows,
+                       static_cast<__nv_bfloat16 *>(out), lse, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "merge launch");
   return PKV_OK;
 }
 

@@ -63,6 +63,12 @@ struct DecodeParams {
   int64_t num_blocks;
   float scale_log2;     // softmax_scale * log2(e)
   int32_t validate;
+  // Context-parallel shard view: keys are a shard's own keys when dcp_n > 1
+  // (item-local key x is global key ((x / dcp_k) * dcp_n + dcp_r) * dcp_k +
+  // x % dcp_k; dcp_k a multiple of the stage's key count), and results go
+  // to out_f32 (fp32, normalised) instead of out when out_f32 is set.
+  int32_t dcp_n, dcp_r, dcp_k;
+  float *out_f32;
 };
 
 struct PrefillParams {
@@ -120,6 +126,9 @@ cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p,
                               int num_items, cudaStream_t s);
 cudaError_t launch_check(const CheckParams &p, cudaStream_t s);
+cudaError_t launch_lse_merge(const float *parts_o, const float *parts_lse, int num_parts,
+                             int64_t num_rows, __nv_bfloat16 *out, float *lse,
+                             cudaStream_t s);
 cudaError_t launch_mixed(const CUtensorMap &qmap, const CUtensorMap &kmap_pf,
                          const CUtensorMap &vmap_pf, const CUtensorMap &kmap_dec,
                          const CUtensorMap &vmap_dec, const PrefillParams &pp,

@@ -74,16 +74,19 @@ class Paged:
         self.q = _bf16(rng, (self.T, hq, d), q_scale)
         self.scale = 1.0 / math.sqrt(d)
 
-    def run(self, lib, rows=None, k_range=None):
+    def run(self, lib, rows=None, k_range=None, shard=None):
         return oracle.attention(self.kc, self.vc, self.q, self.qsl,
                                 np.asarray(self.seq_lens, np.int32), self.bt,
-                                self.scale, rows=rows, k_range=k_range, lib=lib)
+                                self.scale, rows=rows, k_range=k_range, shard=shard,
+                                lib=lib)
 
-    def sdpa(self):
+    def sdpa(self, keep=None):
         """torch fp64 scaled_dot_product_attention on the contiguous K/V,
         with one extra zero key whose value is a unit vector in an extra
         column: its weight w0 = 1 / (1 + sum_j exp(s_j)) gives
-        lse = ln(1/w0 - 1).  Returns (out [T*hq, d], lse [T*hq])."""
+        lse = ln(1/w0 - 1).  ``keep(j)`` (optional) further restricts the keys;
+        a row that keeps none gets out 0 and lse -inf.  Returns
+        (out [T*hq, d], lse [T*hq])."""
         G = self.hq // self.hkv
         outs = np.zeros((self.T, self.hq, self.d))
         lses = np.zeros((self.T, self.hq))
@@ -104,7 +107,10 @@ class Paged:
             h = L - qi
             pos = torch.arange(qi)[:, None] + h
             j = torch.arange(L)[None, :]
-            mask = torch.cat([torch.ones(qi, 1, dtype=torch.bool), j <= pos], 1)
+            vis = j <= pos
+            if keep is not None:
+                vis = vis & torch.tensor([bool(keep(x)) for x in range(L)])[None, :]
+            mask = torch.cat([torch.ones(qi, 1, dtype=torch.bool), vis], 1)
             # scale the scores to the original ones; the extra column is
             # exactly sum_j w_j * 0 + w0 * 1
             o = torch.nn.functional.scaled_dot_product_attention(
@@ -112,6 +118,8 @@ class Paged:
                 scale=self.scale)[0]
             w0 = o[:, :, self.d]
             body = o[:, :, :self.d] / (1.0 - w0)[:, :, None]
+            none = ~vis.any(1)                        # rows with no kept key
+            body[:, none, :] = 0.0
             outs[a:a + qi] = body.permute(1, 0, 2).numpy()
             lses[a:a + qi] = torch.log(1.0 / w0 - 1.0).permute(1, 0).numpy()
         return outs.reshape(-1, self.d), lses.reshape(-1)
@@ -283,6 +291,38 @@ def pin_lse_merge(lib):
         np.testing.assert_allclose(o2, o, rtol=0, atol=1e-15)
 
 
+def pin_context_parallel_shards(lib):
+    """Decode context parallelism (page "vLLM Agentic 推理｜面向 Agent 负载的推理优化",
+    sections 4.3.1 and 4.3.3): with interleave 1, token i belongs to rank
+    i % N; with runs of k tokens, run i // k belongs to rank (i // k) % N.
+    Each rank's partial equals torch fp64 SDPA over exactly its keys, a
+    rank with no visible key gives (0, -inf), and the log-sum-exp merge of
+    all ranks' partials is the unsharded result."""
+    rng = np.random.default_rng(19)
+    P = Paged(rng, 8, 2, 16, 4, [1, 3, 1, 1], [29, 41, 3, 1], q_scale=2.0)
+    full, full_lse = P.run(lib)
+    for n, k in ((2, 1), (3, 1), (8, 1), (2, 4), (3, 5), (2, 16)):
+        parts = []
+        for r in range(n):
+            if k == 1:
+                keep = (lambda r: lambda i: i % n == r)(r)          # token i -> rank i % N
+            else:
+                keep = (lambda r: lambda i: (i // k) % n == r)(r)   # run i // k -> rank
+            out, lse = P.run(lib, shard=(n, r, k))
+            ref, ref_lse = P.sdpa(keep=keep)
+            assert np.all(np.isfinite(out)), "poison leaked"
+            np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+            fin = np.isfinite(ref_lse)
+            assert np.array_equal(np.isfinite(lse), fin), (n, k, r)
+            np.testing.assert_allclose(lse[fin], ref_lse[fin], rtol=0, atol=1e-9)
+            parts.append((out, lse))
+        for row in range(full.shape[0]):
+            o, l = oracle.lse_merge(np.array([p[1][row] for p in parts]),
+                                    np.stack([p[0][row] for p in parts]), lib=lib)
+            np.testing.assert_allclose(o, full[row], rtol=0, atol=1e-12)
+            assert abs(l - full_lse[row]) < 1e-11
+
+
 # ---- KV append and FP8 pins -----------------------------------------------------
 
 def pin_write_slots_bf16(lib):
@@ -415,5 +455,6 @@ def pin_fp8_attention(lib):
 
 ALL_PINS = [pin_sdpa, pin_block_permutation, pin_chunked_prefill,
             pin_closed_forms, pin_gqa_is_repeated_mha, pin_lse_merge,
+            pin_context_parallel_shards,
             pin_write_slots_bf16, pin_e4m3_decode, pin_e4m3_encode,
             pin_write_slots_fp8, pin_fp8_attention]

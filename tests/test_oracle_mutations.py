@@ -37,6 +37,10 @@ MUTATIONS = {
                           ";"),
     "quantize_multiplies": ("volatile float q = x / scale;",
                             "volatile float q = x * scale;"),
+    "shard_runs_not_tokens": ("return n <= 1 || (j / k) % n == r;",
+                              "return n <= 1 || (j % n) == r;"),
+    "shard_off_by_one_rank": ("return n <= 1 || (j / k) % n == r;",
+                              "return n <= 1 || (j / k + 1) % n == r;"),
     "v_append_from_k": ("const uint16_t *vs = v_new + ((size_t)t * hkv + h) * d;",
                         "const uint16_t *vs = k_new + ((size_t)t * hkv + h) * d;"),
 }
