@@ -32,7 +32,11 @@ EXPORTS = ["pkv_create", "pkv_write_slots", "pkv_attention_varlen",
            "pkv_check_device_errors", "pkv_status_string", "pkv_last_error",
            "pkv_destroy", "pkv_plan", "pkv_timing_reset", "pkv_timing_read",
            "pkv_decode_static", "pkv_graph_prepare", "pkv_attention_partial",
-           "pkv_lse_merge"]
+           "pkv_lse_merge",
+           # host block pool (include/pkv_blocks.h)
+           "pkv_blocks_create", "pkv_blocks_destroy", "pkv_blocks_lookup",
+           "pkv_blocks_allocate", "pkv_blocks_commit", "pkv_blocks_free",
+           "pkv_blocks_slots", "pkv_blocks_stats", "pkv_blocks_ref_count"]
 
 
 class PkvError(RuntimeError):
@@ -84,6 +88,19 @@ def load(path: str | None = None):
                                           vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.pkv_lse_merge.restype = ctypes.c_int
     lib.pkv_lse_merge.argtypes = [vp, vp, vp, i32, i64, vp, vp, vp]
+    i64p = ctypes.POINTER(i64)
+    for n, args in (("pkv_blocks_create", [i64, i32, ctypes.POINTER(vp)]),
+                    ("pkv_blocks_destroy", [vp]),
+                    ("pkv_blocks_lookup", [vp, vp, i64, i64p]),
+                    ("pkv_blocks_allocate", [vp, i64, vp, i64, i64, i32, vp, i64, i64p, i64p,
+                                             ctypes.POINTER(i32)]),
+                    ("pkv_blocks_commit", [vp, i64, vp, i64, i64]),
+                    ("pkv_blocks_free", [vp, i64]),
+                    ("pkv_blocks_slots", [vp, i64, i64, i64, vp]),
+                    ("pkv_blocks_stats", [vp, i64p, i64p, i64p]),
+                    ("pkv_blocks_ref_count", [vp, i32])):
+        getattr(lib, n).restype = ctypes.c_int32
+        getattr(lib, n).argtypes = args
     lib.pkv_graph_prepare.restype = ctypes.c_int
     lib.pkv_graph_prepare.argtypes = [vp, vp, vp, i32, i32]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -270,6 +287,74 @@ class Handle:
         self._check(self._lib.pkv_timing_read(self._h, kind, ctypes.byref(n),
                                               ctypes.byref(ms)))
         return n.value, ms.value
+
+
+class Blocks:
+    """Host block pool with prefix caching (include/pkv_blocks.h)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._lib = load()
+        self.block_size = block_size
+        h = ctypes.c_void_p()
+        st = self._lib.pkv_blocks_create(num_blocks, block_size, ctypes.byref(h))
+        if st != 0:
+            raise PkvError(st, "pkv_blocks_create rejected its arguments")
+        self._h = h
+
+    def _call(self, name, *args):
+        st = getattr(self._lib, name)(self._h, *args)
+        if st != 0:
+            raise PkvError(st, f"{name} rejected its arguments")
+
+    def lookup(self, tokens) -> int:
+        t = _host_i32(tokens)
+        hit = ctypes.c_int64()
+        self._call("pkv_blocks_lookup", _ptr(t), int(t.shape[0]), ctypes.byref(hit))
+        return hit.value
+
+    def allocate(self, req: int, tokens, num_new_tokens: int, num_lookahead: int = 0):
+        """(block table or None if the pool cannot hold it, num_computed)."""
+        t = _host_i32(tokens)
+        cap = (int(t.shape[0]) + num_lookahead + self.block_size) // self.block_size + 1
+        table = np.zeros(max(cap, 1), np.int32)
+        nb, nc, ok = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+        self._call("pkv_blocks_allocate", int(req), _ptr(t), int(t.shape[0]),
+                   int(num_new_tokens), int(num_lookahead), _ptr(table), int(table.shape[0]),
+                   ctypes.byref(nb), ctypes.byref(nc), ctypes.byref(ok))
+        if not ok.value:
+            return None, None
+        return table[:nb.value].copy(), nc.value
+
+    def commit(self, req: int, tokens, num_computed: int) -> None:
+        t = _host_i32(tokens)
+        self._call("pkv_blocks_commit", int(req), _ptr(t), int(t.shape[0]), int(num_computed))
+
+    def free(self, req: int) -> None:
+        self._call("pkv_blocks_free", int(req))
+
+    def slots(self, req: int, pos0: int, n: int) -> np.ndarray:
+        out = np.zeros(max(n, 1), np.int64)
+        self._call("pkv_blocks_slots", int(req), int(pos0), int(n), _ptr(out))
+        return out[:n]
+
+    def stats(self) -> dict:
+        f, c, e = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        self._call("pkv_blocks_stats", ctypes.byref(f), ctypes.byref(c), ctypes.byref(e))
+        return {"free": f.value, "cached": c.value, "evictable": e.value}
+
+    def ref_count(self, block: int) -> int:
+        return self._lib.pkv_blocks_ref_count(self._h, int(block))
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.pkv_blocks_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def plan(config: Config, query_start_loc_host, seq_lens_host, num_sms: int = 152):

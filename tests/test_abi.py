@@ -1,4 +1,4 @@
-"""The C ABI: libpkv loads, exports every symbol include/pkv.h declares, and
+"""The C ABI: libpkv loads, exports every symbol include/*.h declares, and
 rejects bad arguments with status codes (CPU only: no kernel is launched)."""
 import ctypes
 import os
@@ -14,7 +14,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def declared_symbols():
-    src = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc))
+                  if f.endswith(".h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", src)))
 
