@@ -125,6 +125,34 @@ pkv_status pkv_write_slots(pkv_handle *h, const void *k_new, const void *v_new,
                            const float *v_scale, void *stream);
 
 /*
+ * Rotary position embedding fused with the KV append: the pages' first
+ * per-layer kernel applies RoPE and writes the KV in one launch (page "vLLM
+ * Agentic 推理｜面向 Agent 负载的推理优化", section 5.2, K1).  For each token t:
+ * q[t] (all Hq heads) is rotated in place, k_new[t] is rotated and stored at
+ * slot_mapping[t] like pkv_write_slots (k_new itself is not modified), and
+ * v_new[t] is stored unrotated.  Rotation of the 64 pairs of a 128-element
+ * head row by the angles of position p = positions[t]:
+ *   y_a = x_a cos_i - x_b sin_i,  y_b = x_b cos_i + x_a sin_i,
+ * with (a, b) = (i, i + 64) when neox != 0 (rotate-half layout) or
+ * (2i, 2i + 1) otherwise, cos_i = cos_sin_cache[p][i] and sin_i =
+ * cos_sin_cache[p][64 + i].  Computed in fp32, rounded to bf16 (an E4M3
+ * pool then quantises that bf16 value as pkv_write_slots does).
+ *  q              [num_tokens][Hq][128] bf16, device, read and written;
+ *  positions      [num_tokens] int64, device, each in [0, max_pos);
+ *  cos_sin_cache  [max_pos][128] fp32, device, 16-byte aligned.
+ * Other arguments as pkv_write_slots.  A position outside [0, max_pos) skips
+ * that token (q and KV untouched) and is recorded for
+ * pkv_check_device_errors (PKV_ERR_DEVICE_CHECK).
+ */
+pkv_status pkv_rope_write_slots(pkv_handle *h, void *q, const void *k_new,
+                                const void *v_new, const int64_t *positions,
+                                const float *cos_sin_cache, int64_t max_pos,
+                                int32_t neox, const int64_t *slot_mapping,
+                                int32_t num_tokens, void *k_cache, void *v_cache,
+                                const float *k_scale, const float *v_scale,
+                                void *stream);
+
+/*
  * Attention for one step.
  *  q                [num_tokens][Hq][128] bf16, device; the tokens of request
  *                   i are rows query_start_loc[i] .. query_start_loc[i+1]-1.

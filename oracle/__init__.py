@@ -61,6 +61,12 @@ def load(path: str | None = None):
     lib.pko_lse_merge.restype = None
     lib.pko_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p,
                                   _f64p, _f64p]
+    lib.pko_bf16_round.restype = ctypes.c_uint16
+    lib.pko_bf16_round.argtypes = [ctypes.c_double]
+    lib.pko_rope.restype = ctypes.c_int
+    lib.pko_rope.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, _u16p, _i64p,
+                             ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                             ctypes.c_void_p]
     lib.pko_num_threads.restype = ctypes.c_int
     lib.pko_num_threads.argtypes = []
     if path is None:
@@ -74,6 +80,30 @@ def _ptr(a: np.ndarray | None):
 
 def num_threads() -> int:
     return int(load().pko_num_threads())
+
+
+def bf16_round(v: float, lib=None) -> int:
+    """bf16 bit pattern of v rounded to nearest, ties to even."""
+    return int((lib or load()).pko_bf16_round(float(v)))
+
+
+def rope(x: np.ndarray, positions: np.ndarray, cos_sin: np.ndarray, neox: bool = True,
+         lib=None):
+    """Rotary embedding of ``x`` ``[T, H, d]`` (bf16 bits) at ``positions``
+    with the ``[max_pos, d]`` fp32 cos/sin table; returns (fp64 values,
+    bf16 bits), both ``[T, H, d]``."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    t, h, d = x.shape
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    cs = np.ascontiguousarray(cos_sin, dtype=np.float32)
+    f64 = np.zeros((t, h, d), np.float64)
+    bits = np.zeros((t, h, d), np.uint16)
+    st = lib.pko_rope(t, h, d, x, pos, _ptr(cs), cs.shape[0], int(bool(neox)), _ptr(f64),
+                      _ptr(bits))
+    if st != 0:
+        raise ValueError(f"oracle rope rejected its arguments ({st})")
+    return f64, bits
 
 
 def bf16_value(bits: int) -> float:

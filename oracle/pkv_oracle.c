@@ -22,6 +22,12 @@
  *    Agentic 推理", section 4.3.1.
  *  - Partial results over disjoint key sets merge through their log-sum-exp.
  *    Page "vLLM Agentic 推理", section 4.3.3 (step 4, online-softmax merge).
+ *  - Rotary position embedding applied to q and to K before the KV write
+ *    (the pages' first per-layer kernel does both: page "vLLM Agentic 推理",
+ *    section 5.2, K1).  The pages do not define RoPE; the reading taken is
+ *    the usual one: the 64 pairs of a 128-wide head rotate by the angle whose
+ *    cosine and sine the caller's table gives for the token's position, pairs
+ *    (i, i + 64) ("neox") or (2i, 2i + 1).
  *  - Decode context parallelism: a request's KV tokens are dealt out to N
  *    ranks in runs of `interleave` tokens (interleave 1: token i on rank
  *    i % N); each rank attends to its own tokens only.  Page "vLLM Agentic
@@ -64,6 +70,38 @@ double pko_bf16_value(uint16_t bits)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* Round a real number to bf16 (8 significant bits, binary32 exponent
+ * range), to nearest, ties to even; returns the bf16 bit pattern.  Values
+ * at or beyond the largest finite bf16 plus half an ulp become infinities. */
+uint16_t pko_bf16_round(double v)
+{
+    if (isnan(v))
+        return 0x7FC0;
+    double a = fabs(v);
+    double r;
+    if (a == 0.0) {
+        r = 0.0;
+    } else {
+        int e;
+        frexp(a, &e);                       /* a = f * 2^e, f in [0.5, 1) */
+        int ulp_exp = e - 8;                /* 8 significant bits */
+        if (ulp_exp < -133)                 /* below the smallest normal: fixed quantum */
+            ulp_exp = -133;
+        double q = ldexp(1.0, ulp_exp);
+        double n = a / q;                   /* exact: q is a power of two */
+        double fl = floor(n), fr = n - fl;
+        double k = fr > 0.5 ? fl + 1.0 : fr < 0.5 ? fl : (fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0);
+        r = k * q;
+    }
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    if (r >= ldexp(1.0, 128))
+        return sign | 0x7F80;
+    float f = (float)r;                     /* exact: r has <= 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (u >> 16));
 }
 
 /* OCP E4M3 decode, written from the format definition. */
@@ -349,6 +387,50 @@ int pko_attention(int kv_fp8, const void *k_cache, const void *v_cache,
         free(scores);
     }
     return status;
+}
+
+/*
+ * Rotary position embedding of rows x [n][heads][d] (bf16 bits), token t
+ * at position positions[t]: for pair (a, b) with angle index i,
+ *   y_a = x_a cos_i - x_b sin_i,  y_b = x_b cos_i + x_a sin_i,
+ * cos_i = cos_sin[p * d + i], sin_i = cos_sin[p * d + d/2 + i]; pairs are
+ * (i, i + d/2) when neox, else (2i, 2i + 1).  fp64 arithmetic; out_f64
+ * (optional) receives y, out_bits (optional) y rounded to bf16.
+ */
+int pko_rope(int64_t n, int heads, int d, const uint16_t *x, const int64_t *positions,
+             const float *cos_sin, int64_t max_pos, int neox, double *out_f64,
+             uint16_t *out_bits)
+{
+    if (n < 0 || heads <= 0 || d <= 0 || d % 2 != 0)
+        return PKO_BAD_ARG;
+    int half = d / 2;
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t p = positions[t];
+        if (p < 0 || p >= max_pos)
+            return PKO_BAD_ARG;
+        const float *cs = cos_sin + (size_t)p * d;
+        for (int h = 0; h < heads; ++h) {
+            const uint16_t *row = x + ((size_t)t * heads + h) * d;
+            size_t o = ((size_t)t * heads + h) * d;
+            for (int i = 0; i < half; ++i) {
+                int a = neox ? i : 2 * i;
+                int b = neox ? i + half : 2 * i + 1;
+                double xa = pko_bf16_value(row[a]), xb = pko_bf16_value(row[b]);
+                double c = cs[i], s = cs[half + i];
+                double ya = xa * c - xb * s;
+                double yb = xb * c + xa * s;
+                if (out_f64) {
+                    out_f64[o + a] = ya;
+                    out_f64[o + b] = yb;
+                }
+                if (out_bits) {
+                    out_bits[o + a] = pko_bf16_round(ya);
+                    out_bits[o + b] = pko_bf16_round(yb);
+                }
+            }
+        }
+    }
+    return PKO_OK;
 }
 
 /*

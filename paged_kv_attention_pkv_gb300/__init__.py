@@ -32,7 +32,7 @@ EXPORTS = ["pkv_create", "pkv_write_slots", "pkv_attention_varlen",
            "pkv_check_device_errors", "pkv_status_string", "pkv_last_error",
            "pkv_destroy", "pkv_plan", "pkv_timing_reset", "pkv_timing_read",
            "pkv_decode_static", "pkv_graph_prepare", "pkv_attention_partial",
-           "pkv_lse_merge",
+           "pkv_lse_merge", "pkv_rope_write_slots",
            # host block pool (include/pkv_blocks.h)
            "pkv_blocks_create", "pkv_blocks_destroy", "pkv_blocks_lookup",
            "pkv_blocks_allocate", "pkv_blocks_commit", "pkv_blocks_free",
@@ -86,6 +86,9 @@ def load(path: str | None = None):
     lib.pkv_attention_partial.restype = ctypes.c_int
     lib.pkv_attention_partial.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
                                           vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.pkv_rope_write_slots.restype = ctypes.c_int
+    lib.pkv_rope_write_slots.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, vp, i32, vp, vp,
+                                         vp, vp, vp]
     lib.pkv_lse_merge.restype = ctypes.c_int
     lib.pkv_lse_merge.argtypes = [vp, vp, vp, i32, i64, vp, vp, vp]
     i64p = ctypes.POINTER(i64)
@@ -209,6 +212,16 @@ class Handle:
             self._h, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
             int(slot_mapping.shape[0]), _ptr(k_cache), _ptr(v_cache),
             _ptr(k_scale), _ptr(v_scale), _stream(stream, self.device)))
+
+    def rope_write_slots(self, q, k_new, v_new, positions, cos_sin_cache, slot_mapping,
+                         k_cache, v_cache, neox=True, k_scale=None, v_scale=None,
+                         stream=None) -> None:
+        """pkv_rope_write_slots: rotate q in place, rotate and append K, append V."""
+        self._check(self._lib.pkv_rope_write_slots(
+            self._h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(cos_sin_cache),
+            int(cos_sin_cache.shape[0]), int(bool(neox)), _ptr(slot_mapping),
+            int(slot_mapping.shape[0]), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+            _ptr(v_scale), _stream(stream, self.device)))
 
     def attention_varlen(self, q, k_cache, v_cache, query_start_loc, seq_lens,
                          block_tables, query_start_loc_host, seq_lens_host,

@@ -74,6 +74,95 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
   }
 }
 
+// Rotary position embedding fused with the append (the KV write and RoPE
+// run in one kernel in the pages' first per-layer kernel: page "vLLM
+// Agentic 推理｜面向 Agent 负载的推理优化", section 5.2, K1).  A CTA handles one
+// token; each warp handles whole 128-element rows (q heads, then K heads,
+// then V heads), 4 elements per lane.  Pairs rotate by the angle of the
+// token's position: NEOX pairs element i with i + 64, otherwise 2i with
+// 2i + 1 (pair index i in 0..63 either way).  Rotation runs in fp32 and is
+// rounded to bf16, which is also what an FP8 pool quantises.
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+template <bool FP8, bool NEOX>
+__global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendParams rp) {
+  const AppendParams &p = rp.a;
+  const int64_t t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t pos = __ldg(rp.positions + t);
+  if (pos < 0 || pos >= rp.max_pos) {
+    if (threadIdx.x == 0) record_error(p.err, kErrBadPosition);
+    return;
+  }
+  const int64_t slot = p.slots[t];
+  const int64_t blk = slot >= 0 ? slot / p.bs : -1;
+  if (slot >= 0 && blk >= p.num_blocks && threadIdx.x == 0) record_error(p.err, kErrBadSlot);
+  const bool write_kv = slot >= 0 && blk < p.num_blocks;
+  // this lane's 4 elements e = 4 lane + j and their pair indices
+  const float *cs = rp.cos_sin + pos * kHeadDim;
+  float c[4], sn[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * lane + j;
+    const int i = NEOX ? (e & 63) : (e >> 1);
+    c[j] = __ldg(cs + i);
+    sn[j] = __ldg(cs + 64 + i);
+  }
+  auto rotate = [&](uint2 w, float (&y)[4]) {
+    float x[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
+    float xp[4];
+    if (NEOX) {   // partner of element e is e ^ 64: lane ^ 16, same j
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xp[j] = __shfl_xor_sync(0xffffffffu, x[j], 16);
+    } else {
+      xp[0] = x[1]; xp[1] = x[0]; xp[2] = x[3]; xp[3] = x[2];
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * lane + j;
+      const bool second = NEOX ? (e >= 64) : (e & 1);
+      // first of a pair: x cos - x' sin; second: x cos + x' sin
+      y[j] = fmaf(x[j], c[j], second ? xp[j] * sn[j] : -(xp[j] * sn[j]));
+    }
+  };
+  const int rows = rp.hq + 2 * p.hkv;
+  for (int r = warp; r < rows; r += blockDim.x >> 5) {
+    if (r < rp.hq) {
+      uint2 *qrow = reinterpret_cast<uint2 *>(rp.q + (t * rp.hq + r) * kHeadDim);
+      float y[4];
+      rotate(qrow[lane], y);
+      qrow[lane] = make_uint2(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]));
+      continue;
+    }
+    const bool is_k = r < rp.hq + p.hkv;
+    const int h = is_k ? r - rp.hq : r - rp.hq - p.hkv;
+    const int64_t row = t * p.hkv + h;
+    const uint2 w = __ldg(reinterpret_cast<const uint2 *>(is_k ? p.k_new : p.v_new) +
+                          row * (kHeadDim / 4) + lane);
+    float y[4];
+    if (is_k) {
+      rotate(w, y);   // whole warp (the shuffle needs every lane)
+    } else {
+      y[0] = bf16_lo(w.x); y[1] = bf16_hi(w.x); y[2] = bf16_lo(w.y); y[3] = bf16_hi(w.y);
+    }
+    if (!write_kv) continue;
+    const size_t dst = (static_cast<size_t>(blk) * p.hkv + h) * p.bs + slot % p.bs;
+    void *pool = is_k ? p.k_cache : p.v_cache;
+    if constexpr (!FP8) {
+      reinterpret_cast<uint2 *>(pool)[dst * (kHeadDim / 4) + lane] =
+          make_uint2(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]));
+    } else {
+      const float sc = __ldg((is_k ? p.k_scale : p.v_scale) + static_cast<size_t>(blk) * p.hkv + h);
+      const uint16_t a = cvt_e4m3x2(__fdiv_rn(bf16_round(y[0]), sc), __fdiv_rn(bf16_round(y[1]), sc));
+      const uint16_t b = cvt_e4m3x2(__fdiv_rn(bf16_round(y[2]), sc), __fdiv_rn(bf16_round(y[3]), sc));
+      reinterpret_cast<uint32_t *>(pool)[dst * (kHeadDim / 4) + lane] =
+          static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
+    }
+  }
+}
+
 // Validate mode: the device metadata must equal the host mirrors the plan
 // was built from, and every block-table entry in use must be in the pool.
 __global__ void __launch_bounds__(256) check_kernel(CheckParams p) {
@@ -93,6 +182,17 @@ __global__ void __launch_bounds__(256) check_kernel(CheckParams p) {
 }
 
 }  // namespace
+
+cudaError_t launch_rope_append(const RopeAppendParams &p, bool fp8, bool neox,
+                               cudaStream_t s) {
+  if (p.a.num_tokens == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>(p.a.num_tokens);
+  if (fp8 && neox) rope_append_kernel<true, true><<<grid, 256, 0, s>>>(p);
+  else if (fp8) rope_append_kernel<true, false><<<grid, 256, 0, s>>>(p);
+  else if (neox) rope_append_kernel<false, true><<<grid, 256, 0, s>>>(p);
+  else rope_append_kernel<false, false><<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_append(const AppendParams &p, bool fp8, cudaStream_t s) {
   const int64_t total = p.num_tokens * p.hkv * (kHeadDim / 8);

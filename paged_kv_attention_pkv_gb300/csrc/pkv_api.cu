@@ -762,6 +762,59 @@ pkv_status pkv_lse_merge(pkv_handle *h, const float *parts_o, const float *parts
   return PKV_OK;
 }
 
+pkv_status pkv_rope_write_slots(pkv_handle *h, void *q, const void *k_new,
+                                const void *v_new, const int64_t *positions,
+                                const float *cos_sin_cache, int64_t max_pos, int32_t neox,
+                                const int64_t *slot_mapping, int32_t num_tokens,
+                                void *k_cache, void *v_cache, const float *k_scale,
+                                const float *v_scale, void *stream) {
+  if (h == nullptr) return PKV_ERR_INVALID_ARG;
+  h->last_error.clear();
+  if (num_tokens < 0 || num_tokens > h->cfg.max_num_tokens)
+    return fail(h, PKV_ERR_INVALID_ARG, fmt("num_tokens %d outside [0, max_num_tokens]", num_tokens));
+  if (num_tokens == 0) return PKV_OK;
+  if (!q || !k_new || !v_new || !positions || !cos_sin_cache || !slot_mapping || !k_cache ||
+      !v_cache)
+    return fail(h, PKV_ERR_INVALID_ARG, "NULL buffer");
+  if (max_pos < 1) return fail(h, PKV_ERR_INVALID_ARG, "max_pos must be >= 1");
+  const bool fp8 = h->cfg.kv_dtype == PKV_KV_FP8_E4M3;
+  if (fp8 && (!k_scale || !v_scale))
+    return fail(h, PKV_ERR_INVALID_ARG, "FP8 pools need k_scale and v_scale");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(cos_sin_cache))
+    return fail(h, PKV_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  RopeAppendParams rp{};
+  rp.a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  rp.a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  rp.a.slots = slot_mapping;
+  rp.a.k_cache = k_cache;
+  rp.a.v_cache = v_cache;
+  rp.a.k_scale = k_scale;
+  rp.a.v_scale = v_scale;
+  rp.a.err = h->d_err;
+  rp.a.num_tokens = num_tokens;
+  rp.a.hkv = h->cfg.num_kv_heads;
+  rp.a.bs = h->cfg.block_size;
+  rp.a.num_blocks = h->cfg.num_blocks;
+  rp.a.validate = (h->cfg.flags & PKV_FLAG_VALIDATE) != 0;
+  rp.q = static_cast<__nv_bfloat16 *>(q);
+  rp.positions = positions;
+  rp.cos_sin = cos_sin_cache;
+  rp.max_pos = max_pos;
+  rp.hq = h->cfg.num_q_heads;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if ((e = cudaStreamIsCapturing(s, &cap)) != cudaSuccess) return cuda_fail(h, e, "capture query");
+  h->capturing = cap != cudaStreamCaptureStatusNone;
+  timing_begin(h, PKV_KERNEL_APPEND, s);
+  e = launch_rope_append(rp, fp8, neox != 0, s);
+  timing_end(h, PKV_KERNEL_APPEND, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "rope + KV append launch");
+  return PKV_OK;
+}
+
 pkv_status pkv_graph_prepare(pkv_handle *h, const int32_t *qsl_host,
                              const int32_t *lens_host, int32_t num_seqs,
                              int32_t num_tokens) {
@@ -811,6 +864,7 @@ pkv_status pkv_check_device_errors(pkv_handle *h) {
     if (word & kErrBadBlock) what += " block-table entry outside the pool;";
     if (word & kErrBadSlot) what += " slot outside the pool;";
     if (word & kErrMismatch) what += " device metadata differs from the host mirrors;";
+    if (word & kErrBadPosition) what += " rotary position outside the cos/sin cache;";
     return fail(h, PKV_ERR_DEVICE_CHECK, "device check:" + what);
   }
   return PKV_OK;

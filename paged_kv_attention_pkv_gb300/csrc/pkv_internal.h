@@ -18,6 +18,7 @@ enum : int32_t {
   kErrBadSlot = 2,      // a slot_mapping entry is outside the pool
   kErrTimeout = 4,      // a bounded wait gave up
   kErrMismatch = 8,     // device metadata differs from the host mirrors
+  kErrBadPosition = 16, // a rotary position is outside the cos/sin cache
 };
 
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
@@ -101,6 +102,18 @@ struct AppendParams {
   int32_t validate;
 };
 
+// Rotary embedding fused with the KV append: q rotated in place, K rotated
+// then written, V written.  cos_sin: [max_pos][128] fp32, cos in columns
+// 0..63 and sin in 64..127 for the 64 rotation pairs.
+struct RopeAppendParams {
+  AppendParams a;
+  __nv_bfloat16 *q;          // [num_tokens][hq][128], rotated in place
+  const int64_t *positions;  // [num_tokens]
+  const float *cos_sin;
+  int64_t max_pos;
+  int32_t hq;
+};
+
 struct CheckParams {
   const int32_t *qsl;
   const int32_t *seq_lens;
@@ -116,6 +129,7 @@ struct CheckParams {
 
 // Launchers (each returns the launch's cudaError_t).
 cudaError_t launch_append(const AppendParams &p, bool fp8, cudaStream_t s);
+cudaError_t launch_rope_append(const RopeAppendParams &p, bool fp8, bool neox, cudaStream_t s);
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
                           const DecodeParams &p, int num_items, bool fp8,
                           cudaStream_t s);

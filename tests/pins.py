@@ -323,6 +323,52 @@ def pin_context_parallel_shards(lib):
             assert abs(l - full_lse[row]) < 1e-11
 
 
+# ---- rotary embedding pins ---------------------------------------------------------
+
+def _rope_table(rng, max_pos, d=128):
+    ang = rng.uniform(-math.pi, math.pi, (max_pos, d // 2))
+    ang[0] = 0.0                                        # position 0: identity
+    return np.concatenate([np.cos(ang), np.sin(ang)], 1).astype(np.float32)
+
+
+def pin_rope_is_a_complex_rotation(lib):
+    """Library routine: each pair (a, b) rotates like the complex number
+    x_a + i x_b multiplied by cos + i sin (torch complex128), for both pair
+    layouts; position 0 with angle 0 is the identity (bit-exact)."""
+    rng = np.random.default_rng(23)
+    x = _bf16(rng, (7, 3, 128), 3.0)
+    tab = _rope_table(rng, 50)
+    pos = np.array([0, 1, 49, 7, 7, 0, 30], np.int64)
+    xf = torch.from_numpy(_f64(x))
+    c = torch.from_numpy(tab[pos, :64].astype(np.float64))[:, None, :]
+    sn = torch.from_numpy(tab[pos, 64:].astype(np.float64))[:, None, :]
+    rot = torch.complex(c, sn)
+    for neox in (True, False):
+        y, bits = oracle.rope(x, pos, tab, neox=neox, lib=lib)
+        if neox:
+            z = torch.complex(xf[..., :64], xf[..., 64:]) * rot
+            ref = torch.cat([z.real, z.imag], -1)
+        else:
+            z = torch.view_as_complex(xf.reshape(7, 3, 64, 2).contiguous()) * rot
+            ref = torch.view_as_real(z).reshape(7, 3, 128)
+        np.testing.assert_allclose(y, ref.numpy(), rtol=0, atol=1e-14)
+        assert np.array_equal(bits[pos == 0], x[pos == 0])
+
+
+def pin_bf16_round(lib):
+    """Rounding to bf16 equals torch's float32 -> bfloat16 cast (nearest,
+    ties to even) on float32 values: random, ties, subnormals, overflow."""
+    rng = np.random.default_rng(29)
+    v = (rng.standard_normal(4000) * np.exp(rng.uniform(-85, 85, 4000))).astype(np.float32)
+    ties = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(2.0 + 2.0 ** -7),
+                     2.0 ** -130, 3.5 * 2.0 ** -133, 2.0 ** -134, 3.4e38, -3.39e38,
+                     0.0, -0.0], np.float32)
+    v = np.concatenate([v, ties])
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.bf16_round(float(a), lib=lib) for a in v], np.uint16)
+    assert np.array_equal(got, ref), v[got != ref][:5]
+
+
 # ---- KV append and FP8 pins -----------------------------------------------------
 
 def pin_write_slots_bf16(lib):
@@ -455,6 +501,6 @@ def pin_fp8_attention(lib):
 
 ALL_PINS = [pin_sdpa, pin_block_permutation, pin_chunked_prefill,
             pin_closed_forms, pin_gqa_is_repeated_mha, pin_lse_merge,
-            pin_context_parallel_shards,
+            pin_context_parallel_shards, pin_rope_is_a_complex_rotation, pin_bf16_round,
             pin_write_slots_bf16, pin_e4m3_decode, pin_e4m3_encode,
             pin_write_slots_fp8, pin_fp8_attention]

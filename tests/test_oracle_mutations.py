@@ -41,6 +41,11 @@ MUTATIONS = {
                               "return n <= 1 || (j % n) == r;"),
     "shard_off_by_one_rank": ("return n <= 1 || (j / k) % n == r;",
                               "return n <= 1 || (j / k + 1) % n == r;"),
+    "rope_sign_swapped": ("double ya = xa * c - xb * s;", "double ya = xa * c + xb * s;"),
+    "rope_wrong_partner": ("int b = neox ? i + half : 2 * i + 1;",
+                           "int b = neox ? (i + 1) % half + half : 2 * i + 1;"),
+    "bf16_ties_up": ("double k = fr > 0.5 ? fl + 1.0 : fr < 0.5 ? fl : (fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0);",
+                     "double k = fr >= 0.5 ? fl + 1.0 : fl;"),
     "v_append_from_k": ("const uint16_t *vs = v_new + ((size_t)t * hkv + h) * d;",
                         "const uint16_t *vs = k_new + ((size_t)t * hkv + h) * d;"),
 }
