@@ -179,8 +179,10 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
                  "rows (q * G <= %d) only", i, (long long)(q * G), kDecCols);
     }
   }
-  // decode split size: ~4 waves of 2 CTAs per SM, at least 1024 keys
-  const int64_t target = int64_t(8) * std::max(num_sms, 1);
+  // decode split size: ~4 whole waves of the resident decode CTAs (2 per SM
+  // for bf16 pools, 3 for E4M3), at least 1024 keys
+  const int64_t resident = c.kv_dtype == PKV_KV_FP8_E4M3 ? 3 : 2;
+  const int64_t target = 4 * resident * std::max(num_sms, 1);
   int64_t chunk = std::max<int64_t>(1024, (dec_keys / target + kSplitAlign - 1) / kSplitAlign * kSplitAlign);
   for (;;) {
     int64_t parts = 0;
