@@ -2,6 +2,8 @@
 // one-launch mixed-step kernel).  See decode.cu for what it computes.
 #pragma once
 
+#include <type_traits>
+
 #include <math_constants.h>
 
 #include "pkv_device.cuh"
@@ -200,10 +202,37 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
   for (int mt = 0; mt < 8; ++mt)
     acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 
+  // E4M3 pools: the per-block scales of a stage's sub-tiles are loaded
+  // before its wait (block ids one stage ahead), so their latency hides
+  // behind the copy instead of sitting between the MMAs and the softmax
+  auto stage_blocks = [&](int i, int32_t (&blk)[Tile::kSubs]) {
+#pragma unroll
+    for (int sub = 0; sub < Tile::kSubs; ++sub) {
+      const int k16 = kb + (warp + i * kDecWarps) * KS + 16 * sub;
+      blk[sub] = (FP8 && i < my_n && k16 < ke) ? __ldg(bt + global_key(p, k16) / p.bs) : -1;
+    }
+  };
+  int32_t blk_next[Tile::kSubs];
+  stage_blocks(0, blk_next);
+
   int consumed = 0;
   bool timed_out = false;
   for (int i = 0; i < my_n; ++i) {
     const int slot = i % kDecStages;
+    float sk_sub[Tile::kSubs], sv_sub[Tile::kSubs];
+    if constexpr (FP8) {
+#pragma unroll
+      for (int sub = 0; sub < Tile::kSubs; ++sub) {
+        const int32_t blk = blk_next[sub];
+        sk_sub[sub] = sv_sub[sub] = 0.f;
+        if (blk >= 0 && blk < p.num_blocks) {
+          const int64_t si = static_cast<int64_t>(blk) * p.hkv + it.kv_head;
+          sk_sub[sub] = __ldg(p.k_scale + si);
+          sv_sub[sub] = __ldg(p.v_scale + si);
+        }
+      }
+      stage_blocks(i + 1, blk_next);
+    }
     const bool ok = mbar_wait(&full[slot], (i / kDecStages) & 1);
     if (!__all_sync(0xffffffffu, ok)) {  // warp-uniform way out
       timed_out = true;
@@ -246,16 +275,9 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       float sc0 = p.scale_log2, sc1 = p.scale_log2;
       float pv_scale = 1.f;
       if constexpr (FP8) {
-        const int32_t blk = __ldg(bt + g16 / p.bs);
-        float sk = 0.f, sv = 0.f;
-        if (blk >= 0 && blk < p.num_blocks) {
-          const int64_t si = static_cast<int64_t>(blk) * p.hkv + it.kv_head;
-          sk = __ldg(p.k_scale + si);
-          sv = __ldg(p.v_scale + si);
-        }
-        sc0 *= sk * inv_sq0;
-        sc1 *= sk * inv_sq1;
-        pv_scale = sv;
+        sc0 *= sk_sub[sub] * inv_sq0;
+        sc1 *= sk_sub[sub] * inv_sq1;
+        pv_scale = sv_sub[sub];
       }
       // validity on item-local keys, causality on global positions
       const int kr0 = k16 + g, kr1 = k16 + g + 8;
@@ -304,25 +326,38 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       // ---- O^T += V^T P^T
       if constexpr (FP8) {
         const int kA = 16 * sub + 2 * t;
+        // masks only on the item's last, partial sub-tile
+        auto pv8 = [&](auto masked) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t ch = (g >> 2) + 2 * j;
-          const uint32_t bo = 4 * (g & 3);
-          const uint32_t wA = lds32(vbase + swz128(kA, ch) + bo);
-          const uint32_t wB = lds32(vbase + swz128(kA + 1, ch) + bo);
-          const uint32_t wC = lds32(vbase + swz128(kA + 8, ch) + bo);
-          const uint32_t wD = lds32(vbase + swz128(kA + 9, ch) + bo);
-          // pair the two keys' bytes per head-dim column, then convert
-          // in hardware: [A0 B0 A1 B1] and [A2 B2 A3 B3]
-          const uint32_t x01 = __byte_perm(wA, wB, 0x5140);
-          const uint32_t x23 = __byte_perm(wA, wB, 0x7362);
-          const uint32_t y01 = __byte_perm(wC, wD, 0x5140);
-          const uint32_t y23 = __byte_perm(wC, wD, 0x7362);
-          mma_f16(acc[2 * j], mlo & e4m3x2lo_to_f16x2(x01), mlo & e4m3x2hi_to_f16x2(x01),
-                  mhi & e4m3x2lo_to_f16x2(y01), mhi & e4m3x2hi_to_f16x2(y01), b0, b1);
-          mma_f16(acc[2 * j + 1], mlo & e4m3x2lo_to_f16x2(x23), mlo & e4m3x2hi_to_f16x2(x23),
-                  mhi & e4m3x2lo_to_f16x2(y23), mhi & e4m3x2hi_to_f16x2(y23), b0, b1);
-        }
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t ch = (g >> 2) + 2 * j;
+            const uint32_t bo = 4 * (g & 3);
+            const uint32_t wA = lds32(vbase + swz128(kA, ch) + bo);
+            const uint32_t wB = lds32(vbase + swz128(kA + 1, ch) + bo);
+            const uint32_t wC = lds32(vbase + swz128(kA + 8, ch) + bo);
+            const uint32_t wD = lds32(vbase + swz128(kA + 9, ch) + bo);
+            // pair the two keys' bytes per head-dim column, then convert
+            // in hardware: [A0 B0 A1 B1] and [A2 B2 A3 B3]
+            const uint32_t x01 = __byte_perm(wA, wB, 0x5140);
+            const uint32_t x23 = __byte_perm(wA, wB, 0x7362);
+            const uint32_t y01 = __byte_perm(wC, wD, 0x5140);
+            const uint32_t y23 = __byte_perm(wC, wD, 0x7362);
+            uint32_t a[8] = {e4m3x2lo_to_f16x2(x01), e4m3x2hi_to_f16x2(x01),
+                             e4m3x2lo_to_f16x2(y01), e4m3x2hi_to_f16x2(y01),
+                             e4m3x2lo_to_f16x2(x23), e4m3x2hi_to_f16x2(x23),
+                             e4m3x2lo_to_f16x2(y23), e4m3x2hi_to_f16x2(y23)};
+            if (decltype(masked)::value) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u) a[u] &= (u & 2) ? mhi : mlo;
+            }
+            mma_f16(acc[2 * j], a[0], a[1], a[2], a[3], b0, b1);
+            mma_f16(acc[2 * j + 1], a[4], a[5], a[6], a[7], b0, b1);
+          }
+        };
+        if (tail)
+          pv8(std::true_type{});
+        else
+          pv8(std::false_type{});
       } else {
         const int mi = lane >> 3;
         const int key = (mi >> 1) * 8 + (lane & 7);
