@@ -13,7 +13,6 @@
 
 namespace pkv {
 cudaError_t configure_decode();
-cudaError_t configure_prefill();
 cudaError_t configure_prefill_tc();
 cudaError_t configure_mixed();
 }  // namespace pkv
@@ -229,7 +228,7 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
       }
     } else {
       const int rows = q * G;
-      const int tile = prefill_uses_tc(c) ? kPfRowsTc : kPfRows;
+      const int tile = 2 * pf_tile_rows(std::min(G, kPfQTile));
       for (int h = 0; h < H; ++h) {
         for (int r0 = 0; r0 < rows; r0 += tile) {
           pkv_work_item w{};
@@ -389,7 +388,7 @@ pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out) {
     g_create_error = "cuTensorMapEncodeTiled is not available from the driver";
     return PKV_ERR_CUDA;
   }
-  if ((e = configure_decode()) != cudaSuccess || (e = configure_prefill()) != cudaSuccess ||
+  if ((e = configure_decode()) != cudaSuccess ||
       (e = configure_prefill_tc()) != cudaSuccess || (e = configure_mixed()) != cudaSuccess) {
     g_create_error = fmt("configuring kernels: %s", cudaGetErrorString(e));
     return PKV_ERR_CUDA;
@@ -400,7 +399,8 @@ pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out) {
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device);
   const int64_t G = config->num_q_heads / config->num_kv_heads;
   const int64_t pre_items =
-      (int64_t(config->max_num_tokens) * G / kPfRows + config->max_num_seqs) *
+      (int64_t(config->max_num_tokens) * G / (2 * pf_tile_rows(static_cast<int>(std::min<int64_t>(G, kPfQTile)))) +
+       config->max_num_seqs) *
       config->num_kv_heads;
   h->max_items = static_cast<int>(kMaxPartials + int64_t(config->max_num_seqs) * config->num_kv_heads + pre_items);
   h->work_bytes = items_bytes(h->max_items) + sizeof(int32_t) * (2 * size_t(config->max_num_seqs) + 1);
@@ -539,6 +539,9 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   if (fp8 && !plan.pre.empty())
     return fail(h, PKV_ERR_UNSUPPORTED,
                 "prefill rows (q * G > 8) over FP8 pools are not supported");
+  if (!plan.pre.empty() && !prefill_uses_tc(c))
+    return fail(h, PKV_ERR_UNSUPPORTED,
+                "prefill rows (q * G > 8) need at most 128 query heads per KV head");
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       !aligned16(out_f32))
     return fail(h, PKV_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
@@ -574,7 +577,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   if (k_cache != h->map_k_ptr || v_cache != h->map_v_ptr) {
     const int64_t rows = c.num_blocks * c.num_kv_heads * bs;
     const int dec_box = std::min(bs, fp8 ? kDecKeysFp8 : kDecKeysBf16);
-    const int pf_box = std::min(bs, prefill_uses_tc(c) ? 128 : kPfKeys);
+    const int pf_box = std::min(bs, 128);
     bool ok = encode_pool_map(&h->dec_k, k_cache, fp8, rows, dec_box) &&
               encode_pool_map(&h->dec_v, v_cache, fp8, rows, dec_box);
     if (ok && !fp8)
@@ -693,10 +696,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   }
   if (n_pre > 0) {
     timing_begin(h, PKV_KERNEL_PREFILL, s);
-    if (tc)
-      e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, pp, n_pre, s);
-    else
-      e = launch_prefill(h->pf_k, h->pf_v, pp, n_pre, s);
+    e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, pp, n_pre, s);
     timing_end(h, PKV_KERNEL_PREFILL, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
   }

@@ -40,11 +40,6 @@ constexpr int kDecSmemBytesFp8 =
 constexpr int kSplitAlign = 256;          // split ranges start at multiples
 
 // ---- prefill kernel geometry ---------------------------------------------------
-constexpr int kPfRows = 64;               // query rows per item (4 warps x 16)
-constexpr int kPfKeys = 64;               // keys per stage
-constexpr int kPfStages = 3;
-constexpr int kPfStageBytes = 2 * kPfKeys * kHeadDim * 2;  // K + V, bf16
-constexpr int kPfSmemBytes = kPfStages * kPfStageBytes + 1024 + 256;
 
 struct DecodeParams {
   const pkv_work_item *items;
@@ -133,9 +128,6 @@ cudaError_t launch_rope_append(const RopeAppendParams &p, bool fp8, bool neox, c
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
                           const DecodeParams &p, int num_items, bool fp8,
                           cudaStream_t s);
-cudaError_t launch_prefill(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                           const PrefillParams &p, int num_items,
-                           cudaStream_t s);
 cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p,
                               int num_items, cudaStream_t s);
@@ -149,14 +141,15 @@ cudaError_t launch_mixed(const CUtensorMap &qmap, const CUtensorMap &kmap_pf,
                          const DecodeParams &dp, int n_prefill, int n_decode,
                          cudaStream_t s);
 
-// Prefill tiles run on the tcgen05 kernel (128 rows) when the query group
-// size is a power of two (so a tile is a whole number of tokens) and the KV
-// pools are bf16; otherwise on the warp-MMA kernel (64 rows).
-constexpr int kPfRowsTc = 256;   // two 128-row Q tiles per item
+// Prefill runs on the tcgen05 kernel: a work item is two Q tiles of
+// pf_tile_rows(G) = G * floor(128 / G) rows (whole tokens of G query heads;
+// 128 for powers of two, the rest of the 128 TMEM lanes idle otherwise).
+// It needs G <= 128 and a bf16 pool.
 constexpr int kPfQTile = 128;
+constexpr int pf_tile_rows(int G) { return G * (kPfQTile / G); }
 inline bool prefill_uses_tc(const pkv_config &c) {
   const int G = c.num_q_heads / c.num_kv_heads;
-  return G > 0 && (G & (G - 1)) == 0 && G <= 128 && c.kv_dtype == PKV_KV_BF16;
+  return G > 0 && G <= kPfQTile && c.kv_dtype == PKV_KV_BF16;
 }
 cudaError_t configure_kernels();
 

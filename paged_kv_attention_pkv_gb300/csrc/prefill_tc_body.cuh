@@ -104,11 +104,14 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   // Q tile t holds rows [row0 + 128 t, +n_t) and reaches keys [0, kend_t)
-  const int n0 = it.n_rows < 128 ? it.n_rows : 128;
+  // a Q tile holds R = G * floor(128 / G) rows (whole tokens); TMEM lanes
+  // R .. 127 compute on stale rows that are never stored
+  const int R = pf_tile_rows(G);
+  const int n0 = it.n_rows < R ? it.n_rows : R;
   const int n1 = it.n_rows - n0;
   const bool two = n1 > 0;
   const int kend0 = it.hist + (it.row0 + n0 - 1) / G + 1;
-  const int kend1 = two ? it.hist + (it.row0 + 128 + n1 - 1) / G + 1 : kend0;
+  const int kend1 = two ? it.hist + (it.row0 + R + n1 - 1) / G + 1 : kend0;
   const int k_end = it.k_end;                   // = kend1
   const int nt0 = (kend0 + 127) / 128;
   const int nt1 = two ? (kend1 + 127) / 128 : 0;
@@ -172,7 +175,8 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       return y;
     };
     if (is_k && lane == 0) {
-      mbar_arrive_expect_tx(q_full, two ? 2 * kTile : kTile);
+      // each box carries R rows of 128 bytes per 64-column half
+      mbar_arrive_expect_tx(q_full, (two ? 2 : 1) * 2 * R * 128);
       const int t0 = it.tok0 + it.row0 / G;
       tma_load_3d(smem + kOffQ, &qmap, 0, it.kv_head * G, t0, q_full);
       tma_load_3d(smem + kOffQ + kHalf, &qmap, 64, it.kv_head * G, t0, q_full);
@@ -274,7 +278,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     const int ntl = t == 0 ? nt0 : nt1;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t col_s = t * 128, col_o = 256 + t * 128;
-    const int rowg = it.row0 + 128 * t + r;
+    const int rowg = it.row0 + R * t + r;
     const bool row_ok = r < nrow;
     const int pos = it.hist + rowg / G;   // padded rows see every key
     const float c = p.scale_log2;

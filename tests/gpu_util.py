@@ -84,12 +84,13 @@ def gpu_rows(out: torch.Tensor, lse: torch.Tensor, sub: dict, rows=None):
     return o, l
 
 
-# Peaked variants (queries scaled x8, so a few keys dominate each softmax)
-# have outputs of order 1 (up to ~4), where rounding the output to bf16 alone
-# costs up to half an ulp, 2^-8 |x|, and rounding P to bf16 about 2^-9 |x|
-# more.  Their bounds therefore grow with |ref| (derived, not given): each
-# element within max_abs + 2^-7 |ref|, the mean within mean_abs + 2^-8
-# mean|ref|.  The five workloads keep the plain absolute bounds.
+# Outputs of order 1 (few visible keys, or peaked variants whose queries are
+# scaled x8 so a few keys dominate each softmax) cannot meet a purely
+# absolute bound: rounding the output to bf16 alone costs up to half an ulp,
+# 2^-8 |x| (0.0156 at |x| = 4), and rounding P to bf16 about 2^-9 |x| more.
+# Each element is therefore checked against max_abs + 2^-7 |ref| (derived,
+# not given; for the long-context workloads |ref| << 1 and this is the plain
+# gate).  Peaked variants also relax the mean to mean_abs + 2^-8 mean|ref|.
 PEAKED_ELEM_REL = 2.0 ** -7
 PEAKED_MEAN_REL = 2.0 ** -8
 
@@ -101,12 +102,9 @@ def check(got, ref, got_lse, ref_lse, kind: str = "bf16", what: str = "",
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     err = np.abs(got - ref)
-    if peaked:
-        excess = err - (t["max_abs"] + PEAKED_ELEM_REL * np.abs(ref))
-        assert excess.max() <= 0, f"{what}: element error {err.flat[excess.argmax()]:.3e} " \
-            f"at |ref| {np.abs(ref).flat[excess.argmax()]:.3e}"
-    else:
-        assert err.max() <= t["max_abs"], f"{what}: max-abs {err.max():.3e}"
+    excess = err - (t["max_abs"] + PEAKED_ELEM_REL * np.abs(ref))
+    assert excess.max() <= 0, f"{what}: element error {err.flat[excess.argmax()]:.3e} " \
+        f"at |ref| {np.abs(ref).flat[excess.argmax()]:.3e}"
     mean_bound = t["mean_abs"] + (PEAKED_MEAN_REL * np.abs(ref).mean() if peaked else 0.0)
     assert err.mean() <= mean_bound, f"{what}: mean-abs {err.mean():.3e} > {mean_bound:.3e}"
     rel = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)

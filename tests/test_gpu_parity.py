@@ -74,7 +74,12 @@ SWEEP = [
     ("gqa8_bs64", 64, 8, 64, [1, 1, 2, 17, 1], [1, 64, 65, 1000, 4097], "bf16"),
     ("gqa2_bs32", 4, 2, 32, [3, 1, 31, 33], [3, 32, 95, 33], "bf16"),
     ("gqa4_bs128", 8, 2, 128, [2, 70], [129, 300], "bf16"),
-    ("gqa3_warpmma", 6, 2, 16, [1, 2, 3, 40, 22], [5, 100, 40, 300, 22], "bf16"),
+    # query groups that are not powers of two: Q tiles of G * floor(128 / G) rows
+    ("gqa3_tc", 6, 2, 16, [1, 2, 3, 40, 22, 130], [5, 100, 40, 300, 22, 900], "bf16"),
+    ("gqa5_tc", 40, 8, 16, [1, 30, 51, 100], [70, 300, 51, 1000], "bf16"),
+    ("gqa6_bs64", 48, 8, 64, [1, 43, 200], [1, 600, 2100], "bf16"),
+    ("gqa12_tc", 96, 8, 16, [11, 25], [400, 25], "bf16"),
+    ("gqa96_tc", 96, 1, 32, [1, 3, 5], [64, 700, 5], "bf16"),
     ("gqa16_tc", 32, 2, 16, [1, 9, 200], [300, 1000, 4000], "bf16"),
     ("fp8_gqa8_bs64", 64, 8, 64, [1, 1, 1, 1], [1, 63, 65, 5000], "fp8"),
     ("fp8_gqa4_bs16", 32, 8, 16, [1, 2, 1], [17, 33, 2000], "fp8"),
@@ -305,6 +310,13 @@ def test_host_argument_errors():
     h.attention_varlen(b.q[:0], b.k_cache, b.v_cache, m["qsl"][:1], m["lens"][:0],
                        m["bt"], np.zeros(1, np.int32), np.zeros(0, np.int32))
     h.close()
+
+
+def test_query_groups_above_128_refuse_prefill_rows():
+    b = W.generate(spec("g256", 256, 1, 16, [1, 2], [40, 50]), DEV)
+    with pytest.raises(pkv.PkvError) as e:
+        U.gpu_step(b)
+    assert "128 query heads per KV head" in str(e.value)
 
 
 def test_fp8_prefill_is_reported_unsupported():
