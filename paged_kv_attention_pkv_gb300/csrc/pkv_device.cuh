@@ -308,6 +308,26 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
+// The same MMAs with the accumulate flag fixed (no predicate to compute).
+__device__ __forceinline__ void tc_mma_first(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem),
+               "l"(a_desc), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+               "l"(a_desc), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma_tmem_a_acc(uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint64_t b_desc, uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
+               "r"(a_tmem), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
+
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

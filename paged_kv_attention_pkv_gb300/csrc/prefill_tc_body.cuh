@@ -218,14 +218,19 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         // K arrives by TMA (async proxy, like the MMA): the mbarrier alone
         // orders it, and a tcgen05 fence here would drain the MMA pipe
         if (!mbar_wait(&k_full[s], (j / kKst) & 1)) return false;
-        const uint32_t qa = smem_addr(smem + kOffQ + t * kTile);
-        const uint32_t ka = smem_addr(smem + kOffK + s * kTile);
+        // descriptors built once per group; the k-steps add constant
+        // offsets to the start-address field (addresses stay < 256 KB, so
+        // the 14-bit field never carries)
+        const uint64_t a0 = smem_desc_sw128(smem_addr(smem + kOffQ + t * kTile), 16, 1024);
+        const uint64_t b0 = smem_desc_sw128(smem_addr(smem + kOffK + s * kTile), 16, 1024);
         const uint32_t d = tmem + t * 128;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(qa + off, 16, 1024);
-          tc_mma(d, ad, smem_desc_sw128(ka + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
+          const uint64_t off = ((ks >> 2) * kHalf + (ks & 3) * 32) >> 4;
+          if (ks == 0)
+            tc_mma_first(d, a0, b0, kIdescQK);
+          else
+            tc_mma_acc(d, a0 + off, b0 + off, kIdescQK);
         }
         tc_commit(&s_full[t]);
         return true;
@@ -235,12 +240,15 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         if (!mbar_wait(&p_full[t], j & 1)) return false;
         if (!mbar_wait(&v_full[s], (j / kVst) & 1)) return false;
         tc_fence_after();
-        const uint32_t va = smem_addr(smem + kOffV + s * kTile);
+        const uint64_t b0 = smem_desc_sw128(smem_addr(smem + kOffV + s * kTile), kHalf, 1024);
+        const uint32_t dO = tmem + 256 + t * 128, aP = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = smem_desc_sw128(va + kk * 2048, kHalf, 1024);
-          tc_mma_tmem_a(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, bd, kIdescPV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
+          const uint64_t bd = b0 + ((kk * 2048) >> 4);
+          if (kk > 0)
+            tc_mma_tmem_a_acc(dO, aP + kk * 8, bd, kIdescPV);
+          else
+            tc_mma_tmem_a(dO, aP, bd, kIdescPV, j > 0 ? 1u : 0u);
         }
         tc_commit(&o_done[t]);
         return true;
