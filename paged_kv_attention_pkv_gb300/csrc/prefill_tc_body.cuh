@@ -15,12 +15,12 @@ namespace {
 // TMEM owner), warp 9 (TMA producer) and two idle warps completing
 // warpgroup 2, so registers can move between warpgroups (setmaxnreg): the
 // launch gives every thread 168; warpgroup 2 drops to kRegsCtl and the
-// softmax warpgroups rise to kRegsSoftmax (2 x 128 x 208 + 128 x 88 =
+// softmax warpgroups rise to kRegsSoftmax (2 x 128 x 216 + 128 x 72 =
 // 384 x 168, the registers the CTA was launched with; neither side spills).
 constexpr int kTcThreads = 384;
 constexpr uint32_t kRegsLaunch = 168;
-constexpr uint32_t kRegsCtl = 88;
-constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsCtl = 72;
+constexpr uint32_t kRegsSoftmax = 216;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsCtl == kTcThreads * kRegsLaunch,
               "register split must use exactly the launch's registers");
 constexpr int kKst = 2;                           // K ring depth
@@ -213,16 +213,22 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     // ---------------- MMA issuer (one thread) ----------------
     if (lane == 0) {
       bool ok = mbar_wait(q_full, 0);
+      // Descriptors are built once; tiles, stages and k-steps add constant
+      // offsets to the start-address field (addresses stay < 256 KB, so the
+      // 14-bit field never carries).  The issuing warp shares its SM
+      // sub-partition with two softmax warps: every instruction it issues
+      // between MMA groups is time the tensor pipe may sit idle.
+      constexpr uint64_t kTileDesc = kTile >> 4;
+      const uint64_t qd0 = smem_desc_sw128(smem_addr(smem + kOffQ), 16, 1024);
+      const uint64_t kd0 = smem_desc_sw128(smem_addr(smem + kOffK), 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(smem_addr(smem + kOffV), kHalf, 1024);
       auto qk = [&](int t, int j) {   // S_t = Q_t K_j^T
-        const int s = j % kKst;
+        const int s = j & (kKst - 1);
         // K arrives by TMA (async proxy, like the MMA): the mbarrier alone
-        // orders it, and a tcgen05 fence here would drain the MMA pipe
+        // orders it
         if (!mbar_wait(&k_full[s], (j / kKst) & 1)) return false;
-        // descriptors built once per group; the k-steps add constant
-        // offsets to the start-address field (addresses stay < 256 KB, so
-        // the 14-bit field never carries)
-        const uint64_t a0 = smem_desc_sw128(smem_addr(smem + kOffQ + t * kTile), 16, 1024);
-        const uint64_t b0 = smem_desc_sw128(smem_addr(smem + kOffK + s * kTile), 16, 1024);
+        const uint64_t a0 = qd0 + t * kTileDesc;
+        const uint64_t b0 = kd0 + s * kTileDesc;
         const uint32_t d = tmem + t * 128;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
@@ -235,12 +241,11 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         tc_commit(&s_full[t]);
         return true;
       };
-      auto pv = [&](int t, int j) {   // O_t += P_t V_j
-        const int s = j % kVst;
+      auto pv = [&](int t, int j, int s, int vpar) {   // O_t += P_t V_j, V_j in stage s
         if (!mbar_wait(&p_full[t], j & 1)) return false;
-        if (!mbar_wait(&v_full[s], (j / kVst) & 1)) return false;
+        if (!mbar_wait(&v_full[s], vpar)) return false;
         tc_fence_after();
-        const uint64_t b0 = smem_desc_sw128(smem_addr(smem + kOffV + s * kTile), kHalf, 1024);
+        const uint64_t b0 = vd0 + s * kTileDesc;
         const uint32_t dO = tmem + 256 + t * 128, aP = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -261,18 +266,24 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       // PV_t(j) (tcgen05.mma of one thread execute in order).
       // V_j is released as soon as its last PV is issued, K_{j+1} after its
       // last QK.
+      static_assert((kKst & (kKst - 1)) == 0, "K ring depth: a power of two");
+      int vs = 0, vpar = 0;   // V_j's stage and its phase parity
       for (int j = 0; ok && j < n_tiles; ++j) {
         if (j < nt0) {
-          ok = pv(0, j);
+          ok = pv(0, j, vs, vpar);
           if (ok && j + 1 < nt0) ok = qk(0, j + 1);
         }
         const bool t1 = two && j < nt1;
-        if (ok && t1) ok = pv(1, j);
+        if (ok && t1) ok = pv(1, j, vs, vpar);
         if (!ok) break;
-        tc_commit(&v_empty[j % kVst]);
+        tc_commit(&v_empty[vs]);
+        if (++vs == kVst) {
+          vs = 0;
+          vpar ^= 1;
+        }
         if (t1 && j + 1 < nt1) ok = qk(1, j + 1);
         if (!ok) break;
-        if (j + 1 < n_tiles) tc_commit(&k_empty[(j + 1) % kKst]);
+        if (j + 1 < n_tiles) tc_commit(&k_empty[(j + 1) & (kKst - 1)]);
       }
       if (!ok) record_error(p.err, kErrTimeout);
     }
