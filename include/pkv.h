@@ -173,6 +173,10 @@ pkv_status pkv_rope_write_slots(pkv_handle *h, void *q, const void *k_new,
  * executed by the kernels.  The new tokens' K/V must already be in the pools
  * (call pkv_write_slots first on the same stream).  A step that needs more
  * workspace than the handle was created for returns PKV_ERR_WORKSPACE.
+ * Requests with more than 8 query rows per KV head (q_i * G > 8) run on the
+ * tensor-core prefill kernel over bf16 pools with G <= 128; over E4M3 pools,
+ * or with G > 128, the decode kernel takes their rows 8 at a time (same
+ * results within tolerance, at memory-bound speed).
  */
 pkv_status pkv_attention_varlen(pkv_handle *h, const void *q,
                                 const void *k_cache, const void *v_cache,
@@ -281,7 +285,9 @@ pkv_status pkv_destroy(pkv_handle *h);
  * row range and a key range.  Rows r = t * G + g enumerate (query token t,
  * head g of the group). */
 typedef struct {
-    int32_t kind;        /* 0 = split-KV decode, 1 = prefill tile */
+    int32_t kind;        /* 0 = decode kernel (decode rows, or a chunk of
+                            8 prefill rows over E4M3 pools / G > 128),
+                            1 = tensor-core prefill tile */
     int32_t seq;         /* request index */
     int32_t kv_head;
     int32_t tok0;        /* index of the request's first query token in q */
@@ -299,7 +305,7 @@ typedef struct {
  * Plan a step on the host without a GPU: the work items the kernels of
  * pkv_attention_varlen would run for these lengths on a device with
  * `num_sms` multiprocessors.  Items of each kind are in launch order
- * (longest first).  *num_items receives the count; if it exceeds
+ * (longest first; the prefill items of one (request, KV head) adjacent).  *num_items receives the count; if it exceeds
  * max_items only the first max_items are stored.  *num_partials receives the
  * split partial slots used.  Errors: PKV_ERR_INVALID_ARG for inconsistent
  * metadata (same checks as pkv_attention_varlen).

@@ -226,6 +226,30 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
           plan->dec.push_back(w);
         }
       }
+    } else if (!prefill_uses_tc(c)) {
+      // E4M3 pools and groups above 128: the decode kernel takes the prefill
+      // rows in chunks of kDecCols, each over its own causal key range.  The
+      // chunks of one (request, KV head) are adjacent in the list, so CTAs
+      // running together read the same keys and mostly hit L2.
+      const int rows = q * G;
+      for (int h = 0; h < H; ++h) {
+        for (int r0 = 0; r0 < rows; r0 += kDecCols) {
+          pkv_work_item w{};
+          w.kind = 0;
+          w.seq = i;
+          w.kv_head = h;
+          w.tok0 = qsl[i];
+          w.row0 = r0;
+          w.n_rows = std::min(kDecCols, rows - r0);
+          w.hist = hist;
+          w.k_begin = 0;
+          w.k_end = hist + (r0 + w.n_rows - 1) / G + 1;
+          w.part = -1;
+          w.pair = -1;
+          w.n_split = 1;
+          plan->dec.push_back(w);
+        }
+      }
     } else {
       const int rows = q * G;
       const int tile = 2 * pf_tile_rows(std::min(G, kPfQTile));
@@ -250,11 +274,39 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
     }
   }
   plan->partials = part;
+  // Decode items longest first.  Prefill row chunks (row0 > 0 or more than
+  // one chunk per request) stay together per (request, KV head), the group
+  // placed by its longest chunk, so the CTAs of a group run side by side.
   auto dec_cost = [](const pkv_work_item &w) { return int64_t(w.k_end) - w.k_begin; };
-  std::stable_sort(plan->dec.begin(), plan->dec.end(),
-                   [&](const pkv_work_item &a, const pkv_work_item &b) {
-                     return dec_cost(a) > dec_cost(b);
-                   });
+  {
+    const size_t n = plan->dec.size();
+    std::vector<int64_t> unit_cost(n), unit_id(n);
+    std::vector<int64_t> group_max(size_t(B) * H, -1);
+    auto chunked = [&](const pkv_work_item &w) {
+      return int64_t(qsl[w.seq + 1] - qsl[w.seq]) * G > kDecCols;
+    };
+    for (const auto &w : plan->dec)
+      if (chunked(w)) {
+        int64_t &m = group_max[size_t(w.seq) * H + w.kv_head];
+        m = std::max(m, dec_cost(w));
+      }
+    for (size_t k = 0; k < n; ++k) {
+      const pkv_work_item &w = plan->dec[k];
+      const bool ch = chunked(w);
+      unit_cost[k] = ch ? group_max[size_t(w.seq) * H + w.kv_head] : dec_cost(w);
+      unit_id[k] = ch ? int64_t(w.seq) * H + w.kv_head : int64_t(B) * H + int64_t(k);
+    }
+    std::vector<size_t> order(n);
+    for (size_t k = 0; k < n; ++k) order[k] = k;
+    std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) {
+      if (unit_cost[a] != unit_cost[b]) return unit_cost[a] > unit_cost[b];
+      if (unit_id[a] != unit_id[b]) return unit_id[a] < unit_id[b];
+      return dec_cost(plan->dec[a]) > dec_cost(plan->dec[b]);
+    });
+    std::vector<pkv_work_item> sorted(n);
+    for (size_t k = 0; k < n; ++k) sorted[k] = plan->dec[order[k]];
+    plan->dec.swap(sorted);
+  }
   // Prefill tiles of one (request, KV head) read the same K/V stream: keep
   // them adjacent so the CTAs running together share it through L2, and
   // order the groups longest first.
@@ -398,11 +450,20 @@ pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out) {
   h->device = device;
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device);
   const int64_t G = config->num_q_heads / config->num_kv_heads;
+  // prefill rows: 256-row tiles on the tensor-core kernel, else chunks of
+  // kDecCols rows on the decode kernel
+  const int64_t pre_rows = prefill_uses_tc(*config)
+                               ? 2 * pf_tile_rows(static_cast<int>(std::min<int64_t>(G, kPfQTile)))
+                               : kDecCols;
   const int64_t pre_items =
-      (int64_t(config->max_num_tokens) * G / (2 * pf_tile_rows(static_cast<int>(std::min<int64_t>(G, kPfQTile)))) +
-       config->max_num_seqs) *
-      config->num_kv_heads;
-  h->max_items = static_cast<int>(kMaxPartials + int64_t(config->max_num_seqs) * config->num_kv_heads + pre_items);
+      (int64_t(config->max_num_tokens) * G / pre_rows + config->max_num_seqs) * config->num_kv_heads;
+  const int64_t max_items = kMaxPartials + int64_t(config->max_num_seqs) * config->num_kv_heads + pre_items;
+  if (max_items > INT32_MAX / 2) {
+    g_create_error = "max_num_tokens * query group too large for the work list";
+    delete h;
+    return PKV_ERR_INVALID_ARG;
+  }
+  h->max_items = static_cast<int>(max_items);
   h->work_bytes = items_bytes(h->max_items) + sizeof(int32_t) * (2 * size_t(config->max_num_seqs) + 1);
   bool ok = cudaMalloc(&h->d_work, h->work_bytes) == cudaSuccess &&
             cudaMalloc(&h->d_part_o, sizeof(float) * size_t(kMaxPartials) * kDecCols * kHeadDim) == cudaSuccess &&
@@ -536,12 +597,6 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   const bool fp8 = c.kv_dtype == PKV_KV_FP8_E4M3;
   if (fp8 && (!k_scale || !v_scale))
     return fail(h, PKV_ERR_INVALID_ARG, "FP8 pools need k_scale and v_scale");
-  if (fp8 && !plan.pre.empty())
-    return fail(h, PKV_ERR_UNSUPPORTED,
-                "prefill rows (q * G > 8) over FP8 pools are not supported");
-  if (!plan.pre.empty() && !prefill_uses_tc(c))
-    return fail(h, PKV_ERR_UNSUPPORTED,
-                "prefill rows (q * G > 8) need at most 128 query heads per KV head");
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       !aligned16(out_f32))
     return fail(h, PKV_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");

@@ -83,6 +83,11 @@ SWEEP = [
     ("gqa16_tc", 32, 2, 16, [1, 9, 200], [300, 1000, 4000], "bf16"),
     ("fp8_gqa8_bs64", 64, 8, 64, [1, 1, 1, 1], [1, 63, 65, 5000], "fp8"),
     ("fp8_gqa4_bs16", 32, 8, 16, [1, 2, 1], [17, 33, 2000], "fp8"),
+    # prefill rows without tensor-core tiles: 8-row chunks on the decode kernel
+    ("fp8_prefill_gqa4", 32, 8, 16, [1, 40, 3, 130], [17, 300, 2000, 130], "fp8"),
+    ("fp8_prefill_gqa8_bs64", 64, 8, 64, [1, 70, 5], [5000, 700, 65], "fp8"),
+    ("fp8_prefill_gqa3", 6, 2, 64, [10, 1, 33], [100, 64, 1500], "fp8"),
+    ("gqa256_chunks", 256, 1, 16, [1, 2, 9], [40, 50, 300], "bf16"),
 ]
 
 
@@ -312,16 +317,3 @@ def test_host_argument_errors():
     h.close()
 
 
-def test_query_groups_above_128_refuse_prefill_rows():
-    b = W.generate(spec("g256", 256, 1, 16, [1, 2], [40, 50]), DEV)
-    with pytest.raises(pkv.PkvError) as e:
-        U.gpu_step(b)
-    assert "128 query heads per KV head" in str(e.value)
-
-
-def test_fp8_prefill_is_reported_unsupported():
-    s = spec("fp8pf", 8, 2, 64, [40], [100], kv="fp8")
-    b = W.generate(s, DEV)
-    with pytest.raises(pkv.PkvError) as e:
-        U.gpu_step(b)
-    assert e.value.status == 2

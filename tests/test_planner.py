@@ -29,11 +29,16 @@ def test_plan_covers_the_workloads(index):
         i, h = w["seq"], w["kv_head"]
         q, L = spec.q_lens[i], spec.seq_lens[i]
         assert w["tok0"] == qsl[i] and w["hist"] == L - q
-        if w["kind"] == 0:
-            assert q * G <= 8 and w["row0"] == 0 and w["n_rows"] == q * G
+        if w["kind"] == 0 and q * G <= 8:
+            assert w["row0"] == 0 and w["n_rows"] == q * G
             dec_keys.setdefault((i, h), []).append((w["k_begin"], w["k_end"], w))
         else:
             assert q * G > 8
+            # bf16 pools with G <= 128 use tensor-core tiles, the rest 8-row
+            # chunks on the decode kernel
+            assert w["kind"] == (1 if spec.kv_dtype == "bf16" and G <= 128 else 0)
+            if w["kind"] == 0:
+                assert w["n_rows"] <= 8 and w["row0"] % 8 == 0 and w["part"] == -1
             assert w["k_begin"] == 0
             last_tok = (w["row0"] + w["n_rows"] - 1) // G
             assert w["k_end"] == L - q + last_tok + 1          # causal reach
@@ -109,3 +114,35 @@ def test_plan_empty_and_zero_token_requests():
     assert all(w["seq"] == 1 for w in items) and parts == 0
     items, parts = pkv.plan(cfg, np.asarray([0], np.int32), np.asarray([], np.int32))
     assert items == []
+
+
+@pytest.mark.parametrize("kv,hq,hkv", [("fp8", 32, 8), ("fp8", 6, 2), ("bf16", 256, 1)])
+def test_prefill_rows_without_tensor_core_tiles_are_chunked(kv, hq, hkv):
+    """Over E4M3 pools, or with query groups above 128, prefill rows become
+    decode-kernel items of at most 8 rows: they tile [0, q*G) exactly, each
+    reaches keys up to its last token's position, writes the output directly,
+    and the chunks of one (request, KV head) are adjacent in launch order."""
+    spec = workloads.custom_spec("chunks", hq, hkv, 16, [1, 40, 3, 130],
+                                 [17, 300, 2000, 130], seed=3, kv_dtype=kv)
+    items, parts, qsl = _plan(spec)
+    G = hq // hkv
+    assert all(w["kind"] == 0 for w in items)
+    rows = {}
+    order = []
+    for w in items:
+        i, h = w["seq"], w["kv_head"]
+        q, L = spec.q_lens[i], spec.seq_lens[i]
+        if q * G <= 8:
+            continue
+        assert w["k_begin"] == 0 and w["part"] == -1 and w["n_split"] == 1
+        assert w["k_end"] == L - q + (w["row0"] + w["n_rows"] - 1) // G + 1
+        rows.setdefault((i, h), []).append((w["row0"], w["n_rows"]))
+        if not order or order[-1] != (i, h):
+            order.append((i, h))
+    assert len(order) == len(set(order))                   # contiguous groups
+    for (i, h), rs in rows.items():
+        rs.sort()
+        assert [r0 for r0, _ in rs] == list(range(0, spec.q_lens[i] * G, 8))
+        assert sum(n for _, n in rs) == spec.q_lens[i] * G
+    chunked = {i for i, q in enumerate(spec.q_lens) if q * G > 8}
+    assert set(rows) == {(i, h) for i in chunked for h in range(hkv)}
