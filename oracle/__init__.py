@@ -7,7 +7,8 @@ states what is computed and which page and section each step follows.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force against a library attention routine, closed forms, invariances,
-the FP8 format definition and a library FP8 cast) and by
+the FP8 format definition and a library FP8 cast, the FP4 format's published
+value table and brute-force nearest rounding) and by
 ``tests/test_oracle_mutations.py`` (planted mistakes must fail those pins).
 """
 from __future__ import annotations
@@ -45,6 +46,13 @@ def load(path: str | None = None):
     lib.pko_e4m3_encode.argtypes = [ctypes.c_float]
     lib.pko_e4m3_quantize.restype = ctypes.c_uint8
     lib.pko_e4m3_quantize.argtypes = [ctypes.c_uint16, ctypes.c_float]
+    lib.pko_e2m1_value.restype = ctypes.c_double
+    lib.pko_e2m1_value.argtypes = [ctypes.c_uint8]
+    lib.pko_e2m1_encode.restype = ctypes.c_uint8
+    lib.pko_e2m1_encode.argtypes = [ctypes.c_float]
+    lib.pko_nvfp4_quantize_row.restype = None
+    lib.pko_nvfp4_quantize_row.argtypes = [_u16p, ctypes.c_int, ctypes.c_float,
+                                           ctypes.c_void_p, ctypes.c_void_p]
     lib.pko_write_slots.restype = ctypes.c_int
     lib.pko_write_slots.argtypes = [
         ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -122,6 +130,39 @@ def e4m3_quantize(x_bf16_bits: int, scale: float) -> int:
     return int(load().pko_e4m3_quantize(x_bf16_bits, scale))
 
 
+def e2m1_value(code: int) -> float:
+    return float(load().pko_e2m1_value(code))
+
+
+def e2m1_encode(x: float) -> int:
+    return int(load().pko_e2m1_encode(x))
+
+
+def nvfp4_quantize_row(x_bf16_bits: np.ndarray, scale: float):
+    """NVFP4 codes (``d/2`` bytes) and E4M3 micro scales (``d/16``) of one
+    row of bf16 bits under the (block, KV head) scale."""
+    x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+    d = x.shape[0]
+    codes = np.zeros(d // 2, np.uint8)
+    ms = np.zeros(d // 16, np.uint8)
+    load().pko_nvfp4_quantize_row(x, d, float(scale), _ptr(codes), _ptr(ms))
+    return codes, ms
+
+
+def _pool_format(cache: np.ndarray, d: int | None = None):
+    """(kv_fmt, num_blocks, hkv, bs, d) of a pool array: bf16 bits
+    [nb, hkv, bs, d] uint16, E4M3 codes [nb, hkv, bs, d] uint8, or NVFP4
+    tiles [nb, hkv, bs * 9 d / 16] uint8 (d = 128 unless given)."""
+    if cache.ndim == 3:
+        assert cache.dtype == np.uint8
+        d = d or 128
+        nb, hkv, tile = cache.shape
+        assert tile % (9 * d // 16) == 0
+        return 2, nb, hkv, tile // (9 * d // 16), d
+    nb, hkv, bs, dd = cache.shape
+    return (1 if cache.dtype == np.uint8 else 0), nb, hkv, bs, dd
+
+
 def write_slots(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray,
                 v_new: np.ndarray, slot_mapping: np.ndarray,
                 k_scale: np.ndarray | None = None,
@@ -129,19 +170,20 @@ def write_slots(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray,
     """Scatter new K/V rows into the pools in place.
 
     Pools are ``[num_blocks, Hkv, bs, D]`` arrays of uint16 (bf16 bits) or
-    uint8 (E4M3 codes, with ``[num_blocks, Hkv]`` float32 scales).  ``k_new``
-    and ``v_new`` are ``[T, Hkv, D]`` uint16 bf16 bits.
+    uint8 (E4M3 codes), or ``[num_blocks, Hkv, bs * 9 D / 16]`` uint8 NVFP4
+    tiles; quantised pools come with ``[num_blocks, Hkv]`` float32 scales.
+    ``k_new`` and ``v_new`` are ``[T, Hkv, D]`` uint16 bf16 bits.
     """
     lib = lib or load()
-    fp8 = k_cache.dtype == np.uint8
-    nb, hkv, bs, d = k_cache.shape
+    fmt, nb, hkv, bs, d = _pool_format(k_cache, k_new.shape[-1])
+    quantised = fmt != 0
     assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
     st = lib.pko_write_slots(
-        int(fp8), int(k_new.shape[0]), hkv, d, bs, nb,
+        fmt, int(k_new.shape[0]), hkv, d, bs, nb,
         np.ascontiguousarray(k_new), np.ascontiguousarray(v_new),
         np.ascontiguousarray(slot_mapping, dtype=np.int64),
         _ptr(k_cache), _ptr(v_cache),
-        _ptr(k_scale) if fp8 else None, _ptr(v_scale) if fp8 else None)
+        _ptr(k_scale) if quantised else None, _ptr(v_scale) if quantised else None)
     if st != 0:
         raise ValueError(f"oracle write_slots rejected its arguments ({st})")
 
@@ -162,9 +204,9 @@ def attention(k_cache: np.ndarray, v_cache: np.ndarray, q: np.ndarray,
     tokens are dealt out in runs of ``k`` (run ``j`` to rank ``j % n``).
     """
     lib = lib or load()
-    fp8 = k_cache.dtype == np.uint8
-    nb, hkv, bs, d = k_cache.shape
     t, hq, dq = q.shape
+    fmt, nb, hkv, bs, d = _pool_format(k_cache, dq)
+    quantised = fmt != 0
     assert dq == d
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
     assert bt.ndim == 2
@@ -178,10 +220,10 @@ def attention(k_cache: np.ndarray, v_cache: np.ndarray, q: np.ndarray,
     lo, hi = (0, np.iinfo(np.int64).max) if k_range is None else k_range
     k_cache = np.ascontiguousarray(k_cache)
     v_cache = np.ascontiguousarray(v_cache)
-    ks = np.ascontiguousarray(k_scale, dtype=np.float32) if fp8 else None
-    vs = np.ascontiguousarray(v_scale, dtype=np.float32) if fp8 else None
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32) if quantised else None
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32) if quantised else None
     st = lib.pko_attention(
-        int(fp8), _ptr(k_cache), _ptr(v_cache), _ptr(ks), _ptr(vs), nb, hkv, d,
+        fmt, _ptr(k_cache), _ptr(v_cache), _ptr(ks), _ptr(vs), nb, hkv, d,
         bs, hq, np.ascontiguousarray(q), qsl, seq_lens, bt, bt.shape[1],
         int(seq_lens.shape[0]), t, float(softmax_scale), int(lo), int(hi),
         *((1, 0, 1) if shard is None else tuple(int(x) for x in shard)),

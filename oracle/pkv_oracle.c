@@ -46,8 +46,23 @@
  * * scale.  Quantisation on append divides in fp32 and rounds to nearest,
  * ties to even, saturating at +-448.
  *
+ * NVFP4 KV (the compressed KV format the pages name, nearly half the size
+ * of FP8: page "vLLM 优化 DeepSeek-V4.1-Flash：智能体吞吐提升 5 倍", section
+ * Kernels, MegaAttention with NVFP4 KV) is read here as: OCP FP4 E2M1 element codes (sign, two exponent bits
+ * with bias 1, one mantissa bit; largest 6, no infinities or NaN), two per
+ * byte, low nibble first; one E4M3 scale per 16 consecutive elements of a
+ * row; and the per-(block, KV head) fp32 scale as the second level.  An
+ * element's value is e2m1(code) * e4m3(micro scale) * scale.  Quantisation
+ * (the reading taken; the pages give none): amax = largest |x| of the 16
+ * values, micro scale = E4M3(amax / (6 * scale)), and, unless that micro
+ * scale is zero (then every code is 0), code = E2M1(x / (scale * micro
+ * scale)), every product and quotient rounded to fp32, E2M1 rounding to
+ * nearest with ties to even and saturating at +-6.
+ *
  * Pool layout: [num_blocks][num_kv_heads][block_size][head_dim], so slot s of
- * KV head h is row ((s / bs) * Hkv + h) * bs + s % bs.
+ * KV head h is row ((s / bs) * Hkv + h) * bs + s % bs.  NVFP4 pools hold,
+ * per (block, KV head), block_size rows of head_dim / 2 code bytes followed
+ * by block_size rows of head_dim / 16 micro-scale bytes.
  */
 #include <math.h>
 #include <stdint.h>
@@ -174,21 +189,95 @@ uint8_t pko_e4m3_quantize(uint16_t x_bf16, float scale)
     return pko_e4m3_encode(q);
 }
 
+/* OCP FP4 E2M1 decode of the low 4 bits of `code`, written from the format
+ * definition: exponent field 0 is subnormal (0.m * 2^0), else 1.m * 2^(e-1). */
+double pko_e2m1_value(uint8_t code)
+{
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+/* E2M1 encode: round to nearest, ties to even, saturate at +-6; NaN -> 0
+ * (sign kept).  The grid has spacing 1/2 below 2, 1 in [2, 4) and 2 in
+ * [4, 6]; on each range the code is an offset plus the rounded multiple, and
+ * an even multiple is an even code. */
+uint8_t pko_e2m1_encode(float xf)
+{
+    double x = (double)xf;
+    uint8_t sign = signbit(x) ? 0x8 : 0x0;
+    double a = fabs(x);
+    if (isnan(x))
+        return sign;
+    if (a >= 6.0)
+        return (uint8_t)(sign | 0x7);
+    if (a < 2.0)
+        return (uint8_t)(sign | (uint8_t)round_half_even(2.0 * a));
+    if (a < 4.0)
+        return (uint8_t)(sign | (uint8_t)(round_half_even(a) + 2.0));
+    return (uint8_t)(sign | (uint8_t)(round_half_even(0.5 * a) + 4.0));
+}
+
+static float bf16_to_float(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* NVFP4 quantisation of one row of d bf16 values (d a multiple of 16) with
+ * the (block, KV head) scale: d/2 code bytes to `codes` (element 2j in the
+ * low nibble of byte j), d/16 E4M3 micro scales to `mscale`. */
+void pko_nvfp4_quantize_row(const uint16_t *x, int d, float scale, uint8_t *codes,
+                            uint8_t *mscale)
+{
+    for (int b = 0; b < d / 16; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < 16; ++i) {
+            float a = fabsf(bf16_to_float(x[16 * b + i]));
+            if (a > amax)                        /* NaN never compares greater */
+                amax = a;
+        }
+        volatile float six_s = 6.0f * scale;
+        volatile float ratio = amax / six_s;
+        uint8_t ms = pko_e4m3_encode(ratio);
+        mscale[b] = ms;
+        double msv = pko_e4m3_value(ms);
+        for (int i = 0; i < 16; i += 2) {
+            uint8_t c[2] = {0, 0};
+            if (msv != 0.0) {
+                volatile float step = scale * (float)msv;   /* msv is exact in fp32 */
+                for (int k = 0; k < 2; ++k) {
+                    volatile float qv = bf16_to_float(x[16 * b + i + k]) / step;
+                    c[k] = pko_e2m1_encode(qv);
+                }
+            }
+            codes[(16 * b + i) / 2] = (uint8_t)(c[0] | (c[1] << 4));
+        }
+    }
+}
+
 /* ---- KV append --------------------------------------------------------- */
 
 /*
  * For every new token t with slot_mapping[t] >= 0, copy its K and V rows of
  * every KV head into the pool at that slot.  bf16 pools receive the bits
- * unchanged; FP8 pools receive pko_e4m3_quantize(x, scale[block][head]).
+ * unchanged; FP8 pools receive pko_e4m3_quantize(x, scale[block][head]);
+ * NVFP4 pools (kv_fmt 2) the codes and micro scales of
+ * pko_nvfp4_quantize_row with that scale.
  * Returns PKO_BAD_ARG (and writes nothing further) on a slot past the pool.
  */
-int pko_write_slots(int kv_fp8, int64_t num_tokens, int hkv, int d, int bs,
+int pko_write_slots(int kv_fmt, int64_t num_tokens, int hkv, int d, int bs,
                     int64_t num_blocks, const uint16_t *k_new,
                     const uint16_t *v_new, const int64_t *slot_mapping,
                     void *k_cache, void *v_cache, const float *k_scale,
                     const float *v_scale)
 {
-    if (num_tokens < 0 || hkv <= 0 || d <= 0 || bs <= 0 || num_blocks < 0)
+    if (num_tokens < 0 || hkv <= 0 || d <= 0 || bs <= 0 || num_blocks < 0 ||
+        kv_fmt < 0 || kv_fmt > 2 || (kv_fmt == 2 && d % 16 != 0))
         return PKO_BAD_ARG;
     for (int64_t t = 0; t < num_tokens; ++t) {
         int64_t slot = slot_mapping[t];
@@ -202,7 +291,17 @@ int pko_write_slots(int kv_fp8, int64_t num_tokens, int hkv, int d, int bs,
             const uint16_t *ks = k_new + ((size_t)t * hkv + h) * d;
             const uint16_t *vs = v_new + ((size_t)t * hkv + h) * d;
             size_t row = ((size_t)blk * hkv + h) * bs + off;
-            if (!kv_fp8) {
+            if (kv_fmt == 2) {
+                size_t tile = ((size_t)blk * hkv + h) * (size_t)bs * (size_t)(d / 2 + d / 16);
+                size_t codes = tile + (size_t)off * (d / 2);
+                size_t msc = tile + (size_t)bs * (d / 2) + (size_t)off * (d / 16);
+                float sk = k_scale[(size_t)blk * hkv + h];
+                float sv = v_scale[(size_t)blk * hkv + h];
+                pko_nvfp4_quantize_row(ks, d, sk, (uint8_t *)k_cache + codes,
+                                       (uint8_t *)k_cache + msc);
+                pko_nvfp4_quantize_row(vs, d, sv, (uint8_t *)v_cache + codes,
+                                       (uint8_t *)v_cache + msc);
+            } else if (!kv_fmt) {
                 memcpy((uint16_t *)k_cache + row * d, ks, (size_t)d * 2);
                 memcpy((uint16_t *)v_cache + row * d, vs, (size_t)d * 2);
             } else {
@@ -223,7 +322,7 @@ int pko_write_slots(int kv_fp8, int64_t num_tokens, int hkv, int d, int bs,
 /* ---- attention ------------------------------------------------------------ */
 
 typedef struct {
-    int kv_fp8;
+    int kv_fmt;                 /* 0 bf16, 1 E4M3, 2 NVFP4 */
     const void *k_cache, *v_cache;
     const float *k_scale, *v_scale;
     int hkv, d, bs;
@@ -236,11 +335,21 @@ static double pool_elem(const pool_t *p, int is_v, const int32_t *bt,
                         int64_t j, int kvh, int i)
 {
     int64_t blk = bt[j / p->bs];
-    size_t row = ((size_t)blk * p->hkv + kvh) * p->bs + (size_t)(j % p->bs);
+    size_t off = (size_t)(j % p->bs);
+    size_t row = ((size_t)blk * p->hkv + kvh) * p->bs + off;
     const void *base = is_v ? p->v_cache : p->k_cache;
-    if (!p->kv_fp8)
+    if (!p->kv_fmt)
         return pko_bf16_value(((const uint16_t *)base)[row * p->d + i]);
     const float *sc = is_v ? p->v_scale : p->k_scale;
+    if (p->kv_fmt == 2) {
+        const uint8_t *tile = (const uint8_t *)base +
+            ((size_t)blk * p->hkv + kvh) * (size_t)p->bs * (size_t)(p->d / 2 + p->d / 16);
+        uint8_t byte = tile[off * (p->d / 2) + i / 2];
+        uint8_t code = (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+        uint8_t ms = tile[(size_t)p->bs * (p->d / 2) + off * (p->d / 16) + i / 16];
+        return pko_e2m1_value(code) * pko_e4m3_value(ms) *
+               (double)sc[(size_t)blk * p->hkv + kvh];
+    }
     return pko_e4m3_value(((const uint8_t *)base)[row * p->d + i]) *
            (double)sc[(size_t)blk * p->hkv + kvh];
 }
@@ -315,7 +424,7 @@ static int attend_one(const pool_t *p, const uint16_t *qrow, const int32_t *bt,
  * rows: indices (token * hq + head) to evaluate, or NULL for all T*hq rows in
  * order.  out receives nrows * d doubles, lse nrows doubles.
  */
-int pko_attention(int kv_fp8, const void *k_cache, const void *v_cache,
+int pko_attention(int kv_fmt, const void *k_cache, const void *v_cache,
                   const float *k_scale, const float *v_scale,
                   int64_t num_blocks, int hkv, int d, int bs, int hq,
                   const uint16_t *q, const int32_t *qsl,
@@ -327,7 +436,8 @@ int pko_attention(int kv_fp8, const void *k_cache, const void *v_cache,
                   double *lse)
 {
     if (hkv <= 0 || hq <= 0 || hq % hkv != 0 || d <= 0 || bs <= 0 ||
-        num_seqs < 0 || num_tokens < 0)
+        num_seqs < 0 || num_tokens < 0 || kv_fmt < 0 || kv_fmt > 2 ||
+        (kv_fmt == 2 && d % 16 != 0))
         return PKO_BAD_ARG;
     if (shard_n > 1 && (shard_r < 0 || shard_r >= shard_n || shard_k < 1))
         return PKO_BAD_ARG;
@@ -348,7 +458,7 @@ int pko_attention(int kv_fp8, const void *k_cache, const void *v_cache,
     }
     if (rows == NULL)
         nrows = num_tokens * hq;
-    pool_t p = {kv_fp8, k_cache, v_cache, k_scale, v_scale, hkv, d, bs,
+    pool_t p = {kv_fmt, k_cache, v_cache, k_scale, v_scale, hkv, d, bs,
                 num_blocks};
     int group = hq / hkv;
     int64_t max_len = 0;

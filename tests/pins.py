@@ -16,6 +16,7 @@ planted mistakes, each of which must fail at least one pin.
 """
 from __future__ import annotations
 
+import ctypes
 import math
 
 import numpy as np
@@ -499,8 +500,212 @@ def pin_fp8_attention(lib):
     np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
 
 
+# ---- NVFP4 ---------------------------------------------------------------------
+
+def e2m1_table() -> np.ndarray:
+    """The 16 E2M1 values of the golden fixture (the published format table)."""
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "e2m1_values.txt")
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                c, v = line.split("->")
+                vals[int(c)] = float(v)
+    assert sorted(vals) == list(range(16))
+    return np.array([vals[c] for c in range(16)])
+
+
+def _e2m1_nearest(x: float, table: np.ndarray) -> int:
+    """Brute force: the code whose value is nearest to x (saturating beyond
+    +-6), ties to the code with an even mantissa bit, zero keeps x's sign."""
+    if math.isnan(x):
+        return 0x8 if math.copysign(1.0, x) < 0 else 0x0
+    cands = range(8, 16) if math.copysign(1.0, x) < 0 else range(0, 8)
+    best = None
+    for c in cands:
+        dist = abs(x - table[c])
+        key = (dist, c & 1)
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1]
+
+
+def pin_e2m1_decode(lib):
+    """All 16 codes decode to the published E2M1 value table."""
+    table = e2m1_table()
+    for c in range(16):
+        got = lib.pko_e2m1_value(c)
+        assert got == table[c] and math.copysign(1.0, got) == math.copysign(1.0, table[c]), c
+
+
+def pin_e2m1_encode(lib):
+    """Encoding picks the nearest table value (brute force), ties to the even
+    code, saturating at +-6; every table value encodes to its own code."""
+    table = e2m1_table()
+    enc = lib.pko_e2m1_encode
+    for c in range(16):
+        assert enc(float(table[c])) == c, c
+    rng = np.random.default_rng(31)
+    mids = [(table[c] + table[c + 1]) / 2 for c in range(7)]
+    xs = np.concatenate([rng.uniform(-8, 8, 4000), rng.standard_normal(2000) * 2,
+                         mids, [-m for m in mids], [5.0, -5.0, 6.0, 7.0, 1e9, -1e9,
+                                                       0.25, 0.75, 2.5, 3.5]])
+    for x in xs.astype(np.float32):
+        assert enc(float(x)) == _e2m1_nearest(float(x), table), float(x)
+    # ties: 0.25 -> 0, 0.75 -> 1.0, 1.25 -> 1.0, 1.75 -> 2.0, 2.5 -> 2, 3.5 -> 4, 5 -> 4
+    assert [enc(v) for v in (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)] == [0, 2, 2, 4, 4, 6, 6]
+    assert enc(float("inf")) == 7 and enc(float("-inf")) == 15
+
+
+def _nvfp4_reference_row(x_bits: np.ndarray, scale: np.float32, table: np.ndarray):
+    """NVFP4 quantisation of one row with numpy fp32 arithmetic, torch's E4M3
+    cast for the micro scale and brute-force nearest E2M1 codes."""
+    d = x_bits.shape[0]
+    x = _f64(x_bits).astype(np.float32)
+    codes = np.zeros(d // 2, np.uint8)
+    ms = np.zeros(d // 16, np.uint8)
+    for b in range(d // 16):
+        blk = x[16 * b:16 * b + 16]
+        amax = np.float32(np.nanmax(np.abs(blk))) if not np.all(np.isnan(blk)) else np.float32(0)
+        ratio = np.float32(amax / np.float32(np.float32(6.0) * scale))
+        m = torch.tensor([min(float(ratio), 448.0)], dtype=torch.float32).to(
+            torch.float8_e4m3fn)
+        ms[b] = m.view(torch.uint8).item()
+        msv = m.to(torch.float32).item()
+        c = np.zeros(16, np.uint8)
+        if msv != 0.0:
+            step = np.float32(scale * np.float32(msv))
+            for i in range(16):
+                c[i] = _e2m1_nearest(float(np.float32(blk[i] / step)), table)
+        codes[8 * b:8 * b + 8] = c[0::2] | (c[1::2] << 4)
+    return codes, ms
+
+
+def pin_nvfp4_quantize(lib):
+    """NVFP4 row quantisation against an independent numpy/torch restatement
+    (fp32 products and quotients, library E4M3 cast of the micro scale,
+    brute-force nearest E2M1), on Gaussian rows, rows with outliers, rows
+    whose micro scale saturates or underflows to zero, and an all-zero row."""
+    table = e2m1_table()
+    rng = np.random.default_rng(32)
+    d = 128
+    rows = [(_bf16(rng, (d,)), np.float32(2.2 / 2688)),
+            (_bf16(rng, (d,), 40.0), np.float32(1e-3)),
+            (_bf16(rng, (d,)), np.float32(1e-6)),      # micro scales saturate at 448
+            (_bf16(rng, (d,), 1e-6), np.float32(1.0)),  # micro scales round to 0
+            (np.zeros(d, np.uint16), np.float32(0.01))]
+    spike = _bf16(rng, (d,))
+    spike[5] = _bf16(rng, (1,), 300.0)[0]
+    rows.append((spike, np.float32(0.004)))
+    for x, sc in rows:
+        codes, ms = _q(lib, x, sc)
+        rc, rm = _nvfp4_reference_row(x, sc, table)
+        assert np.array_equal(ms, rm)
+        assert np.array_equal(codes, rc)
+
+
+def _q(lib, x, sc):
+    d = x.shape[0]
+    codes = np.zeros(d // 2, np.uint8)
+    ms = np.zeros(d // 16, np.uint8)
+    lib.pko_nvfp4_quantize_row(np.ascontiguousarray(x, np.uint16), d, float(sc),
+                               codes.ctypes.data_as(ctypes.c_void_p),
+                               ms.ctypes.data_as(ctypes.c_void_p))
+    return codes, ms
+
+
+def nvfp4_dequant_tile(tile: np.ndarray, bs: int, d: int, scale: float) -> np.ndarray:
+    """[bs, d] values of one NVFP4 (block, KV head) tile: codes [bs][d/2]
+    then micro scales [bs][d/16]; element 2j in the low nibble of byte j."""
+    table = e2m1_table()
+    e4 = torch.from_numpy(np.arange(256, dtype=np.uint8)).view(
+        torch.float8_e4m3fn).to(torch.float64).numpy()
+    codes = tile[:bs * d // 2].reshape(bs, d // 2)
+    ms = tile[bs * d // 2:].reshape(bs, d // 16)
+    nib = np.empty((bs, d), np.uint8)
+    nib[:, 0::2] = codes & 0xF
+    nib[:, 1::2] = codes >> 4
+    return table[nib] * np.repeat(e4[ms], 16, axis=1) * float(scale)
+
+
+def pin_write_slots_nvfp4(lib):
+    """NVFP4 append writes each new row's codes and micro scales (the row
+    quantiser's output) at its slot inside the (block, KV head) tile and
+    leaves every other byte alone."""
+    rng = np.random.default_rng(33)
+    nb, hkv, bs, d = 4, 2, 16, 128
+    tile = bs * 9 * d // 16
+    kc = np.full((nb, hkv, tile), 0xA5, np.uint8)
+    vc = kc.copy()
+    ks = rng.uniform(0.0005, 0.002, (nb, hkv)).astype(np.float32)
+    vs = rng.uniform(0.0005, 0.002, (nb, hkv)).astype(np.float32)
+    T = 5
+    slots = rng.choice(nb * bs, size=T, replace=False).astype(np.int64)
+    slots[2] = -1
+    kn = _bf16(rng, (T, hkv, d))
+    vn = _bf16(rng, (T, hkv, d))
+    k0, v0 = kc.copy(), vc.copy()
+    oracle.write_slots(kc, vc, kn, vn, slots, k_scale=ks, v_scale=vs, lib=lib)
+    table = e2m1_table()
+    for cache, ref0, src, sc in ((kc, k0, kn, ks), (vc, v0, vn, vs)):
+        want = ref0.copy()
+        for t, s in enumerate(slots):
+            if s < 0:
+                continue
+            b, o = s // bs, s % bs
+            for h in range(hkv):
+                c, m = _nvfp4_reference_row(src[t, h], sc[b, h], table)
+                want[b, h, o * d // 2:(o + 1) * d // 2] = c
+                base = bs * d // 2
+                want[b, h, base + o * d // 16:base + (o + 1) * d // 16] = m
+        assert np.array_equal(cache, want)
+
+
+def pin_nvfp4_attention(lib):
+    """NVFP4 pools attend over e2m1(code) * e4m3(micro scale) * scale: same
+    result as fp64 SDPA over the tiles dequantised by the published E2M1
+    table and torch's E4M3 decode."""
+    rng = np.random.default_rng(34)
+    hq, hkv, d, bs = 4, 2, 32, 8
+    L, ql = 21, 3
+    nb = 5
+    tile = bs * 9 * d // 16
+    kc = rng.integers(0, 256, (nb, hkv, tile)).astype(np.uint8)
+    vc = rng.integers(0, 256, (nb, hkv, tile)).astype(np.uint8)
+    # micro scales: finite E4M3 codes between 2^-3 and 2^4
+    for c in (kc, vc):
+        c[:, :, bs * d // 2:] = rng.integers(0x20, 0x58, (nb, hkv, bs * d // 16))
+    ks = rng.uniform(0.05, 0.2, (nb, hkv)).astype(np.float32)
+    vs = rng.uniform(0.05, 0.2, (nb, hkv)).astype(np.float32)
+    bt = np.array([[3, 0, 4, np.iinfo(np.int32).max]], np.int32)
+    q = _bf16(rng, (ql, hq, d))
+    out, lse = oracle.attention(kc, vc, q, np.array([0, ql], np.int32),
+                                np.array([L], np.int32), bt, 0.25,
+                                k_scale=ks, v_scale=vs, lib=lib)
+    K = np.zeros((L, hkv, d))
+    V = np.zeros((L, hkv, d))
+    for p in range(L):
+        b = bt[0, p // bs]
+        for h in range(hkv):
+            K[p, h] = nvfp4_dequant_tile(kc[b, h], bs, d, ks[b, h])[p % bs]
+            V[p, h] = nvfp4_dequant_tile(vc[b, h], bs, d, vs[b, h])[p % bs]
+    qq = torch.from_numpy(_f64(q)).permute(1, 0, 2)
+    kk = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(2, 0)
+    vv = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(2, 0)
+    pos = torch.arange(ql)[:, None] + (L - ql)
+    mask = torch.arange(L)[None, :] <= pos
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qq[None], kk[None], vv[None], attn_mask=mask[None, None], scale=0.25)[0]
+    ref = ref.permute(1, 0, 2).reshape(-1, d).numpy()
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
 ALL_PINS = [pin_sdpa, pin_block_permutation, pin_chunked_prefill,
             pin_closed_forms, pin_gqa_is_repeated_mha, pin_lse_merge,
             pin_context_parallel_shards, pin_rope_is_a_complex_rotation, pin_bf16_round,
             pin_write_slots_bf16, pin_e4m3_decode, pin_e4m3_encode,
-            pin_write_slots_fp8, pin_fp8_attention]
+            pin_write_slots_fp8, pin_fp8_attention, pin_e2m1_decode, pin_e2m1_encode,
+            pin_nvfp4_quantize, pin_write_slots_nvfp4, pin_nvfp4_attention]

@@ -18,7 +18,8 @@ MUTATIONS = {
                              "int64_t hi = k_hi < pos ? k_hi : pos;"),
     "wrong_kv_head": ("head / group", "head % hkv"),
     "dropped_softmax_scale": ("        s *= softmax_scale;\n", ""),
-    "wrong_in_block_offset": ("(size_t)(j % p->bs)", "(size_t)((j + 1) % p->bs)"),
+    "wrong_in_block_offset": ("size_t off = (size_t)(j % p->bs);",
+                              "size_t off = (size_t)((j + 1) % p->bs);"),
     "wrong_block_entry": ("int64_t blk = bt[j / p->bs];",
                           "int64_t blk = bt[(j / p->bs) / 2 * 2];"),
     "lse_without_max": ("*lse = m + log(l);", "*lse = log(l);"),
@@ -46,6 +47,22 @@ MUTATIONS = {
                            "int b = neox ? (i + 1) % half + half : 2 * i + 1;"),
     "bf16_ties_up": ("double k = fr > 0.5 ? fl + 1.0 : fr < 0.5 ? fl : (fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0);",
                      "double k = fr >= 0.5 ? fl + 1.0 : fl;"),
+    "e2m1_subnormal_doubled": ("double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);",
+                               "double v = e == 0 ? 1.0 * m : ldexp(1.0 + 0.5 * m, e - 1);"),
+    "e2m1_exponent_bias": ("double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);",
+                           "double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 2);"),
+    "e2m1_top_range_step": ("return (uint8_t)(sign | (uint8_t)(round_half_even(0.5 * a) + 4.0));",
+                            "return (uint8_t)(sign | (uint8_t)(floor(0.5 * a) + 4.0));"),
+    "nvfp4_nibbles_swapped": ("uint8_t code = (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);",
+                              "uint8_t code = (i & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);"),
+    "nvfp4_micro_scale_dropped": ("return pko_e2m1_value(code) * pko_e4m3_value(ms) *",
+                                  "return pko_e2m1_value(code) * 1.0 *"),
+    "nvfp4_wrong_micro_block": ("off * (p->d / 16) + i / 16];",
+                                "off * (p->d / 16) + (i / 16 + 1) % (p->d / 16)];"),
+    "nvfp4_amax_without_six": ("volatile float six_s = 6.0f * scale;",
+                               "volatile float six_s = scale;"),
+    "nvfp4_step_without_tile_scale": ("volatile float step = scale * (float)msv;",
+                                      "volatile float step = (float)msv;"),
     "v_append_from_k": ("const uint16_t *vs = v_new + ((size_t)t * hkv + h) * d;",
                         "const uint16_t *vs = k_new + ((size_t)t * hkv + h) * d;"),
 }
