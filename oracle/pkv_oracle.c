@@ -61,8 +61,10 @@
  *
  * Pool layout: [num_blocks][num_kv_heads][block_size][head_dim], so slot s of
  * KV head h is row ((s / bs) * Hkv + h) * bs + s % bs.  NVFP4 pools hold,
- * per (block, KV head), block_size rows of head_dim / 2 code bytes followed
- * by block_size rows of head_dim / 16 micro-scale bytes.
+ * per (block, KV head), the block's rows in groups of min(block_size, 64)
+ * rows (block_size <= 64 or a multiple of 64): a group is its rows' code
+ * bytes (head_dim / 2 per row) followed by their micro-scale bytes
+ * (head_dim / 16 per row).
  */
 #include <math.h>
 #include <stdint.h>
@@ -260,6 +262,17 @@ void pko_nvfp4_quantize_row(const uint16_t *x, int d, float scale, uint8_t *code
     }
 }
 
+/* Byte offsets, inside its (block, KV head) tile, of the codes and of the
+ * micro scales of row `off` of an NVFP4 pool (groups of min(bs, 64) rows). */
+static void nvfp4_offsets(int bs, int d, int64_t off, size_t *codes, size_t *mscale)
+{
+    int64_t gs = bs < 64 ? bs : 64;
+    size_t group = (size_t)(off / gs) * (size_t)gs * (size_t)(d / 2 + d / 16);
+    int64_t r = off % gs;
+    *codes = group + (size_t)r * (d / 2);
+    *mscale = group + (size_t)gs * (d / 2) + (size_t)r * (d / 16);
+}
+
 /* ---- KV append --------------------------------------------------------- */
 
 /*
@@ -277,7 +290,8 @@ int pko_write_slots(int kv_fmt, int64_t num_tokens, int hkv, int d, int bs,
                     const float *v_scale)
 {
     if (num_tokens < 0 || hkv <= 0 || d <= 0 || bs <= 0 || num_blocks < 0 ||
-        kv_fmt < 0 || kv_fmt > 2 || (kv_fmt == 2 && d % 16 != 0))
+        kv_fmt < 0 || kv_fmt > 2 ||
+        (kv_fmt == 2 && (d % 16 != 0 || (bs > 64 && bs % 64 != 0))))
         return PKO_BAD_ARG;
     for (int64_t t = 0; t < num_tokens; ++t) {
         int64_t slot = slot_mapping[t];
@@ -293,8 +307,10 @@ int pko_write_slots(int kv_fmt, int64_t num_tokens, int hkv, int d, int bs,
             size_t row = ((size_t)blk * hkv + h) * bs + off;
             if (kv_fmt == 2) {
                 size_t tile = ((size_t)blk * hkv + h) * (size_t)bs * (size_t)(d / 2 + d / 16);
-                size_t codes = tile + (size_t)off * (d / 2);
-                size_t msc = tile + (size_t)bs * (d / 2) + (size_t)off * (d / 16);
+                size_t codes, msc;
+                nvfp4_offsets(bs, d, off, &codes, &msc);
+                codes += tile;
+                msc += tile;
                 float sk = k_scale[(size_t)blk * hkv + h];
                 float sv = v_scale[(size_t)blk * hkv + h];
                 pko_nvfp4_quantize_row(ks, d, sk, (uint8_t *)k_cache + codes,
@@ -344,9 +360,11 @@ static double pool_elem(const pool_t *p, int is_v, const int32_t *bt,
     if (p->kv_fmt == 2) {
         const uint8_t *tile = (const uint8_t *)base +
             ((size_t)blk * p->hkv + kvh) * (size_t)p->bs * (size_t)(p->d / 2 + p->d / 16);
-        uint8_t byte = tile[off * (p->d / 2) + i / 2];
+        size_t co, mo;
+        nvfp4_offsets(p->bs, p->d, (int64_t)off, &co, &mo);
+        uint8_t byte = tile[co + i / 2];
         uint8_t code = (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
-        uint8_t ms = tile[(size_t)p->bs * (p->d / 2) + off * (p->d / 16) + i / 16];
+        uint8_t ms = tile[mo + i / 16];
         return pko_e2m1_value(code) * pko_e4m3_value(ms) *
                (double)sc[(size_t)blk * p->hkv + kvh];
     }
@@ -437,7 +455,7 @@ int pko_attention(int kv_fmt, const void *k_cache, const void *v_cache,
 {
     if (hkv <= 0 || hq <= 0 || hq % hkv != 0 || d <= 0 || bs <= 0 ||
         num_seqs < 0 || num_tokens < 0 || kv_fmt < 0 || kv_fmt > 2 ||
-        (kv_fmt == 2 && d % 16 != 0))
+        (kv_fmt == 2 && (d % 16 != 0 || (bs > 64 && bs % 64 != 0))))
         return PKO_BAD_ARG;
     if (shard_n > 1 && (shard_r < 0 || shard_r >= shard_n || shard_k < 1))
         return PKO_BAD_ARG;

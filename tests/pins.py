@@ -617,14 +617,26 @@ def _q(lib, x, sc):
     return codes, ms
 
 
+def nvfp4_split_tile(tile: np.ndarray, bs: int, d: int):
+    """(codes [bs, d/2], micro scales [bs, d/16]) of one NVFP4 (block, KV
+    head) tile: groups of min(bs, 64) rows, each its codes then its scales."""
+    gs = min(bs, 64)
+    per = gs * 9 * d // 16
+    codes, ms = [], []
+    for g0 in range(0, bs, gs):
+        grp = tile[(g0 // gs) * per:(g0 // gs + 1) * per]
+        codes.append(grp[:gs * d // 2].reshape(gs, d // 2))
+        ms.append(grp[gs * d // 2:].reshape(gs, d // 16))
+    return np.concatenate(codes), np.concatenate(ms)
+
+
 def nvfp4_dequant_tile(tile: np.ndarray, bs: int, d: int, scale: float) -> np.ndarray:
-    """[bs, d] values of one NVFP4 (block, KV head) tile: codes [bs][d/2]
-    then micro scales [bs][d/16]; element 2j in the low nibble of byte j."""
+    """[bs, d] values of one NVFP4 (block, KV head) tile; element 2j of a row
+    is the low nibble of its code byte j."""
     table = e2m1_table()
     e4 = torch.from_numpy(np.arange(256, dtype=np.uint8)).view(
         torch.float8_e4m3fn).to(torch.float64).numpy()
-    codes = tile[:bs * d // 2].reshape(bs, d // 2)
-    ms = tile[bs * d // 2:].reshape(bs, d // 16)
+    codes, ms = nvfp4_split_tile(tile, bs, d)
     nib = np.empty((bs, d), np.uint8)
     nib[:, 0::2] = codes & 0xF
     nib[:, 1::2] = codes >> 4
@@ -635,8 +647,13 @@ def pin_write_slots_nvfp4(lib):
     """NVFP4 append writes each new row's codes and micro scales (the row
     quantiser's output) at its slot inside the (block, KV head) tile and
     leaves every other byte alone."""
-    rng = np.random.default_rng(33)
-    nb, hkv, bs, d = 4, 2, 16, 128
+    for bs in (16, 128):
+        _write_slots_nvfp4_case(lib, bs)
+
+
+def _write_slots_nvfp4_case(lib, bs):
+    rng = np.random.default_rng(33 + bs)
+    nb, hkv, d = 4, 2, 128
     tile = bs * 9 * d // 16
     kc = np.full((nb, hkv, tile), 0xA5, np.uint8)
     vc = kc.copy()
@@ -656,11 +673,14 @@ def pin_write_slots_nvfp4(lib):
             if s < 0:
                 continue
             b, o = s // bs, s % bs
+            gs = min(bs, 64)
+            base = (o // gs) * gs * 9 * d // 16
+            r = o % gs
             for h in range(hkv):
                 c, m = _nvfp4_reference_row(src[t, h], sc[b, h], table)
-                want[b, h, o * d // 2:(o + 1) * d // 2] = c
-                base = bs * d // 2
-                want[b, h, base + o * d // 16:base + (o + 1) * d // 16] = m
+                want[b, h, base + r * d // 2:base + (r + 1) * d // 2] = c
+                mb = base + gs * d // 2
+                want[b, h, mb + r * d // 16:mb + (r + 1) * d // 16] = m
         assert np.array_equal(cache, want)
 
 
@@ -668,16 +688,25 @@ def pin_nvfp4_attention(lib):
     """NVFP4 pools attend over e2m1(code) * e4m3(micro scale) * scale: same
     result as fp64 SDPA over the tiles dequantised by the published E2M1
     table and torch's E4M3 decode."""
-    rng = np.random.default_rng(34)
-    hq, hkv, d, bs = 4, 2, 32, 8
-    L, ql = 21, 3
+    for bs, L in ((8, 21), (128, 300)):
+        _nvfp4_attention_case(lib, bs, L)
+
+
+def _nvfp4_attention_case(lib, bs, L):
+    rng = np.random.default_rng(34 + bs)
+    hq, hkv, d = 4, 2, 32
+    ql = 3
     nb = 5
     tile = bs * 9 * d // 16
     kc = rng.integers(0, 256, (nb, hkv, tile)).astype(np.uint8)
     vc = rng.integers(0, 256, (nb, hkv, tile)).astype(np.uint8)
     # micro scales: finite E4M3 codes between 2^-3 and 2^4
+    gs = min(bs, 64)
+    per = gs * 9 * d // 16
     for c in (kc, vc):
-        c[:, :, bs * d // 2:] = rng.integers(0x20, 0x58, (nb, hkv, bs * d // 16))
+        for g0 in range(0, bs, gs):
+            base = (g0 // gs) * per + gs * d // 2
+            c[:, :, base:base + gs * d // 16] = rng.integers(0x20, 0x58, (nb, hkv, gs * d // 16))
     ks = rng.uniform(0.05, 0.2, (nb, hkv)).astype(np.float32)
     vs = rng.uniform(0.05, 0.2, (nb, hkv)).astype(np.float32)
     bt = np.array([[3, 0, 4, np.iinfo(np.int32).max]], np.int32)

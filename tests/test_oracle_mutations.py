@@ -57,8 +57,9 @@ MUTATIONS = {
                               "uint8_t code = (i & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);"),
     "nvfp4_micro_scale_dropped": ("return pko_e2m1_value(code) * pko_e4m3_value(ms) *",
                                   "return pko_e2m1_value(code) * 1.0 *"),
-    "nvfp4_wrong_micro_block": ("off * (p->d / 16) + i / 16];",
-                                "off * (p->d / 16) + (i / 16 + 1) % (p->d / 16)];"),
+    "nvfp4_wrong_micro_block": ("uint8_t ms = tile[mo + i / 16];",
+                                "uint8_t ms = tile[mo + (i / 16 + 1) % (p->d / 16)];"),
+    "nvfp4_groups_ignored": ("int64_t gs = bs < 64 ? bs : 64;", "int64_t gs = bs;"),
     "nvfp4_amax_without_six": ("volatile float six_s = 6.0f * scale;",
                                "volatile float six_s = scale;"),
     "nvfp4_step_without_tile_scale": ("volatile float step = scale * (float)msv;",
