@@ -26,6 +26,14 @@
  *  - A KV pool is [num_blocks][Hkv][block_size][128] elements: bf16, or E4M3
  *    codes (OCP FP8, "FN" variant) with one fp32 scale per (block, KV head)
  *    in a [num_blocks][Hkv] array; an element's value is e4m3(code) * scale.
+ *    NVFP4 pools (the compressed KV format of page "vLLM 优化
+ *    DeepSeek-V4.1-Flash：智能体吞吐提升 5 倍", section Kernels) are
+ *    [num_blocks][Hkv][block_size * 72] bytes: per (block, KV head), rows in
+ *    groups of min(block_size, 64); a group is its rows' 64 code bytes each
+ *    (OCP FP4 E2M1, element 2j in the low nibble of byte j) followed by their
+ *    8 micro-scale bytes each (E4M3, one per 16 elements); with the fp32
+ *    (block, KV head) scale an element's value is e2m1(code) * e4m3(micro
+ *    scale) * scale.  NVFP4 scales must be at most 16.
  *    Logical position p of request i lives in block block_tables[i][p / bs]
  *    at row p % bs; its slot is block * bs + p % bs.
  *  - Query token t (0-based) of request i, which has q_i new tokens and
@@ -72,7 +80,8 @@ typedef enum {
 
 typedef enum {
     PKV_KV_BF16 = 0,
-    PKV_KV_FP8_E4M3 = 1
+    PKV_KV_FP8_E4M3 = 1,
+    PKV_KV_NVFP4 = 2
 } pkv_kv_dtype;
 
 enum {
@@ -114,6 +123,11 @@ pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out);
  * one correctly rounded fp32 division, then rounded to nearest even and
  * saturated to +-448; k_scale / v_scale ([num_blocks][Hkv] fp32, device) are
  * read, never written, and must be finite and > 0 for the blocks written.
+ * NVFP4 pools receive, per 16 elements, the micro scale E4M3(amax / (6 *
+ * scale)) (amax the largest |x| of the 16; fp32 product and quotient) and,
+ * unless it is zero (then all codes are 0), the codes E2M1(x / (scale *
+ * micro scale)) (fp32 product and quotient; nearest, ties to even,
+ * saturating at +-6).
  * slot_mapping is int64 on the device; negative entries are padding.
  * Entries must be distinct.  A slot past the pool is an argument error the
  * host cannot see: in validate mode it is skipped and reported, otherwise it
@@ -203,7 +217,8 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q,
  * decode rows only (q_i * G <= 8; a request with more rows returns
  * PKV_ERR_UNSUPPORTED).  Arguments as for pkv_attention_varlen, except:
  *  interleave  tokens per run, a positive multiple of the decode stage (16
- *              keys for bf16 pools, 32 for E4M3; the pages' default of 1 is
+ *              keys for bf16 pools, 32 for E4M3, 64 for NVFP4; the pages'
+ *              default of 1 is
  *              not supported on the GPU and returns PKV_ERR_UNSUPPORTED);
  *  out         [num_tokens][Hq][128] fp32, device: the shard's softmax-
  *              normalised partial output (0 where the shard owns no visible
@@ -368,7 +383,8 @@ pkv_status pkv_timing_read(pkv_handle *h, int32_t kind, int32_t *launches,
  *    different streams, or from different threads) race on it: serialise
  *    them.
  *  - Returns PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED (prefill rows,
- *    head_dim or block_size not handled), PKV_ERR_WORKSPACE or PKV_ERR_CUDA.
+ *    NVFP4 pools, head_dim or block_size not handled), PKV_ERR_WORKSPACE or
+ *    PKV_ERR_CUDA.
  *    It does not update pkv_last_error() and performs no device-side
  *    validation.
  */

@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                 3: "PKV_ERR_CUDA", 4: "PKV_ERR_OUT_OF_MEMORY",
                 5: "PKV_ERR_DEVICE_CHECK", 6: "PKV_ERR_TIMEOUT",
                 7: "PKV_ERR_WORKSPACE"}
-KV_BF16, KV_FP8_E4M3 = 0, 1
+KV_BF16, KV_FP8_E4M3, KV_NVFP4 = 0, 1, 2
 FLAG_VALIDATE, FLAG_TIMING, FLAG_SEPARATE = 1, 2, 4
 KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL, KERNEL_MIXED = 0, 1, 2, 3
 

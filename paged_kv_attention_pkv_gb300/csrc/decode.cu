@@ -21,7 +21,7 @@
 // head-dim column with byte permutes and converted exactly to f16 in
 // hardware, PV runs in f16 with V's per-block scale folded into P.  K's
 // per-block scale is folded into the fp32 scores.
-#include "decode_body.cuh"
+#include "decode_nvfp4.cuh"
 
 namespace pkv {
 namespace {
@@ -37,13 +37,26 @@ __global__ void __launch_bounds__(kDecWarps * 32, FP8 ? 3 : 2)
   decode_item<FP8, kDecWarps>(kmap, vmap, p, p.items[blockIdx.x], smem, threadIdx.x, 0);
 }
 
+__global__ void __launch_bounds__(kDecWarps * 32, 3)
+    decode_nvfp4_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap,
+                        const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  decode_item_nvfp4<kDecWarps>(kmap, vmap, p, p.items[blockIdx.x], smem, threadIdx.x, 0);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          const DecodeParams &p, int num_items, bool fp8,
+                          const DecodeParams &p, int num_items, int kv_dtype,
                           cudaStream_t s) {
   if (num_items == 0) return cudaSuccess;
-  if (fp8)
+  const bool fp8 = kv_dtype == PKV_KV_FP8_E4M3;
+  if (kv_dtype == PKV_KV_NVFP4)
+    decode_nvfp4_kernel<<<num_items, kDecWarps * 32, kDecSmemBytesNvfp4, s>>>(kmap, vmap, p);
+  else if (fp8)
     decode_kernel<true><<<num_items, kDecWarps * 32, kDecSmemBytesFp8, s>>>(kmap, vmap, p);
   else
     decode_kernel<false><<<num_items, kDecWarps * 32, kDecSmemBytes, s>>>(kmap, vmap, p);
@@ -51,7 +64,11 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
 }
 
 cudaError_t configure_decode() {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<true>,
+  cudaError_t e = cudaFuncSetAttribute(decode_nvfp4_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kDecSmemBytesNvfp4);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_kernel<true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kDecSmemBytesFp8);
   if (e != cudaSuccess) return e;

@@ -48,6 +48,113 @@ __device__ __forceinline__ int fp8_dmap(int mt, int dr) {
   return 4 * ((dr & 7) + 8 * (mt >> 1)) + 2 * (mt & 1) + (dr >> 3);
 }
 
+// End of a decode item, shared by the storage formats: merge the NW warps'
+// (max, sum, O) through shared memory, normalise, and write the rows (or
+// this range's partial, the last range to finish then merging all ranges).
+// `dmap(mt, dr)` is the head-dim index of row dr of m-tile mt of the O^T
+// accumulator; `acc_scale` undoes a power-of-two factor carried in acc.
+template <int NW, typename DMap>
+__device__ __forceinline__ void decode_finish(const DecodeParams &p, const pkv_work_item &it,
+                                              uint8_t *smem, int32_t *flag, const int tid,
+                                              const int bar, float m0, float m1, float l0,
+                                              float l1, const float (&acc)[8][4],
+                                              const float acc_scale, DMap dmap) {
+  constexpr int kDecWarps = NW;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  const int group = p.group;
+  auto sync = [&]() { named_barrier(bar, NW * 32); };
+  // ---- per-warp row sums, then merge the 4 warps through shared memory
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+  sync();  // rings are free now
+  float *red_o = reinterpret_cast<float *>(smem);           // [NW][8][128]
+  float *red_m = red_o + kDecWarps * kDecCols * kHeadDim;   // [NW][8]
+  float *red_l = red_m + kDecWarps * kDecCols;              // [NW][8]
+  if (g == 0) {
+    red_m[warp * kDecCols + 2 * t] = m0;
+    red_m[warp * kDecCols + 2 * t + 1] = m1;
+    red_l[warp * kDecCols + 2 * t] = l0;
+    red_l[warp * kDecCols + 2 * t + 1] = l1;
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int n = 2 * t + (c & 1);
+      const int dr = g + 8 * (c >> 1);
+      red_o[(warp * kDecCols + n) * kHeadDim + dmap(mt, dr)] = acc[mt][c] * acc_scale;
+    }
+  }
+  sync();
+
+  // one head-dim element per thread; NW/4 groups of 128 threads split the rows
+  const int d = tid & 127;
+  const int n_first = tid >> 7, n_step = NW / 4;
+  auto write_row = [&](int n, float o, float lse2) {
+    const int r = it.row0 + n;
+    const int64_t row = static_cast<int64_t>(it.tok0 + r / group) * p.hq +
+                        it.kv_head * group + r % group;
+    if (p.out_f32 != nullptr)
+      p.out_f32[row * kHeadDim + d] = o;
+    else
+      p.out[row * kHeadDim + d] = __float2bfloat16_rn(o);
+    if (d == 0 && p.lse != nullptr) p.lse[row] = lse2 * kLn2;
+  };
+  for (int n = n_first; n < it.n_rows; n += n_step) {
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red_m[w * kDecCols + n]);
+    const float Mu = M == -CUDART_INF_F ? 0.f : M;
+    float Ls = 0.f, o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) {
+      const float sw = exp2f(red_m[w * kDecCols + n] - Mu);
+      Ls += red_l[w * kDecCols + n] * sw;
+      o += red_o[(w * kDecCols + n) * kHeadDim + d] * sw;
+    }
+    const float lse2 = Ls > 0.f ? Mu + log2f(Ls) : -CUDART_INF_F;
+    o = Ls > 0.f ? o / Ls : 0.f;
+    if (it.part < 0) {
+      write_row(n, o, lse2);
+    } else {
+      p.part_o[(static_cast<int64_t>(it.part) * kDecCols + n) * kHeadDim + d] = o;
+      if (d == 0) p.part_lse[static_cast<int64_t>(it.part) * kDecCols + n] = lse2;
+    }
+  }
+  if (it.part < 0) return;
+
+  // ---- last range of this (request, KV head) to finish merges all ranges
+  __threadfence();
+  sync();
+  if (tid == 0) {
+    const int prev = atomicAdd(p.tickets + it.pair, 1);
+    *flag = (prev == it.n_split - 1);
+  }
+  sync();
+  if (*flag == 0) return;
+  __threadfence();
+  for (int n = n_first; n < it.n_rows; n += n_step) {
+    float M = -CUDART_INF_F;
+    for (int s2 = 0; s2 < it.n_split; ++s2)
+      M = fmaxf(M, __ldcg(p.part_lse + static_cast<int64_t>(it.pair + s2) * kDecCols + n));
+    const float Mu = M == -CUDART_INF_F ? 0.f : M;
+    float Ls = 0.f, o = 0.f;
+    for (int s2 = 0; s2 < it.n_split; ++s2) {
+      const int64_t slot = it.pair + s2;
+      const float w = exp2f(__ldcg(p.part_lse + slot * kDecCols + n) - Mu);
+      Ls += w;
+      o += w * __ldcg(p.part_o + (slot * kDecCols + n) * kHeadDim + d);
+    }
+    write_row(n, Ls > 0.f ? o / Ls : 0.f, Ls > 0.f ? Mu + log2f(Ls) : -CUDART_INF_F);
+  }
+  if (tid == 0) p.tickets[it.pair] = 0;  // ready for the next step
+}
+
 // One decode work item processed by NW warps (threads tid = 0 .. 32 NW - 1
 // of the CTA); `smem` is 1024-byte aligned and holds NW rings plus their
 // mbarriers; `bar` is the named barrier these warps synchronise on.
@@ -386,95 +493,8 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       mbar_wait(&full[i % kDecStages], (i / kDecStages) & 1);
   }
 
-  // ---- per-warp row sums, then merge the 4 warps through shared memory
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-  }
-  sync();  // rings are free now
-  float *red_o = reinterpret_cast<float *>(smem);           // [NW][8][128]
-  float *red_m = red_o + kDecWarps * kDecCols * kHeadDim;   // [NW][8]
-  float *red_l = red_m + kDecWarps * kDecCols;              // [NW][8]
-  if (g == 0) {
-    red_m[warp * kDecCols + 2 * t] = m0;
-    red_m[warp * kDecCols + 2 * t + 1] = m1;
-    red_l[warp * kDecCols + 2 * t] = l0;
-    red_l[warp * kDecCols + 2 * t + 1] = l1;
-  }
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int n = 2 * t + (c & 1);
-      const int dr = g + 8 * (c >> 1);
-      const int d = FP8 ? fp8_dmap(mt, dr) : 16 * mt + dr;
-      red_o[(warp * kDecCols + n) * kHeadDim + d] = acc[mt][c];
-    }
-  }
-  sync();
-
-  // one head-dim element per thread; NW/4 groups of 128 threads split the rows
-  const int d = tid & 127;
-  const int n_first = tid >> 7, n_step = NW / 4;
-  auto write_row = [&](int n, float o, float lse2) {
-    const int r = it.row0 + n;
-    const int64_t row = static_cast<int64_t>(it.tok0 + r / group) * p.hq +
-                        it.kv_head * group + r % group;
-    if (p.out_f32 != nullptr)
-      p.out_f32[row * kHeadDim + d] = o;
-    else
-      p.out[row * kHeadDim + d] = __float2bfloat16_rn(o);
-    if (d == 0 && p.lse != nullptr) p.lse[row] = lse2 * kLn2;
-  };
-  for (int n = n_first; n < it.n_rows; n += n_step) {
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red_m[w * kDecCols + n]);
-    const float Mu = M == -CUDART_INF_F ? 0.f : M;
-    float Ls = 0.f, o = 0.f;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) {
-      const float sw = exp2f(red_m[w * kDecCols + n] - Mu);
-      Ls += red_l[w * kDecCols + n] * sw;
-      o += red_o[(w * kDecCols + n) * kHeadDim + d] * sw;
-    }
-    const float lse2 = Ls > 0.f ? Mu + log2f(Ls) : -CUDART_INF_F;
-    o = Ls > 0.f ? o / Ls : 0.f;
-    if (it.part < 0) {
-      write_row(n, o, lse2);
-    } else {
-      p.part_o[(static_cast<int64_t>(it.part) * kDecCols + n) * kHeadDim + d] = o;
-      if (d == 0) p.part_lse[static_cast<int64_t>(it.part) * kDecCols + n] = lse2;
-    }
-  }
-  if (it.part < 0) return;
-
-  // ---- last range of this (request, KV head) to finish merges all ranges
-  __threadfence();
-  sync();
-  if (tid == 0) {
-    const int prev = atomicAdd(p.tickets + it.pair, 1);
-    *flag = (prev == it.n_split - 1);
-  }
-  sync();
-  if (*flag == 0) return;
-  __threadfence();
-  for (int n = n_first; n < it.n_rows; n += n_step) {
-    float M = -CUDART_INF_F;
-    for (int s2 = 0; s2 < it.n_split; ++s2)
-      M = fmaxf(M, __ldcg(p.part_lse + static_cast<int64_t>(it.pair + s2) * kDecCols + n));
-    const float Mu = M == -CUDART_INF_F ? 0.f : M;
-    float Ls = 0.f, o = 0.f;
-    for (int s2 = 0; s2 < it.n_split; ++s2) {
-      const int64_t slot = it.pair + s2;
-      const float w = exp2f(__ldcg(p.part_lse + slot * kDecCols + n) - Mu);
-      Ls += w;
-      o += w * __ldcg(p.part_o + (slot * kDecCols + n) * kHeadDim + d);
-    }
-    write_row(n, Ls > 0.f ? o / Ls : 0.f, Ls > 0.f ? Mu + log2f(Ls) : -CUDART_INF_F);
-  }
-  if (tid == 0) p.tickets[it.pair] = 0;  // ready for the next step
+  decode_finish<NW>(p, it, smem, flag, tid, bar, m0, m1, l0, l1, acc, 1.f,
+                    [](int mt, int dr) { return FP8 ? fp8_dmap(mt, dr) : 16 * mt + dr; });
 }
 
 

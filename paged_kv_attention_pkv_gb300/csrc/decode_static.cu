@@ -114,6 +114,7 @@ extern "C" pkv_status pkv_decode_static(
   if (!q || !k_cache || !v_cache || !block_tables || !qsl || !lens || !out)
     return PKV_ERR_INVALID_ARG;
   const bool fp8 = c->kv_dtype == PKV_KV_FP8_E4M3;
+  if (c->kv_dtype == PKV_KV_NVFP4) return PKV_ERR_UNSUPPORTED;
   if (c->kv_dtype != PKV_KV_BF16 && !fp8) return PKV_ERR_INVALID_ARG;
   if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
   const int G = c->num_q_heads / c->num_kv_heads;
@@ -222,5 +223,6 @@ extern "C" pkv_status pkv_decode_static(
   p.num_blocks = c->num_blocks;
   p.scale_log2 = c->softmax_scale * 1.4426950408889634f;
   p.validate = 0;
-  return launch_decode(kmap, vmap, p, n, fp8, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return launch_decode(kmap, vmap, p, n, c->kv_dtype, s) == cudaSuccess ? PKV_OK
+                                                                         : PKV_ERR_CUDA;
 }

@@ -40,6 +40,105 @@ __device__ __forceinline__ uint2 quantize8(uint4 v, float scale) {
   return make_uint2(out[0], out[1]);
 }
 
+// ---- NVFP4 -------------------------------------------------------------------
+// E2M1 code of an fp32 value: nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6 by its
+// magnitude, ties to the even code, saturating at 6; the sign bit is copied
+// (NaN gives 0).  Each comparison adds one step of the grid; the midpoints
+// that are ties use > when the lower code is even and >= when it is odd.
+__device__ __forceinline__ uint32_t e2m1_code(float q) {
+  const float a = fabsf(q);
+  const uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) +
+                     (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+  return c | ((__float_as_uint(q) >> 28) & 8u);
+}
+
+// Value of an E4M3 code (exact).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  return e4m3x2_to_f32(code & 0xFFu).x;
+}
+
+// Micro scale of 16 values with largest magnitude amax under the (block, KV
+// head) scale: E4M3(amax / (6 scale)), product and quotient in fp32.
+__device__ __forceinline__ uint32_t nvfp4_micro_scale(float amax, float scale) {
+  return e4m3x2_from_f32(__fdiv_rn(amax, __fmul_rn(6.f, scale)), 0.f) & 0xFFu;
+}
+
+// Codes of 8 values (element 2j in the low nibble of byte j) for the
+// quantisation step `step` = scale * micro scale (0: all codes 0).
+__device__ __forceinline__ uint32_t nvfp4_codes8(const float (&x)[8], float step) {
+  uint32_t w = 0;
+  if (step != 0.f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w |= e2m1_code(__fdiv_rn(x[i], step)) << (4 * i);
+  }
+  return w;
+}
+
+// One micro block (16 bf16 values, two uint4) -> 8 code bytes; *ms gets its
+// micro-scale code.
+__device__ __forceinline__ uint2 nvfp4_quantize16(uint4 a, uint4 b, float scale, uint32_t *ms) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float x[2][8];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[i >> 2][2 * (i & 3)] = bf16_lo(w[i]);
+    x[i >> 2][2 * (i & 3) + 1] = bf16_hi(w[i]);
+    amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  }
+  *ms = nvfp4_micro_scale(amax, scale);
+  const float step = __fmul_rn(scale, e4m3_value(*ms));
+  return make_uint2(nvfp4_codes8(x[0], step), nvfp4_codes8(x[1], step));
+}
+
+// Byte offsets inside a (block, KV head) tile of row `off`'s codes and micro
+// scales: rows in groups of min(bs, 64), each group its codes then scales.
+__device__ __forceinline__ void nvfp4_row_offsets(int bs, int64_t off, int64_t *codes,
+                                                  int64_t *mscale) {
+  const int gs = bs < kNvfp4Group ? bs : kNvfp4Group;
+  const int64_t group = (off / gs) * gs * kNvfp4RowBytes;
+  const int64_t r = off % gs;
+  *codes = group + r * (kHeadDim / 2);
+  *mscale = group + gs * (kHeadDim / 2) + r * (kHeadDim / 16);
+}
+
+// NVFP4 append: one thread per micro block (16 elements) of a (token, KV
+// head) row of K and of V; 8 threads cover a row.
+__global__ void __launch_bounds__(256) kv_append_nvfp4_kernel(AppendParams p) {
+  constexpr int kBlocks = kHeadDim / 16;
+  const int64_t total = p.num_tokens * p.hkv * kBlocks;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       i < total; i += stride) {
+    const int64_t row = i / kBlocks;  // token * hkv + head
+    const int b = static_cast<int>(i % kBlocks);
+    const int64_t t = row / p.hkv;
+    const int h = static_cast<int>(row % p.hkv);
+    const int64_t slot = p.slots[t];
+    if (slot < 0) continue;
+    const int64_t blk = slot / p.bs;
+    if (blk >= p.num_blocks) {
+      record_error(p.err, kErrBadSlot);
+      continue;
+    }
+    const int64_t tile = (blk * p.hkv + h) * p.bs * kNvfp4RowBytes;
+    int64_t co, mo;
+    nvfp4_row_offsets(p.bs, slot % p.bs, &co, &mo);
+    const size_t si = static_cast<size_t>(blk) * p.hkv + h;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(kv ? p.v_new : p.k_new) +
+                         row * (kHeadDim / 8) + 2 * b;
+      uint32_t ms;
+      const uint2 c = nvfp4_quantize16(__ldg(src), __ldg(src + 1),
+                                       __ldg((kv ? p.v_scale : p.k_scale) + si), &ms);
+      uint8_t *pool = static_cast<uint8_t *>(kv ? p.v_cache : p.k_cache) + tile;
+      *reinterpret_cast<uint2 *>(pool + co + 8 * b) = c;
+      pool[mo + b] = static_cast<uint8_t>(ms);
+    }
+  }
+}
+
 template <bool FP8>
 __global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
   constexpr int kChunks = kHeadDim / 8;  // 16-byte chunks of a bf16 row
@@ -86,7 +185,7 @@ __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-template <bool FP8, bool NEOX>
+template <int FMT, bool NEOX>
 __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendParams rp) {
   const AppendParams &p = rp.a;
   const int64_t t = blockIdx.x;
@@ -147,10 +246,39 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendParams rp) {
     } else {
       y[0] = bf16_lo(w.x); y[1] = bf16_hi(w.x); y[2] = bf16_lo(w.y); y[3] = bf16_hi(w.y);
     }
+    if constexpr (FMT == PKV_KV_NVFP4) {
+      // a micro block is 4 lanes (16 elements); the amax reduction needs
+      // every lane of the warp, so it runs before the write_kv exit
+      float xr[4];
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        xr[j] = bf16_round(y[j]);
+        amax = fmaxf(amax, fabsf(xr[j]));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      if (!write_kv) continue;
+      const float sc = __ldg((is_k ? p.k_scale : p.v_scale) + static_cast<size_t>(blk) * p.hkv + h);
+      const uint32_t ms = nvfp4_micro_scale(amax, sc);
+      const float step = __fmul_rn(sc, e4m3_value(ms));
+      uint32_t w = 0;
+      if (step != 0.f) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w |= e2m1_code(__fdiv_rn(xr[j], step)) << (4 * j);
+      }
+      int64_t co, mo;
+      nvfp4_row_offsets(p.bs, slot % p.bs, &co, &mo);
+      uint8_t *pool = static_cast<uint8_t *>(is_k ? p.k_cache : p.v_cache) +
+                      (blk * p.hkv + h) * p.bs * kNvfp4RowBytes;
+      *reinterpret_cast<uint16_t *>(pool + co + 2 * lane) = static_cast<uint16_t>(w);
+      if ((lane & 3) == 0) pool[mo + (lane >> 2)] = static_cast<uint8_t>(ms);
+      continue;
+    }
     if (!write_kv) continue;
     const size_t dst = (static_cast<size_t>(blk) * p.hkv + h) * p.bs + slot % p.bs;
     void *pool = is_k ? p.k_cache : p.v_cache;
-    if constexpr (!FP8) {
+    if constexpr (FMT == PKV_KV_BF16) {
       reinterpret_cast<uint2 *>(pool)[dst * (kHeadDim / 4) + lane] =
           make_uint2(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]));
     } else {
@@ -183,26 +311,34 @@ __global__ void __launch_bounds__(256) check_kernel(CheckParams p) {
 
 }  // namespace
 
-cudaError_t launch_rope_append(const RopeAppendParams &p, bool fp8, bool neox,
+cudaError_t launch_rope_append(const RopeAppendParams &p, int kv_dtype, bool neox,
                                cudaStream_t s) {
   if (p.a.num_tokens == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(p.a.num_tokens);
-  if (fp8 && neox) rope_append_kernel<true, true><<<grid, 256, 0, s>>>(p);
-  else if (fp8) rope_append_kernel<true, false><<<grid, 256, 0, s>>>(p);
-  else if (neox) rope_append_kernel<false, true><<<grid, 256, 0, s>>>(p);
-  else rope_append_kernel<false, false><<<grid, 256, 0, s>>>(p);
+  switch (kv_dtype * 2 + (neox ? 1 : 0)) {
+    case 0: rope_append_kernel<PKV_KV_BF16, false><<<grid, 256, 0, s>>>(p); break;
+    case 1: rope_append_kernel<PKV_KV_BF16, true><<<grid, 256, 0, s>>>(p); break;
+    case 2: rope_append_kernel<PKV_KV_FP8_E4M3, false><<<grid, 256, 0, s>>>(p); break;
+    case 3: rope_append_kernel<PKV_KV_FP8_E4M3, true><<<grid, 256, 0, s>>>(p); break;
+    case 4: rope_append_kernel<PKV_KV_NVFP4, false><<<grid, 256, 0, s>>>(p); break;
+    default: rope_append_kernel<PKV_KV_NVFP4, true><<<grid, 256, 0, s>>>(p); break;
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_append(const AppendParams &p, bool fp8, cudaStream_t s) {
-  const int64_t total = p.num_tokens * p.hkv * (kHeadDim / 8);
+cudaError_t launch_append(const AppendParams &p, int kv_dtype, cudaStream_t s) {
+  const bool nvfp4 = kv_dtype == PKV_KV_NVFP4;
+  const bool fp8 = kv_dtype == PKV_KV_FP8_E4M3;
+  const int64_t total = p.num_tokens * p.hkv * (kHeadDim / (nvfp4 ? 16 : 8));
   if (total == 0) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t want = (total + 255) / 256;
   const int blocks = static_cast<int>(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
-  if (fp8)
+  if (nvfp4)
+    kv_append_nvfp4_kernel<<<blocks, 256, 0, s>>>(p);
+  else if (fp8)
     kv_append_kernel<true><<<blocks, 256, 0, s>>>(p);
   else
     kv_append_kernel<false><<<blocks, 256, 0, s>>>(p);

@@ -119,7 +119,8 @@ std::string check_config(const pkv_config *c, pkv_status *st) {
   if (c->num_blocks <= 0) return "num_blocks must be > 0";
   if (c->max_num_seqs <= 0 || c->max_num_tokens <= 0)
     return "max_num_seqs and max_num_tokens must be > 0";
-  if (c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_FP8_E4M3)
+  if (c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_FP8_E4M3 &&
+      c->kv_dtype != PKV_KV_NVFP4)
     return fmt("unknown kv_dtype %d", c->kv_dtype);
   if (c->flags & ~static_cast<uint32_t>(PKV_FLAG_VALIDATE | PKV_FLAG_TIMING | PKV_FLAG_SEPARATE))
     return fmt("unknown flag bits 0x%x", c->flags);
@@ -128,8 +129,12 @@ std::string check_config(const pkv_config *c, pkv_status *st) {
   const int bs = c->block_size;
   if (bs != 16 && bs != 32 && bs != 64 && bs != 128 && bs != 256)
     return fmt("block_size %d is not supported (16, 32, 64, 128 or 256)", bs);
-  if (c->num_blocks * c->num_kv_heads * bs > kMaxPoolRows)
-    return "pool too large: num_blocks * num_kv_heads * block_size must be < 2^31 - 4096";
+  // NVFP4 pools are addressed in 64-byte rows: 9 per 8 tokens
+  const int64_t pool_rows = c->num_blocks * c->num_kv_heads * bs *
+                            (c->kv_dtype == PKV_KV_NVFP4 ? 9 : 8) / 8;
+  if (pool_rows > kMaxPoolRows)
+    return "pool too large: num_blocks * num_kv_heads * block_size must be < 2^31 - 4096 "
+           "(NVFP4: 8/9 of that)";
   *st = PKV_OK;
   return "";
 }
@@ -179,8 +184,8 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
     }
   }
   // decode split size: ~4 whole waves of the resident decode CTAs (2 per SM
-  // for bf16 pools, 3 for E4M3), at least 1024 keys
-  const int64_t resident = c.kv_dtype == PKV_KV_FP8_E4M3 ? 3 : 2;
+  // for bf16 pools, 3 for E4M3 and NVFP4), at least 1024 keys
+  const int64_t resident = c.kv_dtype == PKV_KV_BF16 ? 2 : 3;
   const int64_t target = 4 * resident * std::max(num_sms, 1);
   int64_t chunk = std::max<int64_t>(1024, (dec_keys / target + kSplitAlign - 1) / kSplitAlign * kSplitAlign);
   for (;;) {
@@ -324,6 +329,21 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
                    });
   *st = PKV_OK;
   return "";
+}
+
+// NVFP4 pool as rows of 64 bytes (code rows and micro-scale rows alike);
+// boxes of one group's code rows, 64-byte swizzled.
+bool encode_nvfp4_map(CUtensorMap *m, const void *base, int64_t rows, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {64};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool encode_pool_map(CUtensorMap *m, const void *base, bool fp8, int64_t rows,
@@ -532,9 +552,9 @@ pkv_status pkv_write_slots(pkv_handle *h, const void *k_new, const void *v_new,
   if (num_tokens == 0) return PKV_OK;
   if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
     return fail(h, PKV_ERR_INVALID_ARG, "NULL buffer");
-  const bool fp8 = h->cfg.kv_dtype == PKV_KV_FP8_E4M3;
-  if (fp8 && (!k_scale || !v_scale))
-    return fail(h, PKV_ERR_INVALID_ARG, "FP8 pools need k_scale and v_scale");
+  const bool quantised = h->cfg.kv_dtype != PKV_KV_BF16;
+  if (quantised && (!k_scale || !v_scale))
+    return fail(h, PKV_ERR_INVALID_ARG, "FP8 and NVFP4 pools need k_scale and v_scale");
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
     return fail(h, PKV_ERR_INVALID_ARG, "K/V buffers must be 16-byte aligned");
   cudaError_t e = cudaSetDevice(h->device);
@@ -558,7 +578,7 @@ pkv_status pkv_write_slots(pkv_handle *h, const void *k_new, const void *v_new,
   if ((e = cudaStreamIsCapturing(s, &cap)) != cudaSuccess) return cuda_fail(h, e, "capture query");
   h->capturing = cap != cudaStreamCaptureStatusNone;
   timing_begin(h, PKV_KERNEL_APPEND, s);
-  e = launch_append(p, fp8, s);
+  e = launch_append(p, h->cfg.kv_dtype, s);
   timing_end(h, PKV_KERNEL_APPEND, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "KV append launch");
   return PKV_OK;
@@ -595,8 +615,9 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
       !(out || out_f32))
     return fail(h, PKV_ERR_INVALID_ARG, "NULL buffer");
   const bool fp8 = c.kv_dtype == PKV_KV_FP8_E4M3;
-  if (fp8 && (!k_scale || !v_scale))
-    return fail(h, PKV_ERR_INVALID_ARG, "FP8 pools need k_scale and v_scale");
+  const bool nvfp4 = c.kv_dtype == PKV_KV_NVFP4;
+  if ((fp8 || nvfp4) && (!k_scale || !v_scale))
+    return fail(h, PKV_ERR_INVALID_ARG, "FP8 and NVFP4 pools need k_scale and v_scale");
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       !aligned16(out_f32))
     return fail(h, PKV_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
@@ -633,9 +654,11 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     const int64_t rows = c.num_blocks * c.num_kv_heads * bs;
     const int dec_box = std::min(bs, fp8 ? kDecKeysFp8 : kDecKeysBf16);
     const int pf_box = std::min(bs, 128);
-    bool ok = encode_pool_map(&h->dec_k, k_cache, fp8, rows, dec_box) &&
-              encode_pool_map(&h->dec_v, v_cache, fp8, rows, dec_box);
-    if (ok && !fp8)
+    bool ok = nvfp4 ? encode_nvfp4_map(&h->dec_k, k_cache, rows / 8 * 9, std::min(bs, kNvfp4Group)) &&
+                          encode_nvfp4_map(&h->dec_v, v_cache, rows / 8 * 9, std::min(bs, kNvfp4Group))
+                    : encode_pool_map(&h->dec_k, k_cache, fp8, rows, dec_box) &&
+                          encode_pool_map(&h->dec_v, v_cache, fp8, rows, dec_box);
+    if (ok && !fp8 && !nvfp4)
       ok = encode_pool_map(&h->pf_k, k_cache, false, rows, pf_box) &&
            encode_pool_map(&h->pf_v, v_cache, false, rows, pf_box);
     if (!ok) {
@@ -686,6 +709,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   const float scale_log2 = c.softmax_scale * 1.4426950408889634f;
   const int G = c.num_q_heads / c.num_kv_heads;
   const int32_t rows_total = static_cast<int32_t>(c.num_blocks * c.num_kv_heads * bs);
+  const int32_t nvfp4_rows = static_cast<int32_t>(c.num_blocks * c.num_kv_heads * bs / 8 * 9);
   DecodeParams dp{};
   dp.items = d_items;
   dp.q = static_cast<const __nv_bfloat16 *>(q);
@@ -703,7 +727,9 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   dp.hkv = c.num_kv_heads;
   dp.group = G;
   dp.bs = bs;
-  dp.rows_total = rows_total;
+  dp.rows_total = nvfp4 ? nvfp4_rows : rows_total;
+  dp.k_pool = static_cast<const uint8_t *>(k_cache);
+  dp.v_pool = static_cast<const uint8_t *>(v_cache);
   dp.num_blocks = c.num_blocks;
   dp.scale_log2 = scale_log2;
   dp.validate = validate;
@@ -745,7 +771,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   }
   if (n_dec > 0) {
     timing_begin(h, PKV_KERNEL_DECODE, s);
-    e = launch_decode(h->dec_k, h->dec_v, dp, n_dec, fp8, s);
+    e = launch_decode(h->dec_k, h->dec_v, dp, n_dec, c.kv_dtype, s);
     timing_end(h, PKV_KERNEL_DECODE, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
   }
@@ -785,7 +811,9 @@ pkv_status pkv_attention_partial(pkv_handle *h, const void *q, const void *k_cac
                                  int32_t interleave, float *out, float *lse, void *stream) {
   if (h == nullptr) return PKV_ERR_INVALID_ARG;
   h->last_error.clear();
-  const int stage = h->cfg.kv_dtype == PKV_KV_FP8_E4M3 ? kDecKeysFp8 : kDecKeysBf16;
+  const int stage = h->cfg.kv_dtype == PKV_KV_FP8_E4M3 ? kDecKeysFp8
+                    : h->cfg.kv_dtype == PKV_KV_NVFP4  ? kDecKeysNvfp4
+                                                       : kDecKeysBf16;
   if (num_shards < 1 || shard < 0 || shard >= num_shards)
     return fail(h, PKV_ERR_INVALID_ARG, fmt("shard %d of %d", shard, num_shards));
   if (interleave < stage || interleave % stage != 0)
@@ -834,9 +862,9 @@ pkv_status pkv_rope_write_slots(pkv_handle *h, void *q, const void *k_new,
       !v_cache)
     return fail(h, PKV_ERR_INVALID_ARG, "NULL buffer");
   if (max_pos < 1) return fail(h, PKV_ERR_INVALID_ARG, "max_pos must be >= 1");
-  const bool fp8 = h->cfg.kv_dtype == PKV_KV_FP8_E4M3;
-  if (fp8 && (!k_scale || !v_scale))
-    return fail(h, PKV_ERR_INVALID_ARG, "FP8 pools need k_scale and v_scale");
+  const bool quantised = h->cfg.kv_dtype != PKV_KV_BF16;
+  if (quantised && (!k_scale || !v_scale))
+    return fail(h, PKV_ERR_INVALID_ARG, "FP8 and NVFP4 pools need k_scale and v_scale");
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
       !aligned16(v_cache) || !aligned16(cos_sin_cache))
     return fail(h, PKV_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
@@ -866,7 +894,7 @@ pkv_status pkv_rope_write_slots(pkv_handle *h, void *q, const void *k_new,
   if ((e = cudaStreamIsCapturing(s, &cap)) != cudaSuccess) return cuda_fail(h, e, "capture query");
   h->capturing = cap != cudaStreamCaptureStatusNone;
   timing_begin(h, PKV_KERNEL_APPEND, s);
-  e = launch_rope_append(rp, fp8, neox != 0, s);
+  e = launch_rope_append(rp, h->cfg.kv_dtype, neox != 0, s);
   timing_end(h, PKV_KERNEL_APPEND, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "rope + KV append launch");
   return PKV_OK;

@@ -37,6 +37,17 @@ constexpr int kDecSmemBytes =
 constexpr int kDecStagesFp8 = 2;
 constexpr int kDecSmemBytesFp8 =
     kDecWarps * kDecStagesFp8 * kDecStageBytes + 1024 + 256;
+// NVFP4 pools: 64 code bytes + 8 micro-scale bytes per 128-element row;
+// rows of a (block, KV head) tile in groups of min(block_size, 64).  Decode
+// stages hold 64 keys (K and V codes 4 KB each, micro scales 512 B each),
+// two per warp ring, three CTAs per SM.
+constexpr int kNvfp4RowBytes = kHeadDim / 2 + kHeadDim / 16;   // 72
+constexpr int kNvfp4Group = 64;
+constexpr int kDecKeysNvfp4 = 64;
+constexpr int kDecStagesNvfp4 = 2;
+constexpr int kDecStageBytesNvfp4 = 2 * kDecKeysNvfp4 * kNvfp4RowBytes;   // 9216
+constexpr int kDecSmemBytesNvfp4 =
+    kDecWarps * kDecStagesNvfp4 * kDecStageBytesNvfp4 + 1024 + 256;
 constexpr int kSplitAlign = 256;          // split ranges start at multiples
 
 // ---- prefill kernel geometry ---------------------------------------------------
@@ -65,6 +76,10 @@ struct DecodeParams {
   // to out_f32 (fp32, normalised) instead of out when out_f32 is set.
   int32_t dcp_n, dcp_r, dcp_k;
   float *out_f32;
+  // NVFP4 pools (byte addresses of the micro scales); rows_total then counts
+  // the pools' 64-byte rows
+  const uint8_t *k_pool;
+  const uint8_t *v_pool;
 };
 
 struct PrefillParams {
@@ -123,10 +138,10 @@ struct CheckParams {
 };
 
 // Launchers (each returns the launch's cudaError_t).
-cudaError_t launch_append(const AppendParams &p, bool fp8, cudaStream_t s);
-cudaError_t launch_rope_append(const RopeAppendParams &p, bool fp8, bool neox, cudaStream_t s);
+cudaError_t launch_append(const AppendParams &p, int kv_dtype, cudaStream_t s);
+cudaError_t launch_rope_append(const RopeAppendParams &p, int kv_dtype, bool neox, cudaStream_t s);
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          const DecodeParams &p, int num_items, bool fp8,
+                          const DecodeParams &p, int num_items, int kv_dtype,
                           cudaStream_t s);
 cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p,

@@ -16,14 +16,21 @@ import workloads as W
 TOL = {
     "bf16": dict(max_abs=1e-2, mean_abs=1e-3, rel=1e-2, lse=1e-3),
     "fp8": dict(max_abs=2e-2, mean_abs=1e-3, rel=2e-2, lse=1e-3),
+    # NVFP4 KV: the oracle attends over the stored codes exactly, and the
+    # kernel's rounding sources are those of the E4M3 path (f16 P with the
+    # block scale folded in, fp32 accumulation, bf16 output; its K side is
+    # exact in f16), so the E4M3 gate applies
+    "nvfp4": dict(max_abs=2e-2, mean_abs=1e-3, rel=2e-2, lse=1e-3),
 }
+
+KV_DTYPES = {"bf16": pkv.KV_BF16, "fp8": pkv.KV_FP8_E4M3, "nvfp4": pkv.KV_NVFP4}
 
 
 def make_handle(batch: W.Batch, flags: int = pkv.FLAG_VALIDATE) -> pkv.Handle:
     s = batch.spec
     cfg = pkv.make_config(s.hq, s.hkv, s.block_size, batch.num_blocks,
                           max(1, s.num_seqs), max(1, s.num_tokens),
-                          kv_dtype=pkv.KV_FP8_E4M3 if s.kv_dtype == "fp8" else pkv.KV_BF16,
+                          kv_dtype=KV_DTYPES[s.kv_dtype],
                           softmax_scale=s.softmax_scale, flags=flags)
     return pkv.Handle(cfg)
 

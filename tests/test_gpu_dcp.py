@@ -21,6 +21,8 @@ CASES = [
     ("bf16_g8_n2_i64", 64, 8, 64, [1, 1], [3000, 65], "bf16", 2, 64),
     ("bf16_g4_n1", 32, 8, 16, [1, 1], [1234, 17], "bf16", 1, 16),
     ("fp8_g8_n2_i64", 64, 8, 64, [1, 1, 1], [4000, 64, 129], "fp8", 2, 64),
+    ("nvfp4_g8_n2_i64", 64, 8, 64, [1, 1, 1], [4000, 64, 129], "nvfp4", 2, 64),
+    ("nvfp4_g4_n3_i128", 32, 8, 16, [1, 1], [5000, 300], "nvfp4", 3, 128),
 ]
 
 

@@ -25,7 +25,8 @@ def spec(name, hq, hkv, bs, q_lens, seq_lens, kv="bf16", seed=7, shared=None):
 
 # ---- KV append -------------------------------------------------------------------
 
-@pytest.mark.parametrize("kv,bs", [("bf16", 16), ("bf16", 64), ("fp8", 64), ("fp8", 16)])
+@pytest.mark.parametrize("kv,bs", [("bf16", 16), ("bf16", 64), ("fp8", 64), ("fp8", 16),
+                                   ("nvfp4", 16), ("nvfp4", 64), ("nvfp4", 128)])
 def test_write_slots_bit_exact(kv, bs):
     """Every byte of both pools equals the oracle's append (new rows at their
     slots, poison everywhere else), including -1 padding slots."""
@@ -42,6 +43,27 @@ def test_write_slots_bit_exact(kv, bs):
     h.check_device_errors()
     oracle.write_slots(kc0, vc0, W.bf16_bits(b.k_new), W.bf16_bits(b.v_new),
                        b.slot_mapping, k_scale=ks, v_scale=vs)
+    assert np.array_equal(W.host_pool(b, "k"), kc0)
+    assert np.array_equal(W.host_pool(b, "v"), vc0)
+
+
+def test_write_slots_nvfp4_saturation_and_underflow_like_the_oracle():
+    """NVFP4 append at the edges: K rows far above 6 * 448 * scale (micro
+    scales saturate at 448, codes at 6) and V rows so small that micro
+    scales round to 0 (all codes 0) or to E4M3 subnormals."""
+    s = spec("sat4", 4, 2, 16, [5], [20], kv="nvfp4")
+    b = W.generate(s, DEV)
+    b.k_new.mul_(4000.0)
+    b.v_new.mul_(1e-6)
+    b.v_new[2].mul_(1e3)
+    kc0, vc0 = W.host_pool(b, "k"), W.host_pool(b, "v")
+    h = U.make_handle(b)
+    m = U.device_meta(b)
+    h.write_slots(b.k_new, b.v_new, m["slots"], b.k_cache, b.v_cache, b.k_scale, b.v_scale)
+    torch.cuda.synchronize()
+    oracle.write_slots(kc0, vc0, W.bf16_bits(b.k_new), W.bf16_bits(b.v_new),
+                       b.slot_mapping, k_scale=b.k_scale.cpu().numpy(),
+                       v_scale=b.v_scale.cpu().numpy())
     assert np.array_equal(W.host_pool(b, "k"), kc0)
     assert np.array_equal(W.host_pool(b, "v"), vc0)
 
@@ -88,6 +110,11 @@ SWEEP = [
     ("fp8_prefill_gqa8_bs64", 64, 8, 64, [1, 70, 5], [5000, 700, 65], "fp8"),
     ("fp8_prefill_gqa3", 6, 2, 64, [10, 1, 33], [100, 64, 1500], "fp8"),
     ("gqa256_chunks", 256, 1, 16, [1, 2, 9], [40, 50, 300], "bf16"),
+    # NVFP4 pools (decode kernel; prefill rows as 8-row chunks)
+    ("nvfp4_gqa8_bs64", 64, 8, 64, [1, 1, 1, 1], [1, 63, 65, 5000], "nvfp4"),
+    ("nvfp4_gqa4_bs16", 32, 8, 16, [1, 2, 1, 40], [17, 33, 2000, 300], "nvfp4"),
+    ("nvfp4_gqa2_bs128", 4, 2, 128, [1, 3, 1], [129, 700, 4100], "nvfp4"),
+    ("nvfp4_gqa8_bs32", 16, 2, 32, [1, 1], [95, 3000], "nvfp4"),
 ]
 
 

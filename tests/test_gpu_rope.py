@@ -42,7 +42,8 @@ def _bf16_ulp_ok(got_bits, ref_f64, ref_bits, x_bits, neox):
     return bool(np.all(same | (near & adjacent))), float(np.mean(~same))
 
 
-@pytest.mark.parametrize("kv,neox", [("bf16", True), ("bf16", False), ("fp8", True)])
+@pytest.mark.parametrize("kv,neox", [("bf16", True), ("bf16", False), ("fp8", True),
+                                     ("nvfp4", False)])
 def test_rope_append_matches_the_oracle(kv, neox):
     s = W.custom_spec(f"rope_{kv}", 32, 8, 16 if kv == "bf16" else 64, [37, 1, 200],
                       [100, 5000, 260], seed=31, kv_dtype=kv)
@@ -69,13 +70,19 @@ def test_rope_append_matches_the_oracle(kv, neox):
     # K rotated then appended, V appended: the oracle's append of its own
     # rotated K must agree with the pools wherever the rotated bf16 K agree
     kf, kbits = oracle.rope(W.bf16_bits(b.k_new), pos, tab, neox=neox)
-    ks = b.k_scale.cpu().numpy() if kv == "fp8" else None
-    vs = b.v_scale.cpu().numpy() if kv == "fp8" else None
+    ks = b.k_scale.cpu().numpy() if kv != "bf16" else None
+    vs = b.v_scale.cpu().numpy() if kv != "bf16" else None
     oracle.write_slots(kc0, vc0, kbits, W.bf16_bits(b.v_new), b.slot_mapping,
                        k_scale=ks, v_scale=vs)
     assert np.array_equal(W.host_pool(b, "v"), vc0)
     kg = W.host_pool(b, "k")
     diff = kg != kc0
+    if kv == "nvfp4":
+        # a rotated K element one bf16 ulp off can move its micro block's
+        # scale and so all 16 codes; such blocks are rare
+        assert diff.mean() < 1e-2
+        h.close()
+        return
     assert diff.mean() < 1e-3
     if kv == "bf16":
         rows = np.nonzero(diff.any(-1))

@@ -11,7 +11,7 @@ import workloads
 def _plan(spec, num_sms=152):
     cfg = pkv.make_config(spec.hq, spec.hkv, spec.block_size, 10 ** 6,
                           max(1, spec.num_seqs), max(1, spec.num_tokens),
-                          kv_dtype=1 if spec.kv_dtype == "fp8" else 0)
+                          kv_dtype={"bf16": 0, "fp8": 1, "nvfp4": 2}[spec.kv_dtype])
     qsl = np.concatenate([[0], np.cumsum(spec.q_lens)]).astype(np.int32)
     items, parts = pkv.plan(cfg, qsl, np.asarray(spec.seq_lens, np.int32), num_sms)
     return items, parts, qsl
@@ -116,7 +116,8 @@ def test_plan_empty_and_zero_token_requests():
     assert items == []
 
 
-@pytest.mark.parametrize("kv,hq,hkv", [("fp8", 32, 8), ("fp8", 6, 2), ("bf16", 256, 1)])
+@pytest.mark.parametrize("kv,hq,hkv", [("fp8", 32, 8), ("fp8", 6, 2), ("bf16", 256, 1),
+                                      ("nvfp4", 32, 8)])
 def test_prefill_rows_without_tensor_core_tiles_are_chunked(kv, hq, hkv):
     """Over E4M3 pools, or with query groups above 128, prefill rows become
     decode-kernel items of at most 8 rows: they tile [0, q*G) exactly, each

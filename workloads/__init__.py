@@ -75,7 +75,7 @@ class Spec:
     hq: int
     hkv: int
     block_size: int
-    kv_dtype: str                      # "bf16" or "fp8"
+    kv_dtype: str                      # "bf16", "fp8" or "nvfp4"
     q_lens: list[int]
     seq_lens: list[int]
     seed: int
@@ -237,6 +237,56 @@ def _fill_fp8_pool(codes: torch.Tensor, scales: torch.Tensor, g: torch.Generator
         scales[b0:b1] = sc
 
 
+# NVFP4 pools: rows of 64 code bytes + 8 micro-scale bytes, grouped per
+# min(block_size, 64) rows inside a (block, KV head) tile.
+NVFP4_ROW = 72
+NVFP4_GROUP = 64
+# magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 drawn with roughly the frequencies a
+# Gaussian block quantised against its own largest element shows
+_E2M1_MAG_WEIGHTS = [0.06, 0.12, 0.115, 0.11, 0.147, 0.16, 0.158, 0.13]
+
+
+def nvfp4_row_bytes(bs: int, off: np.ndarray, head_dim: int = HEAD_DIM):
+    """Byte positions inside an NVFP4 (block, KV head) tile of the codes
+    ([n, D/2]) and micro scales ([n, D/16]) of rows `off`."""
+    gs = min(bs, NVFP4_GROUP)
+    off = np.asarray(off, dtype=np.int64)
+    base = (off // gs) * gs * (head_dim // 2 + head_dim // 16)
+    r = off % gs
+    codes = base[:, None] + r[:, None] * (head_dim // 2) + np.arange(head_dim // 2)[None, :]
+    ms = (base[:, None] + gs * (head_dim // 2) + r[:, None] * (head_dim // 16) +
+          np.arange(head_dim // 16)[None, :])
+    return codes, ms
+
+
+def _fill_nvfp4_pool(tiles: torch.Tensor, scales: torch.Tensor, g: torch.Generator,
+                     chunk_blocks: int = 2048):
+    """NVFP4 tiles drawn directly as codes (no quantisation here): E2M1
+    nibbles with Gaussian-like magnitude frequencies and random signs; micro
+    scales the E4M3 codes (torch's cast) of U[1, 3] / (6 scale); the (block,
+    KV head) scale U[3.5, 4.5] / 2688, so that values look like a N(0, 1)
+    source quantised the usual way."""
+    nb, hkv, tb = tiles.shape
+    bs = tb // NVFP4_ROW
+    gs = min(bs, NVFP4_GROUP)
+    w = torch.tensor(_E2M1_MAG_WEIGHTS, dtype=torch.float32, device=tiles.device)
+    for b0 in range(0, nb, chunk_blocks):
+        b1 = min(nb, b0 + chunk_blocks)
+        n = b1 - b0
+        sc = (torch.rand((n, hkv), generator=g, device=tiles.device) + 3.5) / 2688.0
+        mag = torch.multinomial(w, n * hkv * bs * 128, replacement=True, generator=g)
+        sign = torch.randint(0, 2, mag.shape, generator=g, device=tiles.device) * 8
+        nib = (mag + sign).to(torch.uint8).view(n, hkv, bs // gs, gs, 64, 2)
+        codes = nib[..., 0] | (nib[..., 1] << 4)
+        target = (torch.rand((n, hkv, bs // gs, gs, 8), generator=g, device=tiles.device) * 2 + 1)
+        target = target / (6.0 * sc[:, :, None, None, None])
+        ms = target.clamp(max=448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        grp = tiles[b0:b1].view(n, hkv, bs // gs, gs * NVFP4_ROW)
+        grp[..., :gs * 64] = codes.reshape(n, hkv, bs // gs, gs * 64)
+        grp[..., gs * 64:] = ms.reshape(n, hkv, bs // gs, gs * 8)
+        scales[b0:b1] = sc
+
+
 def generate(spec: Spec, device: str | torch.device = "cpu", q_scale: float = 1.0,
              tail_entries: int = 3, tail_fill: str = "poison_block",
              unused_poison: bool = True) -> Batch:
@@ -269,11 +319,18 @@ def generate(spec: Spec, device: str | torch.device = "cpu", q_scale: float = 1.
         slots[qsl[i]:qsl[i + 1]] = tables[i, p // bs] * bs + p % bs
 
     fp8 = spec.kv_dtype == "fp8"
-    cache_dtype = torch.uint8 if fp8 else torch.bfloat16
-    k_cache = torch.empty((pool, hkv, bs, d), dtype=cache_dtype, device=device)
+    nvfp4 = spec.kv_dtype == "nvfp4"
+    cache_dtype = torch.uint8 if (fp8 or nvfp4) else torch.bfloat16
+    shape = (pool, hkv, bs * NVFP4_ROW) if nvfp4 else (pool, hkv, bs, d)
+    k_cache = torch.empty(shape, dtype=cache_dtype, device=device)
     v_cache = torch.empty_like(k_cache)
     k_scale = v_scale = None
-    if fp8:
+    if nvfp4:
+        k_scale = torch.empty((pool, hkv), dtype=torch.float32, device=device)
+        v_scale = torch.empty_like(k_scale)
+        _fill_nvfp4_pool(k_cache, k_scale, _gen(spec.seed, S_K, gdev))
+        _fill_nvfp4_pool(v_cache, v_scale, _gen(spec.seed, S_V, gdev))
+    elif fp8:
         k_scale = torch.empty((pool, hkv), dtype=torch.float32, device=device)
         v_scale = torch.empty_like(k_scale)
         _fill_fp8_pool(k_cache, k_scale, _gen(spec.seed, S_K, gdev))
@@ -283,6 +340,13 @@ def generate(spec: Spec, device: str | torch.device = "cpu", q_scale: float = 1.
         _fill_normal(v_cache.view(-1, d), _gen(spec.seed, S_V, gdev))
 
     def poison(cache, rows_blk, rows_off):
+        if nvfp4:
+            # codes 6, micro scales NaN: any read shows up as NaN
+            ci, mi = nvfp4_row_bytes(bs, rows_off.cpu().numpy())
+            rb = rows_blk[:, None]
+            cache[rb, :, torch.as_tensor(ci, device=cache.device)] = 0x77
+            cache[rb, :, torch.as_tensor(mi, device=cache.device)] = E4M3_NAN
+            return
         if fp8:
             cache[rows_blk, :, rows_off, :] = E4M3_NAN
         else:
@@ -294,11 +358,11 @@ def generate(spec: Spec, device: str | torch.device = "cpu", q_scale: float = 1.
         mask[used] = False
         unused = torch.from_numpy(np.nonzero(mask)[0]).to(device)
         for cache in (k_cache, v_cache):
-            if fp8:
+            if fp8 or nvfp4:
                 cache[unused] = E4M3_NAN
             else:
                 cache.view(torch.int16)[unused] = BF16_NAN
-        if fp8:
+        if fp8 or nvfp4:
             k_scale[unused] = 1.0
             v_scale[unused] = 1.0
     # rows past the end of each sequence's last block
@@ -423,7 +487,8 @@ def algorithmic_work(spec: Spec) -> dict:
     prefill flops: 4 * D * Hq per causal (query, key) pair.
     """
     d, hq, hkv, bs = spec.head_dim, spec.hq, spec.hkv, spec.block_size
-    s = 1 if spec.kv_dtype == "fp8" else 2
+    # bytes per stored element (NVFP4: codes and micro scales, 72 per 128)
+    s = {"fp8": 1, "nvfp4": NVFP4_ROW / 128}.get(spec.kv_dtype, 2)
     dec_bytes = 0
     pre_flops = 0
     pre_bytes = 0
@@ -432,15 +497,15 @@ def algorithmic_work(spec: Spec) -> dict:
         h = L - q
         if q * (hq // hkv) <= 8:
             n_dec += 1
-            dec_bytes += L * 2 * hkv * d * s + 2 * q * hq * d * 2
-            if s == 1:
+            dec_bytes += int(L * 2 * hkv * d * s) + 2 * q * hq * d * 2
+            if s != 2:
                 dec_bytes += cdiv(L, bs) * hkv * 2 * 4
         else:
             n_pre += 1
             pre_flops += 4 * d * hq * (q * h + q * (q + 1) // 2)
-            pre_bytes += L * 2 * hkv * d * s + 2 * q * hq * d * 2
+            pre_bytes += int(L * 2 * hkv * d * s) + 2 * q * hq * d * 2
     T = spec.num_tokens
-    append_bytes = 2 * T * 2 * hkv * d * 2 if s == 2 else T * 2 * hkv * d * (2 + 1)
+    append_bytes = int(T * 2 * hkv * d * (2 + s))
     return {"decode_bytes": dec_bytes, "prefill_flops": pre_flops,
             "prefill_bytes": pre_bytes, "append_bytes": append_bytes,
             "num_decode": n_dec, "num_prefill": n_pre}
