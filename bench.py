@@ -10,7 +10,7 @@ log-sum-exp combine (pkv_attention_varlen).  `value` is algorithmic bytes
 (every context token's K and V once, Q and O, the append's read + write) per
 second over the whole step, all inputs resident in HBM.  Each rank of a
 multi-GPU run (torchrun) processes its own replica (weak scaling).  The
-incremental-prefill, mixed-step and FP8 workloads are reported in `secondary`
+incremental-prefill, mixed-step, FP8 and NVFP4 workloads are reported in `secondary`
 unless --primary-only is given.
 
 `--impl reference` times the fp64 CPU oracle on the host cores on a bounded
@@ -19,6 +19,7 @@ sample of the same workload (one (request, KV head) slice per step).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -58,6 +59,7 @@ CASES = {
     "small-decode": (1, list(range(16))),     # ~1.3 GB of bf16 KV
     "small-prefill": (2, [4, 5]),             # two post-tool-call sessions
     "small-fp8": (4, [0]),                    # one ~0.6-1M-token FP8 request
+    "small-nvfp4": (4, [0, 1]),               # two such requests, NVFP4 KV
     "small-mixed": (3, list(range(0, 120, 8)) + [120, 127]),
 }
 
@@ -65,8 +67,9 @@ CASES = {
 def case_spec(name: str) -> W.Spec:
     index, seqs = CASES[name]
     full = W.config_spec(index)
+    kv = "nvfp4" if name == "small-nvfp4" else full.kv_dtype
     return W.Spec(f"{full.name}[{name}]", full.hq, full.hkv, full.block_size,
-                  full.kv_dtype, [full.q_lens[i] for i in seqs],
+                  kv, [full.q_lens[i] for i in seqs],
                   [full.seq_lens[i] for i in seqs], full.seed)
 
 
@@ -189,7 +192,8 @@ def make_handle(batch, flags):
     s = batch.spec
     cfg = pkv.make_config(s.hq, s.hkv, s.block_size, batch.num_blocks, s.num_seqs,
                           s.num_tokens, softmax_scale=s.softmax_scale, flags=flags,
-                          kv_dtype=pkv.KV_FP8_E4M3 if s.kv_dtype == "fp8" else pkv.KV_BF16)
+                          kv_dtype={"bf16": pkv.KV_BF16, "fp8": pkv.KV_FP8_E4M3,
+                                    "nvfp4": pkv.KV_NVFP4}[s.kv_dtype])
     return pkv.Handle(cfg, device=batch.q.device.index or 0)
 
 
@@ -444,7 +448,9 @@ def time_graph(index, steps: int, device: str) -> dict:
 def secondary(args, world, peaks, device):
     out = []
     out.append({"cuda_graph": [time_graph(0, 500, device), time_graph(1, 200, device)]})
-    for idx, steps in ((2, 10), (3, 10), (4, 50)):
+    nvfp4 = dataclasses.replace(W.config_spec(4), name="c5_nvfp4_long_decode",
+                                kv_dtype="nvfp4")
+    for idx, steps in ((2, 10), (3, 10), (4, 50), (nvfp4, 50)):
         r = time_workload(idx, steps, 3, world, peaks, device)
         spec, work = r["spec"], r["work"]
         ms_step = r["ms"] / steps

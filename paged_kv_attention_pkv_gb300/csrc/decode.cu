@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, FP8 ? 3 : 2)
   decode_item<FP8, kDecWarps>(kmap, vmap, p, p.items[blockIdx.x], smem, threadIdx.x, 0);
 }
 
-__global__ void __launch_bounds__(kDecWarps * 32, 3)
+__global__ void __launch_bounds__(kDecWarps * 32, kDecCtasNvfp4)
     decode_nvfp4_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap,
                         const DecodeParams p) {

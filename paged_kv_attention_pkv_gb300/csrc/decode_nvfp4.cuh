@@ -8,8 +8,9 @@
 // e2m1(code) * e4m3(micro scale of its 16 elements) * fp32 (block, KV head)
 // scale.
 //
-// A stage is 64 keys: their code rows (64 bytes each) arrive by TMA into a
-// 64-byte-swizzled tile, their micro scales (8 bytes each) by a bulk copy.
+// A stage is kDecKeysNvfp4 keys: their code rows (64 bytes each) arrive by
+// TMA into a 64-byte-swizzled tile, their micro scales (8 bytes each) by a
+// bulk copy.
 // Codes are converted to f16 in hardware and multiplied by their micro scale
 // in f16, which is exact (a 2-bit by 4-bit significand product), so the MMAs
 // see e2m1 * e4m3 exactly; the fp32 block scales are folded into the score
@@ -28,7 +29,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kNvKeys = 64;                       // keys per stage
+constexpr int kNvKeys = kDecKeysNvfp4;            // keys per stage
 constexpr int kNvCodeBytes = kNvKeys * 64;        // code rows of one of K / V
 constexpr int kNvScaleBytes = kNvKeys * 8;        // micro scales of one of K / V
 static_assert(2 * (kNvCodeBytes + kNvScaleBytes) == kDecStageBytesNvfp4, "stage layout");
@@ -84,21 +85,23 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
   uint64_t *full = bars + warp * S;
   const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
   const int gs = p.bs < kNvfp4Group ? p.bs : kNvfp4Group;   // rows per group
+  const int br = gs < KS ? gs : KS;                         // keys per copy
   const int tile_rows = p.bs / 8 * 9;                       // 64-byte rows per tile
   const int group_rows = gs / 8 * 9;
 
-  // Fill ring slot i % S with stage i (lane 0 only): per group of gs keys,
-  // the code rows by TMA and the micro scales by a bulk copy.
+  // Fill ring slot i % S with stage i (lane 0 only): per run of br keys
+  // inside one group, the code rows by TMA and the micro scales by a bulk
+  // copy.
   auto issue = [&](int i) {
     const int key0 = kb + (warp + i * NW) * KS;
     const int slot = i % S;
     uint8_t *st = ring + slot * kDecStageBytesNvfp4;
     const int gkey0 = global_key(p, key0);
-    int groups = 0;
-    for (int r = 0; r < KS; r += gs)
-      if (key0 + r < ke) ++groups;
-    mbar_arrive_expect_tx(&full[slot], groups * gs * 2 * kNvfp4RowBytes);
-    for (int r = 0; r < KS; r += gs) {
+    int runs = 0;
+    for (int r = 0; r < KS; r += br)
+      if (key0 + r < ke) ++runs;
+    mbar_arrive_expect_tx(&full[slot], runs * br * 2 * kNvfp4RowBytes);
+    for (int r = 0; r < KS; r += br) {
       if (key0 + r >= ke) break;
       const int gk = gkey0 + r;
       const int32_t blk = __ldg(bt + gk / p.bs);
@@ -107,13 +110,15 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
       if (blk < 0 || blk >= p.num_blocks) {
         record_error(p.err, kErrBadBlock);
       } else {
-        row = (blk * p.hkv + it.kv_head) * tile_rows + (gk % p.bs) / gs * group_rows;
-        sbyte = static_cast<int64_t>(row + gs) * 64;
+        const int in_blk = gk % p.bs;
+        const int grp0 = (blk * p.hkv + it.kv_head) * tile_rows + in_blk / gs * group_rows;
+        row = grp0 + in_blk % gs;
+        sbyte = static_cast<int64_t>(grp0 + gs) * 64 + (in_blk % gs) * 8;
       }
       tma_load_2d(st + r * 64, &kmap, 0, row, &full[slot]);
       tma_load_2d(st + kNvCodeBytes + r * 64, &vmap, 0, row, &full[slot]);
-      bulk_load(st + 2 * kNvCodeBytes + r * 8, p.k_pool + sbyte, gs * 8, &full[slot]);
-      bulk_load(st + 2 * kNvCodeBytes + kNvScaleBytes + r * 8, p.v_pool + sbyte, gs * 8,
+      bulk_load(st + 2 * kNvCodeBytes + r * 8, p.k_pool + sbyte, br * 8, &full[slot]);
+      bulk_load(st + 2 * kNvCodeBytes + kNvScaleBytes + r * 8, p.v_pool + sbyte, br * 8,
                 &full[slot]);
     }
   };
@@ -216,76 +221,86 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
       break;
     }
     const int key0 = kb + (warp + i * NW) * KS;
+    const int gkey0 = global_key(p, key0);
     const uint32_t kc = smem_addr(ring + slot * kDecStageBytesNvfp4);
     const uint32_t vc = kc + kNvCodeBytes;
     const uint32_t ksc = kc + 2 * kNvCodeBytes;
     const uint32_t vsc = ksc + kNvScaleBytes;
+    // ---- S^T = K Q^T for the stage's sub-tiles (16 keys x 8 columns each):
+    // independent MMA chains, then one softmax step for all 64 keys
+    float s[kSubs][4];
+#pragma unroll
+    for (int sub = 0; sub < kSubs; ++sub) {
+      s[sub][0] = s[sub][1] = s[sub][2] = s[sub][3] = 0.f;
+      if (key0 + 16 * sub >= ke) continue;
+      const int rA = 16 * sub + qk_row, rB = rA + 8;
+      const uint4 x = lds128(kc + swz64(rA * 64 + 16 * t));
+      const uint4 y = lds128(kc + swz64(rB * 64 + 16 * t));
+      // micro scales of micro blocks 2t, 2t+1 of both rows, as f16 pairs
+      const uint32_t sa = e4m3x2lo_to_f16x2(lds16(ksc + rA * 8 + 2 * t));
+      const uint32_t sb = e4m3x2lo_to_f16x2(lds16(ksc + rB * 8 + 2 * t));
+      const uint32_t sa0 = __byte_perm(sa, 0, 0x1010), sa1 = __byte_perm(sa, 0, 0x3232);
+      const uint32_t sb0 = __byte_perm(sb, 0, 0x1010), sb1 = __byte_perm(sb, 0, 0x3232);
+      const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+      const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t ca[4], cb[4];
+        e2m1x8_to_f16x2(xw[w], ca);
+        e2m1x8_to_f16x2(yw[w], cb);
+        const uint32_t ma = w < 2 ? sa0 : sa1, mb = w < 2 ? sb0 : sb1;
+        mma_f16(s[sub], hmul2(ca[0], ma), hmul2(cb[0], mb), hmul2(ca[1], ma),
+                hmul2(cb[1], mb), qf[2 * w][0], qf[2 * w][1]);
+        mma_f16(s[sub], hmul2(ca[2], ma), hmul2(cb[2], mb), hmul2(ca[3], ma),
+                hmul2(cb[3], mb), qf[2 * w + 1][0], qf[2 * w + 1][1]);
+      }
+    }
+    // ---- scale, mask (validity on item-local keys, causality on global
+    // positions), online softmax per column over the whole stage
+    float tm0 = -CUDART_INF_F, tm1 = -CUDART_INF_F;
+#pragma unroll
+    for (int sub = 0; sub < kSubs; ++sub) {
+      const float sc0 = p.scale_log2 * sk_sub[sub] * inv_sq0;
+      const float sc1 = p.scale_log2 * sk_sub[sub] * inv_sq1;
+      const int kr0 = key0 + 16 * sub + qk_row, kr1 = kr0 + 8;
+      const int gr0 = gkey0 + 16 * sub + qk_row, gr1 = gr0 + 8;
+      s[sub][0] = (kr0 < ke && gr0 <= pos0) ? s[sub][0] * sc0 : -CUDART_INF_F;
+      s[sub][1] = (kr0 < ke && gr0 <= pos1) ? s[sub][1] * sc1 : -CUDART_INF_F;
+      s[sub][2] = (kr1 < ke && gr1 <= pos0) ? s[sub][2] * sc0 : -CUDART_INF_F;
+      s[sub][3] = (kr1 < ke && gr1 <= pos1) ? s[sub][3] * sc1 : -CUDART_INF_F;
+      tm0 = fmaxf(tm0, fmaxf(s[sub][0], s[sub][2]));
+      tm1 = fmaxf(tm1, fmaxf(s[sub][1], s[sub][3]));
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
+      tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
+    }
+    const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
+    const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+    const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+    const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+    m0 = mn0;
+    m1 = mn1;
+    l0 *= al0;
+    l1 *= al1;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      acc[mt][0] *= al0;
+      acc[mt][1] *= al1;
+      acc[mt][2] *= al0;
+      acc[mt][3] *= al1;
+    }
 #pragma unroll
     for (int sub = 0; sub < kSubs; ++sub) {
       const int k16 = key0 + 16 * sub;
       if (k16 >= ke) break;
-      const int g16 = global_key(p, key0) + 16 * sub;   // global key of k16
-      // ---- S^T = K Q^T for 16 keys x 8 columns
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const int rA = 16 * sub + qk_row, rB = rA + 8;
-        const uint4 x = lds128(kc + swz64(rA * 64 + 16 * t));
-        const uint4 y = lds128(kc + swz64(rB * 64 + 16 * t));
-        // micro scales of micro blocks 2t, 2t+1 of both rows, as f16 pairs
-        const uint32_t sa = e4m3x2lo_to_f16x2(lds16(ksc + rA * 8 + 2 * t));
-        const uint32_t sb = e4m3x2lo_to_f16x2(lds16(ksc + rB * 8 + 2 * t));
-        const uint32_t sa0 = __byte_perm(sa, 0, 0x1010), sa1 = __byte_perm(sa, 0, 0x3232);
-        const uint32_t sb0 = __byte_perm(sb, 0, 0x1010), sb1 = __byte_perm(sb, 0, 0x3232);
-        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-        const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint32_t ca[4], cb[4];
-          e2m1x8_to_f16x2(xw[w], ca);
-          e2m1x8_to_f16x2(yw[w], cb);
-          const uint32_t ma = w < 2 ? sa0 : sa1, mb = w < 2 ? sb0 : sb1;
-          mma_f16(s, hmul2(ca[0], ma), hmul2(cb[0], mb), hmul2(ca[1], ma), hmul2(cb[1], mb),
-                  qf[2 * w][0], qf[2 * w][1]);
-          mma_f16(s, hmul2(ca[2], ma), hmul2(cb[2], mb), hmul2(ca[3], ma), hmul2(cb[3], mb),
-                  qf[2 * w + 1][0], qf[2 * w + 1][1]);
-        }
-      }
-      // ---- scale, mask, online softmax per column
-      const float sc0 = p.scale_log2 * sk_sub[sub] * inv_sq0;
-      const float sc1 = p.scale_log2 * sk_sub[sub] * inv_sq1;
-      const float pv_scale = sv_sub[sub] * kNvPScale;
-      // validity on item-local keys, causality on global positions
-      const int kr0 = k16 + qk_row, kr1 = kr0 + 8;
-      const int gr0 = g16 + qk_row, gr1 = gr0 + 8;
-      s[0] = (kr0 < ke && gr0 <= pos0) ? s[0] * sc0 : -CUDART_INF_F;
-      s[1] = (kr0 < ke && gr0 <= pos1) ? s[1] * sc1 : -CUDART_INF_F;
-      s[2] = (kr1 < ke && gr1 <= pos0) ? s[2] * sc0 : -CUDART_INF_F;
-      s[3] = (kr1 < ke && gr1 <= pos1) ? s[3] * sc1 : -CUDART_INF_F;
-      float tm0 = fmaxf(s[0], s[2]);
-      float tm1 = fmaxf(s[1], s[3]);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
-        tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
-      }
-      const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
-      const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
-      const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-      const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-      const float p0 = exp2f(s[0] - mu0), p1 = exp2f(s[1] - mu1);
-      const float p2 = exp2f(s[2] - mu0), p3 = exp2f(s[3] - mu1);
-      l0 = l0 * al0 + p0 + p2;
-      l1 = l1 * al1 + p1 + p3;
-      m0 = mn0;
-      m1 = mn1;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        acc[mt][0] *= al0;
-        acc[mt][1] *= al1;
-        acc[mt][2] *= al0;
-        acc[mt][3] *= al1;
-      }
+      const float p0 = exp2f(s[sub][0] - mu0), p1 = exp2f(s[sub][1] - mu1);
+      const float p2 = exp2f(s[sub][2] - mu0), p3 = exp2f(s[sub][3] - mu1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
       // ---- P^T as the B operand (f16, V's block scale folded in)
+      const float pv_scale = sv_sub[sub] * kNvPScale;
       const uint32_t b0 = movmatrix_trans(pack_f16(p0 * pv_scale, p1 * pv_scale));
       const uint32_t b1 = movmatrix_trans(pack_f16(p2 * pv_scale, p3 * pv_scale));
       // ---- O^T += V^T P^T: this thread's micro block g of rows A, B, C, D

@@ -185,7 +185,9 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
   }
   // decode split size: ~4 whole waves of the resident decode CTAs (2 per SM
   // for bf16 pools, 3 for E4M3 and NVFP4), at least 1024 keys
-  const int64_t resident = c.kv_dtype == PKV_KV_BF16 ? 2 : 3;
+  const int64_t resident = c.kv_dtype == PKV_KV_BF16       ? 2
+                           : c.kv_dtype == PKV_KV_FP8_E4M3 ? 3
+                                                           : kDecCtasNvfp4;
   const int64_t target = 4 * resident * std::max(num_sms, 1);
   int64_t chunk = std::max<int64_t>(1024, (dec_keys / target + kSplitAlign - 1) / kSplitAlign * kSplitAlign);
   for (;;) {
@@ -654,8 +656,9 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     const int64_t rows = c.num_blocks * c.num_kv_heads * bs;
     const int dec_box = std::min(bs, fp8 ? kDecKeysFp8 : kDecKeysBf16);
     const int pf_box = std::min(bs, 128);
-    bool ok = nvfp4 ? encode_nvfp4_map(&h->dec_k, k_cache, rows / 8 * 9, std::min(bs, kNvfp4Group)) &&
-                          encode_nvfp4_map(&h->dec_v, v_cache, rows / 8 * 9, std::min(bs, kNvfp4Group))
+    const int nv_box = std::min(std::min(bs, kNvfp4Group), kDecKeysNvfp4);
+    bool ok = nvfp4 ? encode_nvfp4_map(&h->dec_k, k_cache, rows / 8 * 9, nv_box) &&
+                          encode_nvfp4_map(&h->dec_v, v_cache, rows / 8 * 9, nv_box)
                     : encode_pool_map(&h->dec_k, k_cache, fp8, rows, dec_box) &&
                           encode_pool_map(&h->dec_v, v_cache, fp8, rows, dec_box);
     if (ok && !fp8 && !nvfp4)

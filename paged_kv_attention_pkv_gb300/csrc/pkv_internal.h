@@ -39,12 +39,13 @@ constexpr int kDecSmemBytesFp8 =
     kDecWarps * kDecStagesFp8 * kDecStageBytes + 1024 + 256;
 // NVFP4 pools: 64 code bytes + 8 micro-scale bytes per 128-element row;
 // rows of a (block, KV head) tile in groups of min(block_size, 64).  Decode
-// stages hold 64 keys (K and V codes 4 KB each, micro scales 512 B each),
-// two per warp ring, three CTAs per SM.
+// stages hold kDecKeysNvfp4 keys (K and V codes 64 bytes a key, micro scales
+// 8), kDecStagesNvfp4 per warp ring, kDecCtasNvfp4 CTAs per SM.
 constexpr int kNvfp4RowBytes = kHeadDim / 2 + kHeadDim / 16;   // 72
 constexpr int kNvfp4Group = 64;
 constexpr int kDecKeysNvfp4 = 64;
 constexpr int kDecStagesNvfp4 = 2;
+constexpr int kDecCtasNvfp4 = 3;
 constexpr int kDecStageBytesNvfp4 = 2 * kDecKeysNvfp4 * kNvfp4RowBytes;   // 9216
 constexpr int kDecSmemBytesNvfp4 =
     kDecWarps * kDecStagesNvfp4 * kDecStageBytesNvfp4 + 1024 + 256;
