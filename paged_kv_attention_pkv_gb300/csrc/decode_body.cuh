@@ -346,15 +346,16 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       break;
     }
     const int key0 = kb + (warp + i * kDecWarps) * KS;
+    const int gkey0 = global_key(p, key0);
     const uint32_t kbase = smem_addr(ring + slot * kDecStageBytes);
     const uint32_t vbase = kbase + Tile::kKBytes;
+    // ---- S^T = K Q^T, 16 keys x 8 columns per sub-tile; the sub-tiles'
+    // MMA chains are independent, then one softmax step covers the stage
+    float s[Tile::kSubs][4];
 #pragma unroll
     for (int sub = 0; sub < Tile::kSubs; ++sub) {
-      const int k16 = key0 + 16 * sub;
-      if (k16 >= ke) break;
-      const int g16 = global_key(p, key0) + 16 * sub;   // global key of k16
-      // ---- S^T = K Q^T for 16 keys x 8 columns
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
+      s[sub][0] = s[sub][1] = s[sub][2] = s[sub][3] = 0.f;
+      if (key0 + 16 * sub >= ke) continue;
       if constexpr (FP8) {
         // raw K codes straight into FP8 MMAs: thread t's 16 bytes of a row
         // are steps 2h, 2h+1 (words 0,1 -> a0,a2 of step 2h; 2,3 of 2h+1)
@@ -362,10 +363,10 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
         for (int h = 0; h < 2; ++h) {
           const uint4 x = lds128(kbase + swz128(16 * sub + g, 2 * t + h));
           const uint4 y = lds128(kbase + swz128(16 * sub + g + 8, 2 * t + h));
-          mma_e4m3(s, x.x, y.x, x.y, y.y, qf[2 * h][0], qf[2 * h][1]);
-          mma_e4m3(s, x.x, y.x, x.y, y.y, qf[4 + 2 * h][0], qf[4 + 2 * h][1]);
-          mma_e4m3(s, x.z, y.z, x.w, y.w, qf[2 * h + 1][0], qf[2 * h + 1][1]);
-          mma_e4m3(s, x.z, y.z, x.w, y.w, qf[4 + 2 * h + 1][0], qf[4 + 2 * h + 1][1]);
+          mma_e4m3(s[sub], x.x, y.x, x.y, y.y, qf[2 * h][0], qf[2 * h][1]);
+          mma_e4m3(s[sub], x.x, y.x, x.y, y.y, qf[4 + 2 * h][0], qf[4 + 2 * h][1]);
+          mma_e4m3(s[sub], x.z, y.z, x.w, y.w, qf[2 * h + 1][0], qf[2 * h + 1][1]);
+          mma_e4m3(s[sub], x.z, y.z, x.w, y.w, qf[4 + 2 * h + 1][0], qf[4 + 2 * h + 1][1]);
         }
       } else {
 #pragma unroll
@@ -374,49 +375,59 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
           const uint32_t ch = 2 * t + (L & 1);
           const uint4 x = lds128(kbase + off + swz128(g, ch));
           const uint4 y = lds128(kbase + off + swz128(g + 8, ch));
-          mma_bf16(s, x.x, y.x, x.y, y.y, qf[2 * L][0], qf[2 * L][1]);
-          mma_bf16(s, x.z, y.z, x.w, y.w, qf[2 * L + 1][0], qf[2 * L + 1][1]);
+          mma_bf16(s[sub], x.x, y.x, x.y, y.y, qf[2 * L][0], qf[2 * L][1]);
+          mma_bf16(s[sub], x.z, y.z, x.w, y.w, qf[2 * L + 1][0], qf[2 * L + 1][1]);
         }
       }
-      // ---- scale, mask, online softmax per column
+    }
+    // ---- scale, mask (validity on item-local keys, causality on global
+    // positions), online softmax per column over the stage
+    float tm0 = -CUDART_INF_F, tm1 = -CUDART_INF_F;
+#pragma unroll
+    for (int sub = 0; sub < Tile::kSubs; ++sub) {
       float sc0 = p.scale_log2, sc1 = p.scale_log2;
-      float pv_scale = 1.f;
       if constexpr (FP8) {
         sc0 *= sk_sub[sub] * inv_sq0;
         sc1 *= sk_sub[sub] * inv_sq1;
-        pv_scale = sv_sub[sub];
       }
-      // validity on item-local keys, causality on global positions
-      const int kr0 = k16 + g, kr1 = k16 + g + 8;
-      const int gr0 = g16 + g, gr1 = g16 + g + 8;
-      s[0] = (kr0 < ke && gr0 <= pos0) ? s[0] * sc0 : -CUDART_INF_F;
-      s[1] = (kr0 < ke && gr0 <= pos1) ? s[1] * sc1 : -CUDART_INF_F;
-      s[2] = (kr1 < ke && gr1 <= pos0) ? s[2] * sc0 : -CUDART_INF_F;
-      s[3] = (kr1 < ke && gr1 <= pos1) ? s[3] * sc1 : -CUDART_INF_F;
-      float tm0 = fmaxf(s[0], s[2]);
-      float tm1 = fmaxf(s[1], s[3]);
+      const int kr0 = key0 + 16 * sub + g, kr1 = kr0 + 8;
+      const int gr0 = gkey0 + 16 * sub + g, gr1 = gr0 + 8;
+      s[sub][0] = (kr0 < ke && gr0 <= pos0) ? s[sub][0] * sc0 : -CUDART_INF_F;
+      s[sub][1] = (kr0 < ke && gr0 <= pos1) ? s[sub][1] * sc1 : -CUDART_INF_F;
+      s[sub][2] = (kr1 < ke && gr1 <= pos0) ? s[sub][2] * sc0 : -CUDART_INF_F;
+      s[sub][3] = (kr1 < ke && gr1 <= pos1) ? s[sub][3] * sc1 : -CUDART_INF_F;
+      tm0 = fmaxf(tm0, fmaxf(s[sub][0], s[sub][2]));
+      tm1 = fmaxf(tm1, fmaxf(s[sub][1], s[sub][3]));
+    }
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
-        tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
-      }
-      const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
-      const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
-      const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-      const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-      const float p0 = exp2f(s[0] - mu0), p1 = exp2f(s[1] - mu1);
-      const float p2 = exp2f(s[2] - mu0), p3 = exp2f(s[3] - mu1);
-      l0 = l0 * al0 + p0 + p2;
-      l1 = l1 * al1 + p1 + p3;
-      m0 = mn0;
-      m1 = mn1;
+    for (int o = 4; o < 32; o <<= 1) {
+      tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
+      tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
+    }
+    const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
+    const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+    const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+    const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+    m0 = mn0;
+    m1 = mn1;
+    l0 *= al0;
+    l1 *= al1;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        acc[mt][0] *= al0;
-        acc[mt][1] *= al1;
-        acc[mt][2] *= al0;
-        acc[mt][3] *= al1;
-      }
+    for (int mt = 0; mt < 8; ++mt) {
+      acc[mt][0] *= al0;
+      acc[mt][1] *= al1;
+      acc[mt][2] *= al0;
+      acc[mt][3] *= al1;
+    }
+#pragma unroll
+    for (int sub = 0; sub < Tile::kSubs; ++sub) {
+      const int k16 = key0 + 16 * sub;
+      if (k16 >= ke) break;
+      const float p0 = exp2f(s[sub][0] - mu0), p1 = exp2f(s[sub][1] - mu1);
+      const float p2 = exp2f(s[sub][2] - mu0), p3 = exp2f(s[sub][3] - mu1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      const float pv_scale = FP8 ? sv_sub[sub] : 1.f;
       // ---- P^T as the B operand: transpose the two 8x8 halves in registers
       // (f16 for E4M3 pools, whose V is unpacked to f16; bf16 otherwise)
       const uint32_t b0 = movmatrix_trans(FP8 ? pack_f16(p0 * pv_scale, p1 * pv_scale)

@@ -4,6 +4,8 @@ Small cases compare every output row; the five workloads run at full size
 and compare sampled rows the oracle computes one by one (always including
 the first and last rows of each sequence and rows at tile boundaries).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -218,10 +220,20 @@ def test_fp8_long_decode_full_size():
     _sampled(b, [int(L.argmin())], [0, 5], what="c5")
 
 
+def test_nvfp4_long_decode_full_size():
+    """The long-context decode with NVFP4 KV as bench.py times it: the
+    shortest and the longest request, two KV heads each."""
+    full = W.config_spec(4)
+    b = W.generate(dataclasses.replace(full, kv_dtype="nvfp4"), DEV)
+    L = b.seq_lens
+    _sampled(b, [int(L.argmin()), int(L.argmax())], [0, 5], what="c5 nvfp4")
+
+
 # ---- invariances -------------------------------------------------------------------
 
-def test_block_permutation_is_bitwise_invariant():
-    s = spec("perm", 32, 8, 16, [1, 70, 1], [3000, 500, 77])
+@pytest.mark.parametrize("kv", ["bf16", "nvfp4"])
+def test_block_permutation_is_bitwise_invariant(kv):
+    s = spec("perm", 32, 8, 16, [1, 70, 1], [3000, 500, 77], kv=kv)
     b = W.generate(s, DEV)
     out1, lse1 = U.gpu_step(b, append=True)
     perm = torch.randperm(b.num_blocks, generator=torch.Generator().manual_seed(5))
@@ -231,6 +243,11 @@ def test_block_permutation_is_bitwise_invariant():
     kc[pd] = b.k_cache
     vc[pd] = b.v_cache
     b.k_cache, b.v_cache = kc, vc
+    if b.k_scale is not None:
+        ks, vs = torch.empty_like(b.k_scale), torch.empty_like(b.v_scale)
+        ks[pd] = b.k_scale
+        vs[pd] = b.v_scale
+        b.k_scale, b.v_scale = ks, vs
     b.block_tables = perm.numpy()[b.block_tables].astype(np.int32)
     out2, lse2 = U.gpu_step(b, append=False)
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
