@@ -114,3 +114,16 @@ def test_partial_refuses_prefill_rows_and_bad_interleave():
         h2.attention_partial(*args2, 2, 2, 16)
     h.close()
     h2.close()
+    # NVFP4 stages are 64 keys: an interleave of 32 is refused, 64 accepted
+    b3 = W.generate(W.custom_spec("dcp_bad3", 32, 8, 16, [1, 1], [100, 200], seed=3,
+                                  kv_dtype="nvfp4"), DEV)
+    h3 = U.make_handle(b3)
+    m3 = U.device_meta(b3)
+    args3 = (b3.q, b3.k_cache, b3.v_cache, m3["qsl"], m3["lens"], m3["bt"], b3.qsl,
+             b3.seq_lens)
+    with pytest.raises(pkv.PkvError) as e:
+        h3.attention_partial(*args3, 0, 2, 32, k_scale=b3.k_scale, v_scale=b3.v_scale)
+    assert "interleave" in str(e.value)
+    h3.attention_partial(*args3, 0, 2, 64, k_scale=b3.k_scale, v_scale=b3.v_scale)
+    torch.cuda.synchronize()
+    h3.close()

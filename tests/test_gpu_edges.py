@@ -18,10 +18,12 @@ def spec(name, hq, hkv, bs, q_lens, seq_lens, kv="bf16", seed=17):
     return W.custom_spec(name, hq, hkv, bs, q_lens, seq_lens, seed=seed, kv_dtype=kv)
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "nvfp4"])
 def test_block_size_256(kv):
-    ql = [1, 1, 300] if kv == "bf16" else [1, 1, 1]
-    b = W.generate(spec(f"bs256_{kv}", 32, 8, 256, ql, [255, 1000, 900]), DEV)
+    """The largest blocks (NVFP4: four 64-row groups per block), with a
+    300-token prefill (tensor-core tiles for bf16, 8-row decode-kernel
+    chunks otherwise)."""
+    b = W.generate(spec(f"bs256_{kv}", 32, 8, 256, [1, 1, 300], [255, 1000, 900], kv=kv), DEV)
     U.full_parity(b, what=f"bs256 {kv}")
 
 

@@ -16,21 +16,25 @@ DEV = "cuda"
 def _batch(kind):
     if kind == "mixed":     # decodes and a prefill chunk: one mixed launch
         s = W.custom_spec("graph_mixed", 32, 8, 16, [1, 1, 130, 1], [500, 3000, 1200, 64], seed=11)
+    elif kind == "nvfp4":   # NVFP4 pools: decodes and a chunked prefill
+        s = W.custom_spec("graph_nvfp4", 32, 8, 16, [1, 1, 30, 1], [500, 3000, 1200, 64], seed=13,
+                          kv_dtype="nvfp4")
     else:                   # decodes only
         s = W.custom_spec("graph_decode", 32, 8, 16, [1] * 6, [100, 5000, 20000, 17, 333, 4096], seed=12)
     return W.generate(s, DEV)
 
 
-@pytest.mark.parametrize("kind", ["mixed", "decode"])
+@pytest.mark.parametrize("kind", ["mixed", "decode", "nvfp4"])
 def test_captured_step_replays_like_eager(kind):
     b = _batch(kind)
     h = U.make_handle(b, flags=pkv.FLAG_VALIDATE)
     m = U.device_meta(b)
 
     def step(out, lse):
-        h.write_slots(b.k_new, b.v_new, m["slots"], b.k_cache, b.v_cache)
+        h.write_slots(b.k_new, b.v_new, m["slots"], b.k_cache, b.v_cache, b.k_scale, b.v_scale)
         h.attention_varlen(b.q, b.k_cache, b.v_cache, m["qsl"], m["lens"], m["bt"],
-                           b.qsl, b.seq_lens, out=out, lse=lse)
+                           b.qsl, b.seq_lens, out=out, lse=lse, k_scale=b.k_scale,
+                           v_scale=b.v_scale)
 
     T, Hq = b.q.shape[0], b.q.shape[1]
     out_e = torch.empty_like(b.q)
@@ -61,7 +65,7 @@ def test_captured_step_replays_like_eager(kind):
     sub = W.subset(b, list(range(b.spec.num_seqs)))
     ref, ref_lse = U.oracle_subset(sub, b.spec)
     got, got_lse = U.gpu_rows(out_g, lse_g, sub)
-    U.check(got, ref, got_lse, ref_lse, "bf16", f"graph_{kind}")
+    U.check(got, ref, got_lse, ref_lse, b.spec.kv_dtype, f"graph_{kind}")
     h.close()
 
 

@@ -308,8 +308,9 @@ def test_zeros_fail_the_checks():
 
 # ---- validate mode and API errors on the device ----------------------------------------
 
-def test_validate_mode_reports_bad_block_ids():
-    s = spec("badblk", 8, 2, 16, [1, 5], [40, 60])
+@pytest.mark.parametrize("kv", ["bf16", "nvfp4"])
+def test_validate_mode_reports_bad_block_ids(kv):
+    s = spec("badblk", 8, 2, 16, [1, 5], [40, 60], kv=kv)
     b = W.generate(s, DEV)
     b.block_tables[0, 1] = b.num_blocks + 5      # outside the pool
     h = U.make_handle(b)
