@@ -661,9 +661,9 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
                           encode_nvfp4_map(&h->dec_v, v_cache, rows / 8 * 9, nv_box)
                     : encode_pool_map(&h->dec_k, k_cache, fp8, rows, dec_box) &&
                           encode_pool_map(&h->dec_v, v_cache, fp8, rows, dec_box);
-    if (ok && !fp8 && !nvfp4)
-      ok = encode_pool_map(&h->pf_k, k_cache, false, rows, pf_box) &&
-           encode_pool_map(&h->pf_v, v_cache, false, rows, pf_box);
+    if (ok && !nvfp4)
+      ok = encode_pool_map(&h->pf_k, k_cache, fp8, rows, pf_box) &&
+           encode_pool_map(&h->pf_v, v_cache, fp8, rows, pf_box);
     if (!ok) {
       h->map_k_ptr = h->map_v_ptr = nullptr;
       return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled rejected the pool layout");
@@ -747,6 +747,8 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   pp.q = static_cast<const __nv_bfloat16 *>(q);
   pp.block_tables = block_tables;
   pp.bt_stride = block_table_stride;
+  pp.k_scale = k_scale;
+  pp.v_scale = v_scale;
   pp.out = static_cast<__nv_bfloat16 *>(out);
   pp.lse = lse;
   pp.err = h->d_err;
@@ -764,7 +766,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled rejected the query layout");
   const int n_dec = static_cast<int>(plan.dec.size());
   const int n_pre = static_cast<int>(plan.pre.size());
-  if (n_dec > 0 && n_pre > 0 && tc && !(c.flags & PKV_FLAG_SEPARATE)) {
+  if (n_dec > 0 && n_pre > 0 && tc && !fp8 && !(c.flags & PKV_FLAG_SEPARATE)) {
     // a mixed step: one launch for both kinds of work
     timing_begin(h, PKV_KERNEL_MIXED, s);
     e = launch_mixed(qmap, h->pf_k, h->pf_v, h->dec_k, h->dec_v, pp, dp, n_pre, n_dec, s);
@@ -780,7 +782,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   }
   if (n_pre > 0) {
     timing_begin(h, PKV_KERNEL_PREFILL, s);
-    e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, pp, n_pre, s);
+    e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, pp, n_pre, fp8, s);
     timing_end(h, PKV_KERNEL_PREFILL, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
   }

@@ -365,6 +365,19 @@ __device__ __forceinline__ void tc_mma_acc(uint32_t d_tmem, uint64_t a_desc, uin
                "l"(a_desc), "l"(b_desc), "r"(idesc)
                : "memory");
 }
+// kind::f8f6f4 with E4M3 A and B (instruction descriptor idesc_e4m3).
+__device__ __forceinline__ void tc_mma8_first(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, 0;" ::"r"(d_tmem),
+               "l"(a_desc), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma8_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+               "l"(a_desc), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
 __device__ __forceinline__ void tc_mma_tmem_a_acc(uint32_t d_tmem, uint32_t a_tmem,
                                                   uint64_t b_desc, uint32_t idesc) {
   asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
@@ -511,6 +524,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int a_mn, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn) << 15) |
          (uint32_t(b_mn) << 16) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+// kind::f16 with f16 A and B (format fields 0), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, int a_mn, int b_mn) {
+  return (1u << 4) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
+         (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+// kind::f8f6f4 with E4M3 A and B (format fields 0), both K-major, fp32 D.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
+  return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 
 }  // namespace pkv

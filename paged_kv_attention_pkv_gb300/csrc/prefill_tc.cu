@@ -36,6 +36,7 @@
 namespace pkv {
 namespace {
 
+template <bool FP8>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
@@ -44,29 +45,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  prefill_tc_item(qmap, kmap, vmap, p, p.items[blockIdx.x], smem);
+  prefill_tc_item<FP8>(qmap, kmap, vmap, p, p.items[blockIdx.x], smem);
+}
+
+template <bool FP8>
+cudaError_t configure_one() {
+  // setmaxnreg moves registers within the CTA's launch allotment: the split
+  // must not ask for more than the kernel was compiled (and launched) with
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<FP8>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * kTcThreads < static_cast<int>(2 * 128 * kRegsSoftmax + 128 * kRegsCtl))
+    return cudaErrorInvalidConfiguration;
+  return cudaFuncSetAttribute(prefill_tc_kernel<FP8>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p,
-                              int num_items, cudaStream_t s) {
+                              int num_items, bool fp8, cudaStream_t s) {
   if (num_items == 0) return cudaSuccess;
-  prefill_tc_kernel<<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap, vmap, p);
+  if (fp8)
+    prefill_tc_kernel<true><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap, vmap, p);
+  else
+    prefill_tc_kernel<false><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap, vmap, p);
   return cudaGetLastError();
 }
 
 cudaError_t configure_prefill_tc() {
-  // setmaxnreg moves registers within the CTA's launch allotment: the split
-  // must not ask for more than the kernel was compiled (and launched) with
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs * kTcThreads < static_cast<int>(2 * 128 * kRegsSoftmax + 128 * kRegsCtl))
-    return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kTcSmemBytes);
+  cudaError_t e = configure_one<false>();
+  return e != cudaSuccess ? e : configure_one<true>();
 }
 
 }  // namespace pkv

@@ -32,10 +32,23 @@ constexpr uint32_t kOffK = 2 * kTile;             // kKst K tiles
 constexpr uint32_t kOffV = kOffK + kKst * kTile;  // kVst V tiles
 constexpr uint32_t kOffBar = kOffV + kVst * kTile;   // 229376
 static_assert(kOffBar == 229376, "Q, K and V tiles fill 224 KB");
+// E4M3 pools: K tiles stay E4M3 (16 KB: 128 keys x 128 bytes) and feed FP8
+// MMAs; V tiles arrive as E4M3 in a 2-deep staging ring and are converted to
+// f16 (times their block scale) into the same 32 KB V ring.
+constexpr uint32_t kTile8 = 128 * 128;
+constexpr uint32_t kOffK8 = 2 * kTile;
+constexpr uint32_t kOffVs8 = kOffK8 + kKst * kTile8;
+constexpr uint32_t kOffV8 = kOffVs8 + 2 * kTile8;
+static_assert(kOffV8 + kVst * kTile == kOffBar, "the E4M3 layout fills the same 224 KB");
+// per-tile block scales (K of 8 key groups of 16, then V), a ring of 8 tiles
+constexpr uint32_t kOffScales = kOffBar + 256;
+constexpr int kScaleRing = 8;
 constexpr uint32_t kTmemCols = 512;               // S0, S1, O0, O1
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);
 constexpr uint32_t kIdescQK64 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 0, 1);
+constexpr uint32_t kIdescQK8 = idesc_e4m3(128, 128);
+constexpr uint32_t kIdescPV16 = idesc_f16(128, 128, 0, 1);
 constexpr float kRescaleThreshold = 8.f;          // log2 units
 
 __device__ __forceinline__ float ex2(float x) {
@@ -83,7 +96,9 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 }
 
 // One prefill work item processed by all kTcThreads threads of the CTA;
-// `smem` is 1024-byte aligned (kTcSmemBytes - 1024 bytes).
+// `smem` is 1024-byte aligned (kTcSmemBytes - 1024 bytes).  FP8: the pools
+// hold E4M3 codes with one fp32 scale per (block, KV head).
+template <bool FP8>
 __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
                                                 const CUtensorMap &kmap,
                                                 const CUtensorMap &vmap,
@@ -99,6 +114,13 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
   uint64_t *p_full = s_full + 2;             // [2]
   uint64_t *o_done = p_full + 2;             // [2]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_done + 2);
+  // E4M3 pools only
+  uint64_t *q_ready = o_done + 3;            // [2] Q tile t converted
+  uint64_t *vs_full = q_ready + 2;           // [2] E4M3 V staging loaded
+  uint64_t *vs_empty = vs_full + 2;          // [2] ... and converted
+  uint64_t *sc_ready = vs_empty + 2;         // [kScaleRing] tile scales written
+  float *scales = reinterpret_cast<float *>(smem + kOffScales);   // [ring][16]
+  static_assert(8 * (17 + 1 + 2 + 2 + 2 + kScaleRing) <= 256, "barriers fit their 256 bytes");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -124,13 +146,21 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < kVst; ++i) {
-      mbar_init(&v_full[i], 1);
+      mbar_init(&v_full[i], FP8 ? 2 : 1);   // FP8: the two converter warps
       mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
+    }
+    if (FP8) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&q_ready[i], 128);
+        mbar_init(&vs_full[i], 1);
+        mbar_init(&vs_empty[i], 2);
+      }
+      for (int i = 0; i < kScaleRing; ++i) mbar_init(&sc_ready[i], 1);
     }
     prefetch_tmap(&qmap);
     prefetch_tmap(&kmap);
@@ -145,7 +175,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
 
   if (warp >= 8) {
    setmaxnreg_dec<kRegsCtl>();
-   if (warp == 9 || warp == 10) {
+   if (!FP8 && (warp == 9 || warp == 10)) {
     // ---------------- TMA producers: warp 9 loads Q and K, warp 10 V ----
     // Each ring is filled in tile order; K_j waits for the QKs of tile
     // j - kKst, V_j for the PVs of tile j - kVst.  Small blocks take one box
@@ -209,10 +239,155 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       }
       y_cur = y_next;
     }
+   } else if (FP8 && warp == 9) {
+    // ---------------- TMA producer, E4M3 pools: Q, the E4M3 K ring, the
+    // E4M3 V staging ring (one box per block, no column halves), and each
+    // tile's block scales for the softmax and the converters ----
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
+    const int br = p.bs < 128 ? p.bs : 128;
+    const int nbox = 128 / br;  // <= 8
+    // lane b < nbox: pool row of box b of tile j, and its block's scales
+    auto tile_info = [&](int j, float &sk, float &sv) {
+      const int key = j * 128 + lane * br;
+      int32_t y = p.rows_total;
+      sk = sv = 1.f;
+      if (lane < nbox && j < n_tiles && key < k_end) {
+        const int32_t blk = __ldg(bt + key / p.bs);
+        if (blk >= 0 && blk < p.num_blocks) {
+          y = (blk * p.hkv + it.kv_head) * p.bs + key % p.bs;
+          const int64_t si = static_cast<int64_t>(blk) * p.hkv + it.kv_head;
+          sk = __ldg(p.k_scale + si);
+          sv = __ldg(p.v_scale + si);
+        } else {
+          record_error(p.err, kErrBadBlock);
+        }
+      }
+      return y;
+    };
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, (two ? 2 : 1) * 2 * R * 128);
+      const int t0 = it.tok0 + it.row0 / G;
+      tma_load_3d(smem + kOffQ, &qmap, 0, it.kv_head * G, t0, q_full);
+      tma_load_3d(smem + kOffQ + kHalf, &qmap, 64, it.kv_head * G, t0, q_full);
+      if (two) {
+        const int t1 = t0 + 128 / G;
+        tma_load_3d(smem + kOffQ + kTile, &qmap, 0, it.kv_head * G, t1, q_full);
+        tma_load_3d(smem + kOffQ + kTile + kHalf, &qmap, 64, it.kv_head * G, t1, q_full);
+      }
+    }
+    float sk_cur, sv_cur;
+    int32_t y_cur = tile_info(0, sk_cur, sv_cur);
+    for (int j = 0; j < n_tiles; ++j) {
+      float sk_nxt, sv_nxt;
+      const int32_t y_next = tile_info(j + 1, sk_nxt, sv_nxt);
+      // scales of the tile's 8 key groups of 16 (group g lies in box g*16/br)
+      const int gb = (lane * 16 / br) & 31;
+      const float gk = __shfl_sync(0xffffffffu, sk_cur, gb);
+      const float gv = __shfl_sync(0xffffffffu, sv_cur, gb);
+      if (lane < 8) {
+        scales[(j % kScaleRing) * 16 + lane] = gk;
+        scales[(j % kScaleRing) * 16 + 8 + lane] = gv;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sc_ready[j % kScaleRing]);
+      int n = 0;
+      for (int r = 0; r < 128; r += br)
+        if (j * 128 + r < k_end) ++n;
+      // K tile j once the QKs of tile j - kKst are done
+      const int s = j % kKst;
+      if (j >= kKst &&
+          !__all_sync(0xffffffffu, mbar_wait(&k_empty[s], ((j / kKst) - 1) & 1))) {
+        if (lane == 0) record_error(p.err, kErrTimeout);
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&k_full[s], n * br * 128);
+      for (int bx = 0; bx < n; ++bx) {
+        const int32_t y = __shfl_sync(0xffffffffu, y_cur, bx);
+        if (lane == 0)
+          tma_load_2d(smem + kOffK8 + s * kTile8 + bx * br * 128, &kmap, 0, y, &k_full[s]);
+      }
+      // V tile j into staging j & 1 once the converters are done with j - 2
+      const int v2 = j & 1;
+      if (j >= 2 &&
+          !__all_sync(0xffffffffu, mbar_wait(&vs_empty[v2], ((j >> 1) - 1) & 1))) {
+        if (lane == 0) record_error(p.err, kErrTimeout);
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&vs_full[v2], n * br * 128);
+      for (int bx = 0; bx < n; ++bx) {
+        const int32_t y = __shfl_sync(0xffffffffu, y_cur, bx);
+        if (lane == 0)
+          tma_load_2d(smem + kOffVs8 + v2 * kTile8 + bx * br * 128, &vmap, 0, y, &vs_full[v2]);
+      }
+      y_cur = y_next;
+      sk_cur = sk_nxt;
+      sv_cur = sv_nxt;
+    }
+   } else if (FP8 && warp >= 10) {
+    // ---------------- V converters, E4M3 pools: staging -> f16 V ring ----
+    // Warp 10 converts key rows 0-63 of a tile, warp 11 rows 64-127; lane l
+    // takes rows l and l + 32 of its half (8 consecutive rows per 8-lane
+    // phase, which the 128-byte swizzle spreads over all banks).  Codes
+    // become f16 exactly; the multiply by the block scale rounds once.
+    // Rows past the item's last key are written as zeros (PV multiplies them
+    // by P = 0, and stale bytes could be NaN).
+    const int rbase = (warp - 10) * 64;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int v2 = j & 1;
+      const int s = j % kVst;
+      bool wok = mbar_wait(&vs_full[v2], (j >> 1) & 1);
+      if (wok && j >= kVst) wok = mbar_wait(&v_empty[s], ((j / kVst) - 1) & 1);
+      if (wok) wok = mbar_wait(&sc_ready[j % kScaleRing], (j / kScaleRing) & 1);
+      if (!__all_sync(0xffffffffu, wok)) {
+        if (lane == 0) record_error(p.err, kErrTimeout);
+        break;
+      }
+      const uint32_t src = smem_addr(smem + kOffVs8 + v2 * kTile8);
+      const uint32_t dst = smem_addr(smem + kOffV8 + s * kTile);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int k = rbase + lane + 32 * i;   // key row in the tile
+        const uint32_t sw = k & 7;
+        if (j * 128 + k >= k_end) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              sts128(dst + h * kHalf + k * 128 + ((c ^ sw) << 4), 0u, 0u, 0u, 0u);
+          continue;
+        }
+        const float sv = scales[(j % kScaleRing) * 16 + 8 + (k >> 4)];
+        const uint32_t sv2 = pack_f16(sv, sv);
+#pragma unroll
+        for (int oc = 0; oc < 8; ++oc) {   // head dims 16 oc .. 16 oc + 15
+          const uint4 x = lds128(src + k * 128 + ((oc ^ sw) << 4));
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            o[2 * q] = hmul2(e4m3x2lo_to_f16x2(w[q]), sv2);
+            o[2 * q + 1] = hmul2(e4m3x2hi_to_f16x2(w[q]), sv2);
+          }
+          // f16 chunks 2(oc & 3) and 2(oc & 3) + 1 of column half oc >> 2
+          const uint32_t hb = dst + (oc >> 2) * kHalf + k * 128;
+          const uint32_t c0 = 2 * (oc & 3);
+          sts128(hb + ((c0 ^ sw) << 4), o[0], o[1], o[2], o[3]);
+          sts128(hb + (((c0 + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
+        }
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&v_full[s]);
+        mbar_arrive(&vs_empty[v2]);
+      }
+    }
    } else if (warp == 8) {
     // ---------------- MMA issuer (one thread) ----------------
     if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0);
+      // E4M3 pools: the softmax warps turn Q tile t into E4M3 hi/lo parts
+      bool ok = FP8 ? mbar_wait(&q_ready[0], 0) : mbar_wait(q_full, 0);
+      if (FP8) tc_fence_after();
       // Descriptors are built once; tiles, stages and k-steps add constant
       // offsets to the start-address field (addresses stay < 256 KB, so the
       // 14-bit field never carries).  The issuing warp shares its SM
@@ -220,23 +395,42 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       // between MMA groups is time the tensor pipe may sit idle.
       constexpr uint64_t kTileDesc = kTile >> 4;
       const uint64_t qd0 = smem_desc_sw128(smem_addr(smem + kOffQ), 16, 1024);
-      const uint64_t kd0 = smem_desc_sw128(smem_addr(smem + kOffK), 16, 1024);
-      const uint64_t vd0 = smem_desc_sw128(smem_addr(smem + kOffV), kHalf, 1024);
+      const uint64_t kd0 = smem_desc_sw128(smem_addr(smem + (FP8 ? kOffK8 : kOffK)), 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(smem_addr(smem + (FP8 ? kOffV8 : kOffV)), kHalf, 1024);
       auto qk = [&](int t, int j) {   // S_t = Q_t K_j^T
         const int s = j & (kKst - 1);
         // K arrives by TMA (async proxy, like the MMA): the mbarrier alone
         // orders it
         if (!mbar_wait(&k_full[s], (j / kKst) & 1)) return false;
         const uint64_t a0 = qd0 + t * kTileDesc;
-        const uint64_t b0 = kd0 + s * kTileDesc;
         const uint32_t d = tmem + t * 128;
+        if constexpr (FP8) {
+          // S = (Q_hi + Q_lo) K^T: E4M3 K codes, four 32-byte k-steps per part
+          // (Q_hi in the tile's first half, Q_lo in its second)
+          const uint64_t b0 = kd0 + s * (kTile8 >> 4);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t off = ((ks >> 2) * kHalf + (ks & 3) * 32) >> 4;
-          if (ks == 0)
-            tc_mma_first(d, a0, b0, kIdescQK);
-          else
-            tc_mma_acc(d, a0 + off, b0 + off, kIdescQK);
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t off = (ks * 32) >> 4;
+            if (ks == 0)
+              tc_mma8_first(d, a0, b0, kIdescQK8);
+            else
+              tc_mma8_acc(d, a0 + off, b0 + off, kIdescQK8);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t off = (ks * 32) >> 4;
+            tc_mma8_acc(d, a0 + (kHalf >> 4) + off, b0 + off, kIdescQK8);
+          }
+        } else {
+          const uint64_t b0 = kd0 + s * kTileDesc;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t off = ((ks >> 2) * kHalf + (ks & 3) * 32) >> 4;
+            if (ks == 0)
+              tc_mma_first(d, a0, b0, kIdescQK);
+            else
+              tc_mma_acc(d, a0 + off, b0 + off, kIdescQK);
+          }
         }
         tc_commit(&s_full[t]);
         return true;
@@ -251,15 +445,19 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t bd = b0 + ((kk * 2048) >> 4);
           if (kk > 0)
-            tc_mma_tmem_a_acc(dO, aP + kk * 8, bd, kIdescPV);
+            tc_mma_tmem_a_acc(dO, aP + kk * 8, bd, FP8 ? kIdescPV16 : kIdescPV);
           else
-            tc_mma_tmem_a(dO, aP, bd, kIdescPV, j > 0 ? 1u : 0u);
+            tc_mma_tmem_a(dO, aP, bd, FP8 ? kIdescPV16 : kIdescPV, j > 0 ? 1u : 0u);
         }
         tc_commit(&o_done[t]);
         return true;
       };
       // prologue: QK of tile 0 for both Q tiles
       if (ok) ok = qk(0, 0);
+      if (FP8 && ok && two) {
+        ok = mbar_wait(&q_ready[1], 0);
+        tc_fence_after();
+      }
       if (ok && two) ok = qk(1, 0);
       if (ok) tc_commit(&k_empty[0]);
       // P_t(j) lives where QK_t(j+1) writes: QK_t(j+1) is issued after
@@ -300,10 +498,65 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     const int rowg = it.row0 + R * t + r;
     const bool row_ok = r < nrow;
     const int pos = it.hist + rowg / G;   // padded rows see every key
-    const float c = p.scale_log2;
+    float c = p.scale_log2;
     float m = -CUDART_INF_F;              // running max, log2 units
     float l = 0.f;
     bool ok = true;
+    if (FP8 && ntl > 0) {
+      // E4M3 pools: this thread's Q row, scaled by a power of two sq (largest
+      // |q sq| in [128, 256)), becomes hi + lo, both E4M3 (about bf16
+      // precision), written in place over the row: hi into the tile's first
+      // 128-byte half, lo into its second (each the 128B-swizzled K-major
+      // layout of a 128 x 128 E4M3 tile).  1/sq goes into this row's scale.
+      ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0));
+      if (ok) {
+        const uint32_t qt = smem_addr(smem + kOffQ + t * kTile);
+        const uint32_t sw = r & 7;
+        uint32_t w[64];   // bf16 pairs: dims 2i, 2i + 1 in w[i]
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            const uint4 v = lds128(qt + h * kHalf + r * 128 + ((cc ^ sw) << 4));
+            w[32 * h + 4 * cc] = v.x;
+            w[32 * h + 4 * cc + 1] = v.y;
+            w[32 * h + 4 * cc + 2] = v.z;
+            w[32 * h + 4 * cc + 3] = v.w;
+          }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          amax = fmax3(amax, fabsf(__uint_as_float(w[i] << 16)),
+                       fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+        const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
+        const int k2 = 7 - e < 126 ? 7 - e : 126;
+        const float sq = __uint_as_float(static_cast<uint32_t>(127 + k2) << 23);
+        c *= __uint_as_float(static_cast<uint32_t>(127 - k2) << 23);
+#pragma unroll
+        for (int oc = 0; oc < 8; ++oc) {   // 16 dims: words 8 oc .. 8 oc + 7
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t hc[2], lc[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const uint32_t wv = w[8 * oc + 2 * q + u];
+              const float x0 = __uint_as_float(wv << 16) * sq;
+              const float x1 = __uint_as_float(wv & 0xFFFF0000u) * sq;
+              hc[u] = e4m3x2_from_f32(x0, x1);
+              const float2 back = e4m3x2_to_f32(hc[u]);
+              lc[u] = e4m3x2_from_f32(x0 - back.x, x1 - back.y);
+            }
+            hi[q] = hc[0] | (hc[1] << 16);
+            lo[q] = lc[0] | (lc[1] << 16);
+          }
+          sts128(qt + r * 128 + ((oc ^ sw) << 4), hi[0], hi[1], hi[2], hi[3]);
+          sts128(qt + kHalf + r * 128 + ((oc ^ sw) << 4), lo[0], lo[1], lo[2], lo[3]);
+        }
+        fence_proxy_async();
+      }
+      mbar_arrive(&q_ready[t]);
+    }
     // TMEM loads and stores are .sync.aligned: every decision that guards
     // one is warp-uniform (__all_sync / __any_sync).
     for (int j = 0; j < ntl; ++j) {
@@ -323,16 +576,44 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
           s[k] = key > pos ? -CUDART_INF_F : s[k];
         }
       }
-      float mx[8];
+      // E4M3 pools: key group g (16 keys, one block) has its own score
+      // scale c * k_scale (positive), so maxima are taken per group
+      float cg[8];
+      float mt2;
+      if constexpr (FP8) {
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&sc_ready[j % kScaleRing], (j / kScaleRing) & 1))) {
+          ok = false;
+          break;
+        }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[8 + i]);
+        for (int g = 0; g < 8; ++g) cg[g] = c * scales[(j % kScaleRing) * 16 + g];
+        mt2 = -CUDART_INF_F;
 #pragma unroll
-      for (int k = 16; k < 128; k += 16)
+        for (int g = 0; g < 8; ++g) {
+          const float* sg = s + 16 * g;
+          float a = fmax3(sg[0], sg[1], sg[2]);
+          a = fmax3(a, sg[3], sg[4]);
+          a = fmax3(a, sg[5], sg[6]);
+          a = fmax3(a, sg[7], sg[8]);
+          a = fmax3(a, sg[9], sg[10]);
+          a = fmax3(a, sg[11], sg[12]);
+          a = fmax3(a, sg[13], sg[14]);
+          a = fmaxf(a, sg[15]);
+          mt2 = fmaxf(mt2, a * cg[g]);
+        }
+      } else {
+        float mx[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[k + i], s[k + 8 + i]);
-      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                             fmaxf(mx[6], mx[7]));
-      const float mt2 = mt * c;
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[8 + i]);
+#pragma unroll
+        for (int k = 16; k < 128; k += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[k + i], s[k + 8 + i]);
+        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                               fmaxf(mx[6], mx[7]));
+        mt2 = mt * c;
+      }
       float alpha = 1.f;
       bool rescale = false;
       if (mt2 > m + kRescaleThreshold) {
@@ -349,10 +630,12 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           float x0, x1;
-          fma2_bc(x0, x1, s[64 * hh + 2 * k], s[64 * hh + 2 * k + 1], c, -m);
+          fma2_bc(x0, x1, s[64 * hh + 2 * k], s[64 * hh + 2 * k + 1],
+                  FP8 ? cg[(64 * hh + 2 * k) >> 4] : c, -m);
           const float e0 = ex2(x0), e1 = ex2(x1);
           add2(acc[(2 * k) & 7], acc[(2 * k + 1) & 7], e0, e1);
-          pk[k] = pack_bf16(e0, e1);
+          // E4M3 pools run PV in f16 (V converted to f16); bf16 otherwise
+          pk[k] = FP8 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
         }
         tmem_st32u(lane_addr + col_s + 32 * hh, pk);
       }
@@ -376,8 +659,9 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       // The last K/V tile may carry V rows past the item's last key (rows
       // of other requests or never loaded): zero them before any PV reads
       // them.  Q tile 0 does it when it reaches that tile (its PV comes
-      // first), otherwise Q tile 1.
-      if (j == n_tiles - 1 && k_end - key0 < 128 && (t == 0 || nt0 < n_tiles)) {
+      // first), otherwise Q tile 1.  (E4M3 pools: the converters write
+      // those rows as zeros.)
+      if (!FP8 && j == n_tiles - 1 && k_end - key0 < 128 && (t == 0 || nt0 < n_tiles)) {
         const int vvalid = k_end - key0;
         const int vs = j % kVst;
         if (!__all_sync(0xffffffffu, mbar_wait(&v_full[vs], (j / kVst) & 1))) {
@@ -436,7 +720,8 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
 }
 
 
-constexpr uint32_t kTcSmemBytes = kOffBar + 256 + 1024;
+// barriers (256 B), the E4M3 scale ring (8 tiles x 16 fp32), alignment slack
+constexpr uint32_t kTcSmemBytes = kOffScales + kScaleRing * 16 * 4 + 1024;
 
 }  // namespace
 }  // namespace pkv
