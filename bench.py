@@ -60,14 +60,16 @@ CASES = {
     "small-prefill": (2, [4, 5]),             # two post-tool-call sessions
     "small-fp8": (4, [0]),                    # one ~0.6-1M-token FP8 request
     "small-nvfp4": (4, [0, 1]),               # two such requests, NVFP4 KV
+    "small-prefill-fp8": (2, [4, 5]),         # two post-tool-call sessions, E4M3 KV
     "small-mixed": (3, list(range(0, 120, 8)) + [120, 127]),
 }
+CASE_KV = {"small-nvfp4": "nvfp4", "small-prefill-fp8": "fp8"}
 
 
 def case_spec(name: str) -> W.Spec:
     index, seqs = CASES[name]
     full = W.config_spec(index)
-    kv = "nvfp4" if name == "small-nvfp4" else full.kv_dtype
+    kv = CASE_KV.get(name, full.kv_dtype)
     return W.Spec(f"{full.name}[{name}]", full.hq, full.hkv, full.block_size,
                   kv, [full.q_lens[i] for i in seqs],
                   [full.seq_lens[i] for i in seqs], full.seed)
