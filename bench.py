@@ -10,7 +10,7 @@ log-sum-exp combine (pkv_attention_varlen).  `value` is algorithmic bytes
 (every context token's K and V once, Q and O, the append's read + write) per
 second over the whole step, all inputs resident in HBM.  Each rank of a
 multi-GPU run (torchrun) processes its own replica (weak scaling).  The
-incremental-prefill (bf16 and E4M3 KV), mixed-step, FP8 and NVFP4 decode
+incremental-prefill (bf16, E4M3 and NVFP4 KV), mixed-step, FP8 and NVFP4 decode
 workloads are reported in `secondary` unless --primary-only is given.
 
 `--impl reference` times the fp64 CPU oracle on the host cores on a bounded
@@ -454,7 +454,9 @@ def secondary(args, world, peaks, device):
                                 kv_dtype="nvfp4")
     fp8_pf = dataclasses.replace(W.config_spec(2), name="c3_fp8_post_tool_prefill",
                                  kv_dtype="fp8")
-    for idx, steps in ((2, 10), (fp8_pf, 10), (3, 10), (4, 50), (nvfp4, 50)):
+    nv_pf = dataclasses.replace(W.config_spec(2), name="c3_nvfp4_post_tool_prefill",
+                                kv_dtype="nvfp4")
+    for idx, steps in ((2, 10), (fp8_pf, 10), (nv_pf, 5), (3, 10), (4, 50), (nvfp4, 50)):
         r = time_workload(idx, steps, 3, world, peaks, device)
         spec, work = r["spec"], r["work"]
         ms_step = r["ms"] / steps
@@ -479,7 +481,8 @@ def secondary(args, world, peaks, device):
             tf = work["prefill_flops"] / (avg * 1e-3) / 1e12
             peak = peaks["bf16_tflops"]
             # E4M3 KV: QK runs as two FP8 MMAs (query hi + lo parts) and PV in
-            # f16, the tensor time of the bf16 kernel: the same bf16 peak applies
+            # f16; NVFP4 KV: both in f16; the tensor time of the bf16 kernel
+            # either way, so the same bf16 peak applies
             ent["prefill"] = {"value": round(tf, 1), "unit": "TFLOP/s", "bound": "tensor",
                               "frac": round(tf / peak, 4), "peak": peak,
                               "peak_source": f"{peaks['source']} (bf16_tflops)",

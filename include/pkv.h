@@ -188,9 +188,9 @@ pkv_status pkv_rope_write_slots(pkv_handle *h, void *q, const void *k_new,
  * (call pkv_write_slots first on the same stream).  A step that needs more
  * workspace than the handle was created for returns PKV_ERR_WORKSPACE.
  * Requests with more than 8 query rows per KV head (q_i * G > 8) run on the
- * tensor-core prefill kernel over bf16 and E4M3 pools with G <= 128; over
- * NVFP4 pools, or with G > 128, the decode kernel takes their rows 8 at a
- * time (same results within tolerance, at memory-bound speed).
+ * tensor-core prefill kernel when G <= 128 (every pool format); with
+ * G > 128 the decode kernel takes their rows 8 at a time (same results within
+ * tolerance, at memory-bound speed).
  */
 pkv_status pkv_attention_varlen(pkv_handle *h, const void *q,
                                 const void *k_cache, const void *v_cache,
@@ -301,7 +301,7 @@ pkv_status pkv_destroy(pkv_handle *h);
  * head g of the group). */
 typedef struct {
     int32_t kind;        /* 0 = decode kernel (decode rows, or a chunk of
-                            8 prefill rows over NVFP4 pools / G > 128),
+                            8 prefill rows when G > 128),
                             1 = tensor-core prefill tile */
     int32_t seq;         /* request index */
     int32_t kv_head;

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   if (static_cast<int>(blockIdx.x) < n_prefill) {
-    prefill_tc_item<false>(qmap, kmap_pf, vmap_pf, pp, pp.items[blockIdx.x], smem);
+    prefill_tc_item<PKV_KV_BF16>(qmap, kmap_pf, vmap_pf, pp, pp.items[blockIdx.x], smem);
   } else {
     if (threadIdx.x >= kMixedDecWarps * 32) return;
     decode_item<false, kMixedDecWarps>(kmap_dec, vmap_dec, dp,

@@ -335,7 +335,8 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
 
 // NVFP4 pool as rows of 64 bytes (code rows and micro-scale rows alike);
 // boxes of one group's code rows, 64-byte swizzled.
-bool encode_nvfp4_map(CUtensorMap *m, const void *base, int64_t rows, int box_rows) {
+bool encode_nvfp4_map(CUtensorMap *m, const void *base, int64_t rows, int box_rows,
+                      bool swizzle = true) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows)};
@@ -343,7 +344,8 @@ bool encode_nvfp4_map(CUtensorMap *m, const void *base, int64_t rows, int box_ro
   const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -661,6 +663,13 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
                           encode_nvfp4_map(&h->dec_v, v_cache, rows / 8 * 9, nv_box)
                     : encode_pool_map(&h->dec_k, k_cache, fp8, rows, dec_box) &&
                           encode_pool_map(&h->dec_v, v_cache, fp8, rows, dec_box);
+    // prefill: NVFP4 boxes are whole row groups (codes then micro scales,
+    // 9/8 rows of 64 bytes per token), unswizzled
+    if (ok && nvfp4)
+      ok = encode_nvfp4_map(&h->pf_k, k_cache, rows / 8 * 9, std::min(bs, kNvfp4Group) / 8 * 9,
+                            false) &&
+           encode_nvfp4_map(&h->pf_v, v_cache, rows / 8 * 9, std::min(bs, kNvfp4Group) / 8 * 9,
+                            false);
     if (ok && !nvfp4)
       ok = encode_pool_map(&h->pf_k, k_cache, fp8, rows, pf_box) &&
            encode_pool_map(&h->pf_v, v_cache, fp8, rows, pf_box);
@@ -756,7 +765,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   pp.hkv = c.num_kv_heads;
   pp.group = G;
   pp.bs = bs;
-  pp.rows_total = rows_total;
+  pp.rows_total = nvfp4 ? nvfp4_rows : rows_total;
   pp.num_blocks = c.num_blocks;
   pp.scale_log2 = scale_log2;
   pp.validate = validate;
@@ -766,7 +775,8 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled rejected the query layout");
   const int n_dec = static_cast<int>(plan.dec.size());
   const int n_pre = static_cast<int>(plan.pre.size());
-  if (n_dec > 0 && n_pre > 0 && tc && !fp8 && !(c.flags & PKV_FLAG_SEPARATE)) {
+  if (n_dec > 0 && n_pre > 0 && tc && c.kv_dtype == PKV_KV_BF16 &&
+      !(c.flags & PKV_FLAG_SEPARATE)) {
     // a mixed step: one launch for both kinds of work
     timing_begin(h, PKV_KERNEL_MIXED, s);
     e = launch_mixed(qmap, h->pf_k, h->pf_v, h->dec_k, h->dec_v, pp, dp, n_pre, n_dec, s);
@@ -782,7 +792,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   }
   if (n_pre > 0) {
     timing_begin(h, PKV_KERNEL_PREFILL, s);
-    e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, pp, n_pre, fp8, s);
+    e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, pp, n_pre, c.kv_dtype, s);
     timing_end(h, PKV_KERNEL_PREFILL, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
   }

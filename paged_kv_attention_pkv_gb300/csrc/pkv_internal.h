@@ -148,7 +148,7 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
                           cudaStream_t s);
 cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p,
-                              int num_items, bool fp8, cudaStream_t s);
+                              int num_items, int kv_dtype, cudaStream_t s);
 cudaError_t launch_check(const CheckParams &p, cudaStream_t s);
 cudaError_t launch_lse_merge(const float *parts_o, const float *parts_lse, int num_parts,
                              int64_t num_rows, __nv_bfloat16 *out, float *lse,
@@ -162,13 +162,12 @@ cudaError_t launch_mixed(const CUtensorMap &qmap, const CUtensorMap &kmap_pf,
 // Prefill runs on the tcgen05 kernel: a work item is two Q tiles of
 // pf_tile_rows(G) = G * floor(128 / G) rows (whole tokens of G query heads;
 // 128 for powers of two, the rest of the 128 TMEM lanes idle otherwise).
-// It needs G <= 128 and a bf16 or E4M3 pool.
+// It needs G <= 128 (any pool format).
 constexpr int kPfQTile = 128;
 constexpr int pf_tile_rows(int G) { return G * (kPfQTile / G); }
 inline bool prefill_uses_tc(const pkv_config &c) {
   const int G = c.num_q_heads / c.num_kv_heads;
-  return G > 0 && G <= kPfQTile &&
-         (c.kv_dtype == PKV_KV_BF16 || c.kv_dtype == PKV_KV_FP8_E4M3);
+  return G > 0 && G <= kPfQTile;
 }
 cudaError_t configure_kernels();
 

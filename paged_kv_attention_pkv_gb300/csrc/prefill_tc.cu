@@ -36,7 +36,7 @@
 namespace pkv {
 namespace {
 
-template <bool FP8>
+template <int FMT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
@@ -45,19 +45,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  prefill_tc_item<FP8>(qmap, kmap, vmap, p, p.items[blockIdx.x], smem);
+  prefill_tc_item<FMT>(qmap, kmap, vmap, p, p.items[blockIdx.x], smem);
 }
 
-template <bool FP8>
+template <int FMT>
 cudaError_t configure_one() {
   // setmaxnreg moves registers within the CTA's launch allotment: the split
   // must not ask for more than the kernel was compiled (and launched) with
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<FP8>);
+  cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<FMT>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs * kTcThreads < static_cast<int>(2 * 128 * kRegsSoftmax + 128 * kRegsCtl))
     return cudaErrorInvalidConfiguration;
-  return cudaFuncSetAttribute(prefill_tc_kernel<FP8>,
+  return cudaFuncSetAttribute(prefill_tc_kernel<FMT>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
 }
 
@@ -65,18 +65,24 @@ cudaError_t configure_one() {
 
 cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p,
-                              int num_items, bool fp8, cudaStream_t s) {
+                              int num_items, int kv_dtype, cudaStream_t s) {
   if (num_items == 0) return cudaSuccess;
-  if (fp8)
-    prefill_tc_kernel<true><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap, vmap, p);
+  if (kv_dtype == PKV_KV_NVFP4)
+    prefill_tc_kernel<PKV_KV_NVFP4><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap,
+                                                                               vmap, p);
+  else if (kv_dtype == PKV_KV_FP8_E4M3)
+    prefill_tc_kernel<PKV_KV_FP8_E4M3><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap,
+                                                                                  vmap, p);
   else
-    prefill_tc_kernel<false><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap, vmap, p);
+    prefill_tc_kernel<PKV_KV_BF16><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap,
+                                                                              vmap, p);
   return cudaGetLastError();
 }
 
 cudaError_t configure_prefill_tc() {
-  cudaError_t e = configure_one<false>();
-  return e != cudaSuccess ? e : configure_one<true>();
+  cudaError_t e = configure_one<PKV_KV_BF16>();
+  if (e == cudaSuccess) e = configure_one<PKV_KV_FP8_E4M3>();
+  return e != cudaSuccess ? e : configure_one<PKV_KV_NVFP4>();
 }
 
 }  // namespace pkv

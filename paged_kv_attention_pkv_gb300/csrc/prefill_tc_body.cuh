@@ -40,8 +40,18 @@ constexpr uint32_t kOffK8 = 2 * kTile;
 constexpr uint32_t kOffVs8 = kOffK8 + kKst * kTile8;
 constexpr uint32_t kOffV8 = kOffVs8 + 2 * kTile8;
 static_assert(kOffV8 + kVst * kTile == kOffBar, "the E4M3 layout fills the same 224 KB");
+// NVFP4 pools: K and V tiles arrive as NVFP4 (codes then micro scales per
+// group of rows, 9 KB a tile), K into a 2-deep and V into a 1-deep staging
+// ring, and are converted to f16 into 2-stage f16 K and V rings.
+constexpr uint32_t kStgN = 128 * kNvfp4RowBytes;   // 9216
+constexpr uint32_t kOffKn = 2 * kTile;
+constexpr uint32_t kOffVn = kOffKn + kKst * kTile;
+constexpr int kVstN = 2;
+constexpr uint32_t kOffKsN = kOffVn + kVstN * kTile;
+constexpr uint32_t kOffVsN = kOffKsN + 2 * kStgN;
+static_assert(kOffVsN + kStgN <= kOffBar, "the NVFP4 layout fits the same 224 KB");
 // per-tile block scales (K of 8 key groups of 16, then V), a ring of 8 tiles
-constexpr uint32_t kOffScales = kOffBar + 256;
+constexpr uint32_t kOffScales = kOffBar + 512;
 constexpr int kScaleRing = 8;
 constexpr uint32_t kTmemCols = 512;               // S0, S1, O0, O1
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);
@@ -49,6 +59,7 @@ constexpr uint32_t kIdescQK64 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 0, 1);
 constexpr uint32_t kIdescQK8 = idesc_e4m3(128, 128);
 constexpr uint32_t kIdescPV16 = idesc_f16(128, 128, 0, 1);
+constexpr uint32_t kIdescQK16 = idesc_f16(128, 128, 0, 0);
 constexpr float kRescaleThreshold = 8.f;          // log2 units
 
 __device__ __forceinline__ float ex2(float x) {
@@ -96,14 +107,19 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 }
 
 // One prefill work item processed by all kTcThreads threads of the CTA;
-// `smem` is 1024-byte aligned (kTcSmemBytes - 1024 bytes).  FP8: the pools
-// hold E4M3 codes with one fp32 scale per (block, KV head).
-template <bool FP8>
+// `smem` is 1024-byte aligned (kTcSmemBytes - 1024 bytes).  FMT is the pool
+// format (pkv_kv_dtype): bf16, E4M3 or NVFP4 codes with one fp32 scale per
+// (block, KV head).
+template <int FMT>
 __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
                                                 const CUtensorMap &kmap,
                                                 const CUtensorMap &vmap,
                                                 const PrefillParams &p,
                                                 const pkv_work_item it, uint8_t *smem) {
+  constexpr bool FP8 = FMT == PKV_KV_FP8_E4M3;
+  constexpr bool NV = FMT == PKV_KV_NVFP4;
+  constexpr bool CONV = FP8 || NV;    // converter warps, scale ring, Q converted
+  constexpr int VST = NV ? kVstN : kVst;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint64_t *q_full = bars + 0;
   uint64_t *k_full = bars + 1;               // [kKst]
@@ -114,13 +130,15 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
   uint64_t *p_full = s_full + 2;             // [2]
   uint64_t *o_done = p_full + 2;             // [2]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_done + 2);
-  // E4M3 pools only
+  // E4M3 and NVFP4 pools only
   uint64_t *q_ready = o_done + 3;            // [2] Q tile t converted
-  uint64_t *vs_full = q_ready + 2;           // [2] E4M3 V staging loaded
+  uint64_t *vs_full = q_ready + 2;           // [2] V staging loaded
   uint64_t *vs_empty = vs_full + 2;          // [2] ... and converted
   uint64_t *sc_ready = vs_empty + 2;         // [kScaleRing] tile scales written
+  uint64_t *ks_full = sc_ready + kScaleRing; // [2] NVFP4 K staging loaded
+  uint64_t *ks_empty = ks_full + 2;          // [2] ... and converted
   float *scales = reinterpret_cast<float *>(smem + kOffScales);   // [ring][16]
-  static_assert(8 * (17 + 1 + 2 + 2 + 2 + kScaleRing) <= 256, "barriers fit their 256 bytes");
+  static_assert(8 * (17 + 1 + 2 + 2 + 2 + kScaleRing + 4) <= 512, "barriers fit their 512 bytes");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -142,11 +160,11 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < kKst; ++i) {
-      mbar_init(&k_full[i], 1);
+      mbar_init(&k_full[i], NV ? 2 : 1);    // NVFP4: the two converter warps
       mbar_init(&k_empty[i], 1);
     }
     for (int i = 0; i < kVst; ++i) {
-      mbar_init(&v_full[i], FP8 ? 2 : 1);   // FP8: the two converter warps
+      mbar_init(&v_full[i], CONV ? 2 : 1);  // the two converter warps
       mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -154,11 +172,13 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
     }
-    if (FP8) {
+    if (CONV) {
       for (int i = 0; i < 2; ++i) {
         mbar_init(&q_ready[i], 128);
         mbar_init(&vs_full[i], 1);
         mbar_init(&vs_empty[i], 2);
+        mbar_init(&ks_full[i], 1);
+        mbar_init(&ks_empty[i], 2);
       }
       for (int i = 0; i < kScaleRing; ++i) mbar_init(&sc_ready[i], 1);
     }
@@ -175,7 +195,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
 
   if (warp >= 8) {
    setmaxnreg_dec<kRegsCtl>();
-   if (!FP8 && (warp == 9 || warp == 10)) {
+   if (!CONV && (warp == 9 || warp == 10)) {
     // ---------------- TMA producers: warp 9 loads Q and K, warp 10 V ----
     // Each ring is filled in tile order; K_j waits for the QKs of tile
     // j - kKst, V_j for the PVs of tile j - kVst.  Small blocks take one box
@@ -382,12 +402,183 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         mbar_arrive(&vs_empty[v2]);
       }
     }
+   } else if (NV && warp == 9) {
+    // ---------------- TMA producer, NVFP4 pools: Q, the NVFP4 K staging
+    // ring (2 deep), the NVFP4 V staging tile (1 deep), and each tile's block
+    // scales.  A group of min(bs, 64) rows is contiguous in the pool (codes
+    // then micro scales), so one box of 9/8 rows per row brings both ----
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
+    const int gs = p.bs < kNvfp4Group ? p.bs : kNvfp4Group;
+    const int ngrp = 128 / gs;  // <= 8
+    const int tile_rows = p.bs / 8 * 9, group_rows = gs / 8 * 9;
+    // lane b < ngrp: first pool row of group b of tile j, and its scales
+    auto tile_info = [&](int j, float &sk, float &sv) {
+      const int key = j * 128 + lane * gs;
+      int32_t y = p.rows_total;
+      sk = sv = 1.f;
+      if (lane < ngrp && j < n_tiles && key < k_end) {
+        const int32_t blk = __ldg(bt + key / p.bs);
+        if (blk >= 0 && blk < p.num_blocks) {
+          y = (blk * p.hkv + it.kv_head) * tile_rows + (key % p.bs) / gs * group_rows;
+          const int64_t si = static_cast<int64_t>(blk) * p.hkv + it.kv_head;
+          sk = __ldg(p.k_scale + si);
+          sv = __ldg(p.v_scale + si);
+        } else {
+          record_error(p.err, kErrBadBlock);
+        }
+      }
+      return y;
+    };
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, (two ? 2 : 1) * 2 * R * 128);
+      const int t0 = it.tok0 + it.row0 / G;
+      tma_load_3d(smem + kOffQ, &qmap, 0, it.kv_head * G, t0, q_full);
+      tma_load_3d(smem + kOffQ + kHalf, &qmap, 64, it.kv_head * G, t0, q_full);
+      if (two) {
+        const int t1 = t0 + 128 / G;
+        tma_load_3d(smem + kOffQ + kTile, &qmap, 0, it.kv_head * G, t1, q_full);
+        tma_load_3d(smem + kOffQ + kTile + kHalf, &qmap, 64, it.kv_head * G, t1, q_full);
+      }
+    }
+    float sk_cur, sv_cur;
+    int32_t y_cur = tile_info(0, sk_cur, sv_cur);
+    for (int j = 0; j < n_tiles; ++j) {
+      float sk_nxt, sv_nxt;
+      const int32_t y_next = tile_info(j + 1, sk_nxt, sv_nxt);
+      const int gb = (lane * 16 / gs) & 31;   // group of key group `lane`
+      const float gk = __shfl_sync(0xffffffffu, sk_cur, gb);
+      const float gv = __shfl_sync(0xffffffffu, sv_cur, gb);
+      if (lane < 8) {
+        scales[(j % kScaleRing) * 16 + lane] = gk;
+        scales[(j % kScaleRing) * 16 + 8 + lane] = gv;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sc_ready[j % kScaleRing]);
+      int n = 0;
+      for (int r = 0; r < 128; r += gs)
+        if (j * 128 + r < k_end) ++n;
+      // K tile j into staging j & 1 once the converters are done with j - 2
+      const int k2 = j & 1;
+      if (j >= 2 &&
+          !__all_sync(0xffffffffu, mbar_wait(&ks_empty[k2], ((j >> 1) - 1) & 1))) {
+        if (lane == 0) record_error(p.err, kErrTimeout);
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&ks_full[k2], n * gs * kNvfp4RowBytes);
+      for (int bx = 0; bx < n; ++bx) {
+        const int32_t y = __shfl_sync(0xffffffffu, y_cur, bx);
+        if (lane == 0)
+          tma_load_2d(smem + kOffKsN + k2 * kStgN + bx * gs * kNvfp4RowBytes, &kmap, 0, y,
+                      &ks_full[k2]);
+      }
+      // V tile j into the staging tile once the converters are done with j - 1
+      if (j >= 1 &&
+          !__all_sync(0xffffffffu, mbar_wait(&vs_empty[0], (j - 1) & 1))) {
+        if (lane == 0) record_error(p.err, kErrTimeout);
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&vs_full[0], n * gs * kNvfp4RowBytes);
+      for (int bx = 0; bx < n; ++bx) {
+        const int32_t y = __shfl_sync(0xffffffffu, y_cur, bx);
+        if (lane == 0)
+          tma_load_2d(smem + kOffVsN + bx * gs * kNvfp4RowBytes, &vmap, 0, y, &vs_full[0]);
+      }
+      y_cur = y_next;
+      sk_cur = sk_nxt;
+      sv_cur = sv_nxt;
+    }
+   } else if (NV && warp >= 10) {
+    // ---------------- converters, NVFP4 pools: staging -> f16 K and V rings ----
+    // Four lanes share a key row, lane c taking head dims 32c .. 32c + 31 (16
+    // code bytes: micro blocks 2c and 2c + 1); warp 10 converts rows 0-63 of
+    // a tile, warp 11 rows 64-127, eight rows per pass.  K becomes f16 code x
+    // micro scale, exactly (a 2-bit by 4-bit significand product); V becomes
+    // f16 code x (micro scale x block scale), rounded once.  Rows past the
+    // item's last key are written as zeros.
+    const int gs = p.bs < kNvfp4Group ? p.bs : kNvfp4Group;
+    const int c = lane & 3;
+    const int rbase = (warp - 10) * 64 + (lane >> 2);
+    auto convert = [&](uint32_t stg, uint32_t dst, int j, bool is_v) {
+#pragma unroll 2
+      for (int ps = 0; ps < 8; ++ps) {
+        const int k = rbase + 8 * ps;   // key row in the tile
+        const uint32_t sw = k & 7;
+        uint32_t o[16];
+        if (j * 128 + k >= k_end) {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) o[q] = 0u;
+        } else {
+          const uint32_t grp = stg + (k / gs) * gs * kNvfp4RowBytes;
+          const int r = k % gs;
+          const uint4 x = lds128(grp + r * 64 + 16 * c);
+          const uint32_t msb = lds16(grp + gs * 64 + r * 8 + 2 * c);
+          uint32_t m0, m1;   // (s, s) f16 pairs for micro blocks 2c and 2c + 1
+          if (is_v) {
+            const float2 ms = e4m3x2_to_f32(msb);
+            const float sv = scales[(j % kScaleRing) * 16 + 8 + (k >> 4)];
+            m0 = pack_f16(ms.x * sv, ms.x * sv);
+            m1 = pack_f16(ms.y * sv, ms.y * sv);
+          } else {
+            const uint32_t mh = e4m3x2lo_to_f16x2(msb);
+            m0 = __byte_perm(mh, 0, 0x1010);
+            m1 = __byte_perm(mh, 0, 0x3232);
+          }
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t f[4];
+            e2m1x8_to_f16x2(w[q], f);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) o[4 * q + u] = hmul2(f[u], q < 2 ? m0 : m1);
+          }
+        }
+        // f16 row: column half c >> 1, chunks 4 (c & 1) .. + 3
+        const uint32_t hb = dst + (c >> 1) * kHalf + k * 128;
+        const uint32_t c0 = 4 * (c & 1);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          sts128(hb + (((c0 + q) ^ sw) << 4), o[4 * q], o[4 * q + 1], o[4 * q + 2],
+                 o[4 * q + 3]);
+      }
+    };
+    for (int j = 0; j < n_tiles; ++j) {
+      const int k2 = j & 1, s = j % kKst, vs = j % kVstN;
+      bool wok = mbar_wait(&ks_full[k2], (j >> 1) & 1);
+      if (wok && j >= kKst) wok = mbar_wait(&k_empty[s], ((j / kKst) - 1) & 1);
+      if (wok) wok = mbar_wait(&sc_ready[j % kScaleRing], (j / kScaleRing) & 1);
+      if (!__all_sync(0xffffffffu, wok)) {
+        if (lane == 0) record_error(p.err, kErrTimeout);
+        break;
+      }
+      convert(smem_addr(smem + kOffKsN + k2 * kStgN), smem_addr(smem + kOffKn + s * kTile), j,
+              false);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&k_full[s]);
+        mbar_arrive(&ks_empty[k2]);
+      }
+      wok = mbar_wait(&vs_full[0], j & 1);
+      if (wok && j >= kVstN) wok = mbar_wait(&v_empty[vs], ((j / kVstN) - 1) & 1);
+      if (!__all_sync(0xffffffffu, wok)) {
+        if (lane == 0) record_error(p.err, kErrTimeout);
+        break;
+      }
+      convert(smem_addr(smem + kOffVsN), smem_addr(smem + kOffVn + vs * kTile), j, true);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&v_full[vs]);
+        mbar_arrive(&vs_empty[0]);
+      }
+    }
    } else if (warp == 8) {
     // ---------------- MMA issuer (one thread) ----------------
     if (lane == 0) {
-      // E4M3 pools: the softmax warps turn Q tile t into E4M3 hi/lo parts
-      bool ok = FP8 ? mbar_wait(&q_ready[0], 0) : mbar_wait(q_full, 0);
-      if (FP8) tc_fence_after();
+      // E4M3 / NVFP4 pools: the softmax warps first turn Q tile t into E4M3
+      // hi/lo parts / scaled f16
+      bool ok = CONV ? mbar_wait(&q_ready[0], 0) : mbar_wait(q_full, 0);
+      if (CONV) tc_fence_after();
       // Descriptors are built once; tiles, stages and k-steps add constant
       // offsets to the start-address field (addresses stay < 256 KB, so the
       // 14-bit field never carries).  The issuing warp shares its SM
@@ -395,13 +586,16 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       // between MMA groups is time the tensor pipe may sit idle.
       constexpr uint64_t kTileDesc = kTile >> 4;
       const uint64_t qd0 = smem_desc_sw128(smem_addr(smem + kOffQ), 16, 1024);
-      const uint64_t kd0 = smem_desc_sw128(smem_addr(smem + (FP8 ? kOffK8 : kOffK)), 16, 1024);
-      const uint64_t vd0 = smem_desc_sw128(smem_addr(smem + (FP8 ? kOffV8 : kOffV)), kHalf, 1024);
+      const uint64_t kd0 =
+          smem_desc_sw128(smem_addr(smem + (NV ? kOffKn : FP8 ? kOffK8 : kOffK)), 16, 1024);
+      const uint64_t vd0 =
+          smem_desc_sw128(smem_addr(smem + (NV ? kOffVn : FP8 ? kOffV8 : kOffV)), kHalf, 1024);
       auto qk = [&](int t, int j) {   // S_t = Q_t K_j^T
         const int s = j & (kKst - 1);
         // K arrives by TMA (async proxy, like the MMA): the mbarrier alone
-        // orders it
+        // orders it; NVFP4 K is written by the converter warps
         if (!mbar_wait(&k_full[s], (j / kKst) & 1)) return false;
+        if (NV) tc_fence_after();
         const uint64_t a0 = qd0 + t * kTileDesc;
         const uint32_t d = tmem + t * 128;
         if constexpr (FP8) {
@@ -427,9 +621,9 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
           for (int ks = 0; ks < 8; ++ks) {
             const uint64_t off = ((ks >> 2) * kHalf + (ks & 3) * 32) >> 4;
             if (ks == 0)
-              tc_mma_first(d, a0, b0, kIdescQK);
+              tc_mma_first(d, a0, b0, NV ? kIdescQK16 : kIdescQK);
             else
-              tc_mma_acc(d, a0 + off, b0 + off, kIdescQK);
+              tc_mma_acc(d, a0 + off, b0 + off, NV ? kIdescQK16 : kIdescQK);
           }
         }
         tc_commit(&s_full[t]);
@@ -445,16 +639,16 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t bd = b0 + ((kk * 2048) >> 4);
           if (kk > 0)
-            tc_mma_tmem_a_acc(dO, aP + kk * 8, bd, FP8 ? kIdescPV16 : kIdescPV);
+            tc_mma_tmem_a_acc(dO, aP + kk * 8, bd, CONV ? kIdescPV16 : kIdescPV);
           else
-            tc_mma_tmem_a(dO, aP, bd, FP8 ? kIdescPV16 : kIdescPV, j > 0 ? 1u : 0u);
+            tc_mma_tmem_a(dO, aP, bd, CONV ? kIdescPV16 : kIdescPV, j > 0 ? 1u : 0u);
         }
         tc_commit(&o_done[t]);
         return true;
       };
       // prologue: QK of tile 0 for both Q tiles
       if (ok) ok = qk(0, 0);
-      if (FP8 && ok && two) {
+      if (CONV && ok && two) {
         ok = mbar_wait(&q_ready[1], 0);
         tc_fence_after();
       }
@@ -475,7 +669,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         if (ok && t1) ok = pv(1, j, vs, vpar);
         if (!ok) break;
         tc_commit(&v_empty[vs]);
-        if (++vs == kVst) {
+        if (++vs == VST) {
           vs = 0;
           vpar ^= 1;
         }
@@ -502,12 +696,14 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     float m = -CUDART_INF_F;              // running max, log2 units
     float l = 0.f;
     bool ok = true;
-    if (FP8 && ntl > 0) {
+    if (CONV && ntl > 0) {
       // E4M3 pools: this thread's Q row, scaled by a power of two sq (largest
       // |q sq| in [128, 256)), becomes hi + lo, both E4M3 (about bf16
       // precision), written in place over the row: hi into the tile's first
       // 128-byte half, lo into its second (each the 128B-swizzled K-major
-      // layout of a 128 x 128 E4M3 tile).  1/sq goes into this row's scale.
+      // layout of a 128 x 128 E4M3 tile).  NVFP4 pools: the row becomes f16
+      // in place (largest |q sq| in [2^14, 2^15), the bf16 layout).  1/sq
+      // goes into this row's scale.
       ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0));
       if (ok) {
         const uint32_t qt = smem_addr(smem + kOffQ + t * kTile);
@@ -529,11 +725,27 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
           amax = fmax3(amax, fabsf(__uint_as_float(w[i] << 16)),
                        fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
         const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
-        const int k2 = 7 - e < 126 ? 7 - e : 126;
+        const int top = NV ? 14 : 7;
+        const int k2 = top - e < 126 ? top - e : 126;
         const float sq = __uint_as_float(static_cast<uint32_t>(127 + k2) << 23);
         c *= __uint_as_float(static_cast<uint32_t>(127 - k2) << 23);
+        if constexpr (NV) {
 #pragma unroll
-        for (int oc = 0; oc < 8; ++oc) {   // 16 dims: words 8 oc .. 8 oc + 7
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+              uint32_t o[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t wv = w[32 * h + 4 * cc + u];
+                o[u] = pack_f16(__uint_as_float(wv << 16) * sq,
+                                __uint_as_float(wv & 0xFFFF0000u) * sq);
+              }
+              sts128(qt + h * kHalf + r * 128 + ((cc ^ sw) << 4), o[0], o[1], o[2], o[3]);
+            }
+        }
+#pragma unroll
+        for (int oc = 0; oc < (NV ? 0 : 8); ++oc) {   // 16 dims: words 8 oc .. 8 oc + 7
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -576,11 +788,11 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
           s[k] = key > pos ? -CUDART_INF_F : s[k];
         }
       }
-      // E4M3 pools: key group g (16 keys, one block) has its own score
-      // scale c * k_scale (positive), so maxima are taken per group
+      // E4M3 and NVFP4 pools: key group g (16 keys, one block) has its own
+      // score scale c * k_scale (positive), so maxima are taken per group
       float cg[8];
       float mt2;
-      if constexpr (FP8) {
+      if constexpr (CONV) {
         if (!__all_sync(0xffffffffu,
                         mbar_wait(&sc_ready[j % kScaleRing], (j / kScaleRing) & 1))) {
           ok = false;
@@ -631,11 +843,11 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         for (int k = 0; k < 32; ++k) {
           float x0, x1;
           fma2_bc(x0, x1, s[64 * hh + 2 * k], s[64 * hh + 2 * k + 1],
-                  FP8 ? cg[(64 * hh + 2 * k) >> 4] : c, -m);
+                  CONV ? cg[(64 * hh + 2 * k) >> 4] : c, -m);
           const float e0 = ex2(x0), e1 = ex2(x1);
           add2(acc[(2 * k) & 7], acc[(2 * k + 1) & 7], e0, e1);
-          // E4M3 pools run PV in f16 (V converted to f16); bf16 otherwise
-          pk[k] = FP8 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
+          // E4M3 and NVFP4 pools run PV in f16 (V converted to f16)
+          pk[k] = CONV ? pack_f16(e0, e1) : pack_bf16(e0, e1);
         }
         tmem_st32u(lane_addr + col_s + 32 * hh, pk);
       }
@@ -659,9 +871,9 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       // The last K/V tile may carry V rows past the item's last key (rows
       // of other requests or never loaded): zero them before any PV reads
       // them.  Q tile 0 does it when it reaches that tile (its PV comes
-      // first), otherwise Q tile 1.  (E4M3 pools: the converters write
+      // first), otherwise Q tile 1.  (E4M3 and NVFP4 pools: the converters write
       // those rows as zeros.)
-      if (!FP8 && j == n_tiles - 1 && k_end - key0 < 128 && (t == 0 || nt0 < n_tiles)) {
+      if (!CONV && j == n_tiles - 1 && k_end - key0 < 128 && (t == 0 || nt0 < n_tiles)) {
         const int vvalid = k_end - key0;
         const int vs = j % kVst;
         if (!__all_sync(0xffffffffu, mbar_wait(&v_full[vs], (j / kVst) & 1))) {
@@ -722,6 +934,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
 
 // barriers (256 B), the E4M3 scale ring (8 tiles x 16 fp32), alignment slack
 constexpr uint32_t kTcSmemBytes = kOffScales + kScaleRing * 16 * 4 + 1024;
+static_assert(kTcSmemBytes <= 232448, "within the 227 KB a CTA may have");
 
 }  // namespace
 }  // namespace pkv

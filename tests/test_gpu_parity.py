@@ -117,6 +117,11 @@ SWEEP = [
     ("nvfp4_gqa4_bs16", 32, 8, 16, [1, 2, 1, 40], [17, 33, 2000, 300], "nvfp4"),
     ("nvfp4_gqa2_bs128", 4, 2, 128, [1, 3, 1], [129, 700, 4100], "nvfp4"),
     ("nvfp4_gqa8_bs32", 16, 2, 32, [1, 1], [95, 3000], "nvfp4"),
+    # NVFP4 prefill rows on the tensor cores (K and V converted to f16)
+    ("nvfp4_prefill_gqa4", 32, 8, 16, [1, 40, 3, 130], [17, 300, 2000, 130], "nvfp4"),
+    ("nvfp4_prefill_gqa8_bs64", 64, 8, 64, [1, 70, 5], [5000, 700, 65], "nvfp4"),
+    ("nvfp4_prefill_gqa3", 6, 2, 64, [10, 1, 33], [100, 64, 1500], "nvfp4"),
+    ("nvfp4_prefill_bs128", 16, 4, 128, [200, 2], [1300, 300], "nvfp4"),
 ]
 
 

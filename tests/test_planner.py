@@ -34,9 +34,9 @@ def test_plan_covers_the_workloads(index):
             dec_keys.setdefault((i, h), []).append((w["k_begin"], w["k_end"], w))
         else:
             assert q * G > 8
-            # bf16 and E4M3 pools with G <= 128 use tensor-core tiles, the
-            # rest 8-row chunks on the decode kernel
-            assert w["kind"] == (1 if spec.kv_dtype in ("bf16", "fp8") and G <= 128 else 0)
+            # G <= 128 uses tensor-core tiles (every pool format), larger
+            # groups 8-row chunks on the decode kernel
+            assert w["kind"] == (1 if G <= 128 else 0)
             if w["kind"] == 0:
                 assert w["n_rows"] <= 8 and w["row0"] % 8 == 0 and w["part"] == -1
             assert w["k_begin"] == 0
@@ -116,10 +116,9 @@ def test_plan_empty_and_zero_token_requests():
     assert items == []
 
 
-@pytest.mark.parametrize("kv,hq,hkv", [("nvfp4", 32, 8), ("nvfp4", 6, 2), ("bf16", 256, 1),
-                                      ("fp8", 512, 2)])
+@pytest.mark.parametrize("kv,hq,hkv", [("nvfp4", 256, 1), ("bf16", 256, 1), ("fp8", 512, 2)])
 def test_prefill_rows_without_tensor_core_tiles_are_chunked(kv, hq, hkv):
-    """Over NVFP4 pools, or with query groups above 128, prefill rows become
+    """With query groups above 128, prefill rows become
     decode-kernel items of at most 8 rows: they tile [0, q*G) exactly, each
     reaches keys up to its last token's position, writes the output directly,
     and the chunks of one (request, KV head) are adjacent in launch order."""
