@@ -167,6 +167,20 @@ def make_config(num_q_heads, num_kv_heads, block_size, num_blocks, max_num_seqs,
                   max_num_tokens, flags)
 
 
+def pool_shapes(config: Config):
+    """Shapes and dtypes of the K (and V) pool and of the block-scale arrays
+    a handle with ``config`` reads: ``(pool_shape, pool_dtype, scale_shape)``,
+    ``scale_shape`` None for bf16 pools.  bf16 and E4M3 pools are
+    ``[num_blocks, Hkv, block_size, 128]`` (bf16 / uint8); NVFP4 pools are
+    ``[num_blocks, Hkv, block_size * 72]`` uint8 (include/pkv.h, pool layout)."""
+    nb, hkv, bs = int(config.num_blocks), int(config.num_kv_heads), int(config.block_size)
+    if config.kv_dtype == KV_NVFP4:
+        return (nb, hkv, bs * 72), torch.uint8, (nb, hkv)
+    if config.kv_dtype == KV_FP8_E4M3:
+        return (nb, hkv, bs, int(config.head_dim)), torch.uint8, (nb, hkv)
+    return (nb, hkv, bs, int(config.head_dim)), torch.bfloat16, None
+
+
 class Handle:
     """A libpkv handle bound to one CUDA device (pkv_create / pkv_destroy)."""
 

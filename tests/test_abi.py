@@ -72,3 +72,15 @@ def test_create_without_gpu_reports_cuda_error():
     with pytest.raises(pkv.PkvError) as e:
         pkv.Handle(_cfg())
     assert e.value.status == 3
+
+
+def test_pool_shapes_follow_the_header_layout():
+    """bf16 / E4M3 pools are [num_blocks, Hkv, bs, 128]; NVFP4 pools hold 72
+    bytes per token and KV head (64 code bytes + 8 micro scales)."""
+    import torch
+    for kv, shape, dtype, scales in (
+            (pkv.KV_BF16, (10, 2, 16, 128), torch.bfloat16, None),
+            (pkv.KV_FP8_E4M3, (10, 2, 16, 128), torch.uint8, (10, 2)),
+            (pkv.KV_NVFP4, (10, 2, 16 * 72), torch.uint8, (10, 2))):
+        cfg = pkv.make_config(8, 2, 16, 10, 4, 64, kv_dtype=kv)
+        assert pkv.pool_shapes(cfg) == (shape, dtype, scales)
