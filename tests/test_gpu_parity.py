@@ -208,10 +208,14 @@ def test_decode_batch_full_size():
     _sampled(b, seqs, None, what="c2")
 
 
-def test_post_tool_prefill_full_size():
-    b = W.generate(W.config_spec(2), DEV)
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "nvfp4"])
+def test_post_tool_prefill_full_size(kv):
+    """The post-tool-call prefill as bench.py times it (bf16, and the E4M3 /
+    NVFP4 KV variants of its secondary lines): sessions 0 (shared prefix), 3
+    and 9, two KV heads, edge and random tokens."""
+    b = W.generate(dataclasses.replace(W.config_spec(2), kv_dtype=kv), DEV)
     G = 4
-    _sampled(b, [0, 3, 9], [0, 5], token_pick=lambda q: _edge_tokens(q, G), what="c3")
+    _sampled(b, [0, 3, 9], [0, 5], token_pick=lambda q: _edge_tokens(q, G), what=f"c3 {kv}")
 
 
 def test_mixed_step_full_size():
