@@ -122,6 +122,11 @@ SWEEP = [
     ("nvfp4_prefill_gqa8_bs64", 64, 8, 64, [1, 70, 5], [5000, 700, 65], "nvfp4"),
     ("nvfp4_prefill_gqa3", 6, 2, 64, [10, 1, 33], [100, 64, 1500], "nvfp4"),
     ("nvfp4_prefill_bs128", 16, 4, 128, [200, 2], [1300, 300], "nvfp4"),
+    # quantised pools with query groups that leave TMEM lanes padded
+    ("fp8_prefill_gqa12", 96, 8, 16, [11, 25], [400, 25], "fp8"),
+    ("fp8_prefill_gqa96", 96, 1, 32, [1, 3, 5], [64, 700, 5], "fp8"),
+    ("nvfp4_prefill_gqa12", 96, 8, 16, [11, 25], [400, 25], "nvfp4"),
+    ("nvfp4_prefill_gqa96", 96, 1, 32, [1, 3, 5], [64, 700, 5], "nvfp4"),
 ]
 
 
