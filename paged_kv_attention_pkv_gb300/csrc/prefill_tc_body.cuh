@@ -55,7 +55,6 @@ constexpr uint32_t kOffScales = kOffBar + 512;
 constexpr int kScaleRing = 8;
 constexpr uint32_t kTmemCols = 512;               // S0, S1, O0, O1
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);
-constexpr uint32_t kIdescQK64 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 0, 1);
 constexpr uint32_t kIdescQK8 = idesc_e4m3(128, 128);
 constexpr uint32_t kIdescPV16 = idesc_f16(128, 128, 0, 1);
