@@ -383,8 +383,7 @@ pkv_status pkv_timing_read(pkv_handle *h, int32_t kind, int32_t *launches,
  *    different streams, or from different threads) race on it: serialise
  *    them.
  *  - Returns PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED (prefill rows,
- *    NVFP4 pools, head_dim or block_size not handled), PKV_ERR_WORKSPACE or
- *    PKV_ERR_CUDA.
+ *    head_dim or block_size not handled), PKV_ERR_WORKSPACE or PKV_ERR_CUDA.
  *    It does not update pkv_last_error() and performs no device-side
  *    validation.
  */

@@ -65,7 +65,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-bool encode_map(CUtensorMap *m, const void *base, bool fp8, int64_t rows, int box_rows) {
+EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -76,6 +76,11 @@ bool encode_map(CUtensorMap *m, const void *base, bool fp8, int64_t rows, int bo
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<EncodeTiledFn>(p);
   });
+  return fn;
+}
+
+bool encode_map(CUtensorMap *m, const void *base, bool fp8, int64_t rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), cuuint64_t(rows)};
   const cuuint64_t strides[1] = {cuuint64_t(kHeadDim * (fp8 ? 1 : 2))};
@@ -86,6 +91,20 @@ bool encode_map(CUtensorMap *m, const void *base, bool fp8, int64_t rows, int bo
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// NVFP4 pool as rows of 64 bytes; boxes of code rows, 64-byte swizzled (the
+// layout the NVFP4 decode reads).
+bool encode_nvfp4_map(CUtensorMap *m, const void *base, int64_t rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {64, cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {64};
+  const cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Host staging for the work list: a fixed array, no heap.  Serialised by
@@ -108,15 +127,15 @@ extern "C" pkv_status pkv_decode_static(
   if (c->num_kv_heads <= 0 || c->num_q_heads <= 0 || c->num_q_heads % c->num_kv_heads ||
       c->num_blocks <= 0 || !(c->softmax_scale > 0.f))
     return PKV_ERR_INVALID_ARG;
-  if (c->num_blocks * c->num_kv_heads * bs >= (int64_t(1) << 31) - 4096)
+  const bool nvfp4 = c->kv_dtype == PKV_KV_NVFP4;
+  if (c->num_blocks * c->num_kv_heads * bs * (nvfp4 ? 9 : 8) / 8 >= (int64_t(1) << 31) - 4096)
     return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0) return num_tokens == 0 ? PKV_OK : PKV_ERR_INVALID_ARG;
   if (!q || !k_cache || !v_cache || !block_tables || !qsl || !lens || !out)
     return PKV_ERR_INVALID_ARG;
   const bool fp8 = c->kv_dtype == PKV_KV_FP8_E4M3;
-  if (c->kv_dtype == PKV_KV_NVFP4) return PKV_ERR_UNSUPPORTED;
-  if (c->kv_dtype != PKV_KV_BF16 && !fp8) return PKV_ERR_INVALID_ARG;
-  if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+  if (c->kv_dtype != PKV_KV_BF16 && !fp8 && !nvfp4) return PKV_ERR_INVALID_ARG;
+  if ((fp8 || nvfp4) && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
   const int G = c->num_q_heads / c->num_kv_heads;
   const int H = c->num_kv_heads;
   if (qsl[0] != 0 || qsl[num_seqs] != num_tokens) return PKV_ERR_INVALID_ARG;
@@ -155,9 +174,16 @@ extern "C" pkv_status pkv_decode_static(
   if (scratch_address(dev, &scratch) != cudaSuccess) return PKV_ERR_CUDA;
   const int64_t rows = c->num_blocks * c->num_kv_heads * bs;
   CUtensorMap kmap, vmap;
-  const int box = std::min(bs, fp8 ? kDecKeysFp8 : kDecKeysBf16);
-  if (!encode_map(&kmap, k_cache, fp8, rows, box) || !encode_map(&vmap, v_cache, fp8, rows, box))
-    return PKV_ERR_CUDA;
+  if (nvfp4) {
+    const int box = std::min(std::min(bs, kNvfp4Group), kDecKeysNvfp4);
+    if (!encode_nvfp4_map(&kmap, k_cache, rows / 8 * 9, box) ||
+        !encode_nvfp4_map(&vmap, v_cache, rows / 8 * 9, box))
+      return PKV_ERR_CUDA;
+  } else {
+    const int box = std::min(bs, fp8 ? kDecKeysFp8 : kDecKeysBf16);
+    if (!encode_map(&kmap, k_cache, fp8, rows, box) || !encode_map(&vmap, v_cache, fp8, rows, box))
+      return PKV_ERR_CUDA;
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(g_plan_mutex);
@@ -219,7 +245,9 @@ extern "C" pkv_status pkv_decode_static(
   p.hkv = H;
   p.group = G;
   p.bs = bs;
-  p.rows_total = static_cast<int32_t>(rows);
+  p.rows_total = static_cast<int32_t>(nvfp4 ? rows / 8 * 9 : rows);
+  p.k_pool = static_cast<const uint8_t *>(k_cache);
+  p.v_pool = static_cast<const uint8_t *>(v_cache);
   p.num_blocks = c->num_blocks;
   p.scale_log2 = c->softmax_scale * 1.4426950408889634f;
   p.validate = 0;

@@ -20,6 +20,7 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("kv,bs,hq,hkv,lens", [
     ("bf16", 16, 32, 8, [9000, 4097, 17, 30000, 1, 12345]),
     ("fp8", 64, 64, 8, [70000, 65, 3000]),
+    ("nvfp4", 16, 32, 8, [20000, 33, 5000]),
 ])
 def test_static_scratch_decode_matches_the_handle_path(kv, bs, hq, hkv, lens):
     s = W.custom_spec("static", hq, hkv, bs, [1] * len(lens), lens, seed=11, kv_dtype=kv)
