@@ -455,8 +455,63 @@ def time_graph(index, steps: int, device: str) -> dict:
             "graph_ms_per_step": round(graph_ms, 5), "speedup": round(eager_ms / graph_ms, 3)}
 
 
+def time_per_call(index, device: str, calls: int = 20, warmup: int = 5) -> dict:
+    """Latency of single steps (append + attention): `warmup` untimed calls,
+    then `calls` calls each bracketed by CUDA events with the device idle
+    before it, so a call's span includes its host-side enqueue.  "warm" runs
+    the calls back to back; "cold" writes a 256 MB buffer (twice the L2)
+    before each call, outside its events.  The library's own per-kernel
+    events give the device time of the kernels alone."""
+    import paged_kv_attention_pkv_gb300 as pkv
+    spec = W.config_spec(index)
+    batch = W.generate(spec, device)
+    h = make_handle(batch, pkv.FLAG_TIMING)
+    m = device_meta(batch)
+    out = torch.empty_like(batch.q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def step():
+        h.write_slots(batch.k_new, batch.v_new, m["slots"], batch.k_cache,
+                      batch.v_cache, batch.k_scale, batch.v_scale)
+        h.attention_varlen(batch.q, batch.k_cache, batch.v_cache, m["qsl"], m["lens"],
+                           m["bt"], batch.qsl, batch.seq_lens, out=out,
+                           k_scale=batch.k_scale, v_scale=batch.v_scale)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    res = {"workload": spec.name, "calls": calls, "warmup": warmup}
+    for mode in ("warm", "cold"):
+        h.timing_reset()
+        spans = []
+        for i in range(calls):
+            if mode == "cold":
+                flush.fill_(i & 0xFF)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            step()
+            e1.record()
+            torch.cuda.synchronize()
+            spans.append(e0.elapsed_time(e1) * 1e3)
+        kernels_us = 0.0
+        for kind in (pkv.KERNEL_APPEND, pkv.KERNEL_DECODE, pkv.KERNEL_PREFILL,
+                     pkv.KERNEL_MIXED):
+            n, tot = h.timing_read(kind)
+            if n:
+                kernels_us += tot / n * 1e3
+        res[mode] = {"median_us": round(float(np.median(spans)), 2),
+                     "min_us": round(float(np.min(spans)), 2),
+                     "kernels_mean_us": round(kernels_us, 2)}
+    h.close()
+    del batch, flush
+    torch.cuda.empty_cache()
+    return res
+
+
 def secondary(args, world, peaks, device):
     out = []
+    out.append({"per_call": [time_per_call(0, device), time_per_call(1, device)]})
     out.append({"cuda_graph": [time_graph(0, 500, device), time_graph(1, 200, device)]})
     nvfp4 = dataclasses.replace(W.config_spec(4), name="c5_nvfp4_long_decode",
                                 kv_dtype="nvfp4")

@@ -143,6 +143,7 @@ std::string check_config(const pkv_config *c, pkv_status *st) {
 struct Plan {
   std::vector<pkv_work_item> dec, pre;
   int partials = 0;
+  int pre_groups = 0;   // split prefill items: their first ranges lead `pre`
 };
 
 // Keys of a sequence of L keys that context-parallel shard r of n owns when
@@ -280,6 +281,56 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
       }
     }
   }
+  // Few prefill tiles leave most SMs idle while each walks its whole key
+  // range (an incremental prefill of a few new tokens over a long history):
+  // split the key ranges into runs of whole 128-key tiles so that the step
+  // has about one tile per SM; each range writes a partial (O / l and the
+  // log-sum-exp), merged by a second small kernel.  Boundaries lie at
+  // multiples of 128 keys and of the block size, at or below the item's
+  // first query position, so every query row sees at least one key in
+  // every range.  A prefill partial slot is kPfPartSlots decode slots (256
+  // rows) of the same partial buffers.
+  if (dcp == nullptr && !plan->pre.empty() &&
+      int64_t(plan->pre.size()) * 2 <= std::max(num_sms, 1)) {
+    int64_t total_tiles = 0;
+    for (const auto &w : plan->pre) total_tiles += (w.k_end + 127) / 128;
+    std::vector<pkv_work_item> split;
+    for (const auto &w : plan->pre) {
+      const int nt = (w.k_end + 127) / 128;
+      const int unit = std::max(1, c.block_size / 128);    // boundary granularity, tiles
+      // last allowed boundary, in tiles
+      const int max_bound = (w.hist + w.row0 / G) / (128 * unit) * unit;
+      const int want = static_cast<int>(
+          std::min<int64_t>(nt, std::max<int64_t>(1, (int64_t(num_sms) * nt + total_tiles / 2) /
+                                                         std::max<int64_t>(total_tiles, 1))));
+      int ns = std::min({want, nt / kPfMinSplitTiles, max_bound + 1, kPfMaxSplits});
+      if (ns > 1 && part + int64_t(ns) * kPfPartSlots > max_partials) ns = 1;
+      if (ns <= 1) {
+        split.push_back(w);
+        continue;
+      }
+      const int cs = ((nt + ns - 1) / ns + unit - 1) / unit * unit;   // tiles per range
+      int bounds = 0;                       // interior boundaries s * cs <= max_bound
+      while (bounds + 1 < ns && (bounds + 1) * cs <= max_bound) ++bounds;
+      ns = bounds + 1;
+      if (ns <= 1) {
+        split.push_back(w);
+        continue;
+      }
+      const int base = part;
+      for (int s = 0; s < ns; ++s) {
+        pkv_work_item v = w;
+        v.k_begin = s * cs * 128;
+        v.k_end = s + 1 < ns ? (s + 1) * cs * 128 : w.k_end;
+        v.part = part;
+        v.pair = base;
+        v.n_split = ns;
+        part += kPfPartSlots;
+        split.push_back(v);
+      }
+    }
+    plan->pre.swap(split);
+  }
   plan->partials = part;
   // Decode items longest first.  Prefill row chunks (row0 > 0 or more than
   // one chunk per request) stay together per (request, KV head), the group
@@ -317,7 +368,9 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
   // Prefill tiles of one (request, KV head) read the same K/V stream: keep
   // them adjacent so the CTAs running together share it through L2, and
   // order the groups longest first.
-  auto pre_cost = [](const pkv_work_item &w) { return int64_t(w.k_end) * w.n_rows; };
+  auto pre_cost = [](const pkv_work_item &w) {
+    return (int64_t(w.k_end) - w.k_begin) * w.n_rows;
+  };
   std::vector<int64_t> group_cost(size_t(B) * H, 0);
   for (const auto &w : plan->pre) group_cost[size_t(w.seq) * H + w.kv_head] += pre_cost(w);
   std::stable_sort(plan->pre.begin(), plan->pre.end(),
@@ -329,6 +382,12 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
                      if (a.kv_head != b.kv_head) return a.kv_head < b.kv_head;
                      return pre_cost(a) > pre_cost(b);
                    });
+  // the first range of each split item leads the list: the merge kernel
+  // takes its groups from there
+  const auto lead = std::stable_partition(
+      plan->pre.begin(), plan->pre.end(),
+      [](const pkv_work_item &w) { return w.part >= 0 && w.part == w.pair; });
+  plan->pre_groups = static_cast<int>(lead - plan->pre.begin());
   *st = PKV_OK;
   return "";
 }
@@ -769,6 +828,8 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   pp.num_blocks = c.num_blocks;
   pp.scale_log2 = scale_log2;
   pp.validate = validate;
+  pp.part_o = h->d_part_o;
+  pp.part_lse = h->d_part_lse;
   const bool tc = prefill_uses_tc(c);
   CUtensorMap qmap;
   if (!plan.pre.empty() && tc && !encode_q_map(&qmap, q, c.num_q_heads, G, num_tokens))
@@ -780,6 +841,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     // a mixed step: one launch for both kinds of work
     timing_begin(h, PKV_KERNEL_MIXED, s);
     e = launch_mixed(qmap, h->pf_k, h->pf_v, h->dec_k, h->dec_v, pp, dp, n_pre, n_dec, s);
+    if (e == cudaSuccess) e = launch_prefill_merge(pp, plan.pre_groups, s);
     timing_end(h, PKV_KERNEL_MIXED, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed-step launch");
     return PKV_OK;
@@ -793,6 +855,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   if (n_pre > 0) {
     timing_begin(h, PKV_KERNEL_PREFILL, s);
     e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, pp, n_pre, c.kv_dtype, s);
+    if (e == cudaSuccess) e = launch_prefill_merge(pp, plan.pre_groups, s);
     timing_end(h, PKV_KERNEL_PREFILL, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
   }

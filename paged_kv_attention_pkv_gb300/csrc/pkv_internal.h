@@ -98,6 +98,11 @@ struct PrefillParams {
   int64_t num_blocks;
   float scale_log2;
   int32_t validate;
+  // items split over key ranges (part >= 0): partial slots shared with the
+  // decode items (a prefill partial spans kPfPartSlots slots), merged by
+  // launch_prefill_merge
+  float *part_o;
+  float *part_lse;
 };
 
 struct AppendParams {
@@ -149,6 +154,9 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
 cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p,
                               int num_items, int kv_dtype, cudaStream_t s);
+// Merges the ranges of the first num_groups items of p.items (the first
+// ranges of the split prefill items) into bf16 rows and log-sum-exps.
+cudaError_t launch_prefill_merge(const PrefillParams &p, int num_groups, cudaStream_t s);
 cudaError_t launch_check(const CheckParams &p, cudaStream_t s);
 cudaError_t launch_lse_merge(const float *parts_o, const float *parts_lse, int num_parts,
                              int64_t num_rows, __nv_bfloat16 *out, float *lse,
@@ -165,6 +173,12 @@ cudaError_t launch_mixed(const CUtensorMap &qmap, const CUtensorMap &kmap_pf,
 // It needs G <= 128 (any pool format).
 constexpr int kPfQTile = 128;
 constexpr int pf_tile_rows(int G) { return G * (kPfQTile / G); }
+// A prefill item split over key ranges keeps one partial per range: 2 Q
+// tiles of 128 rows, i.e. kPfPartSlots decode partial slots; a range holds
+// at least kPfMinSplitTiles 128-key tiles.
+constexpr int kPfPartSlots = 2 * kPfQTile / kDecCols;
+constexpr int kPfMinSplitTiles = 2;
+constexpr int kPfMaxSplits = 32;
 inline bool prefill_uses_tc(const pkv_config &c) {
   const int G = c.num_q_heads / c.num_kv_heads;
   return G > 0 && G <= kPfQTile;

@@ -48,6 +48,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   prefill_tc_item<FMT>(qmap, kmap, vmap, p, p.items[blockIdx.x], smem);
 }
 
+// Merges the key-range partials of prefill items split over key ranges
+// (online-softmax combine: weights 2^(lse_s - max) over the ranges).  The
+// first ranges of the split items lead the item list; block b takes 8 rows
+// of group b / 32, one warp per row, lane l holding head dims 4l .. 4l + 3
+// and the log-sum-exp of range l (at most kPfMaxSplits ranges).
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams p) {
+  const pkv_work_item it = p.items[blockIdx.x >> 5];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int prow = (blockIdx.x & 31) * 8 + warp;   // line in a partial slot
+  const int t = prow >> 7, r = prow & 127;
+  const int G = p.group, R = pf_tile_rows(G);
+  const int n0 = it.n_rows < R ? it.n_rows : R;
+  if (r >= (t == 0 ? n0 : it.n_rows - n0)) return;
+  const int rowg = it.row0 + R * t + r;
+  const int64_t orow = static_cast<int64_t>(it.tok0 + rowg / G) * p.hq +
+                       it.kv_head * G + rowg % G;
+  const int ns = it.n_split;
+  auto slot = [&](int s2) {
+    return (static_cast<int64_t>(it.pair) + int64_t(s2) * kPfPartSlots) * kDecCols + prow;
+  };
+  const float lse_l = lane < ns ? __ldcg(p.part_lse + slot(lane)) : -CUDART_INF_F;
+  float M = lse_l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float Mu = M == -CUDART_INF_F ? 0.f : M;
+  float w_l = lane < ns ? exp2f(lse_l - Mu) : 0.f;
+  float wsum = w_l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  w_l *= wsum > 0.f ? 1.f / wsum : 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+  for (int s2 = 0; s2 < ns; ++s2) {
+    const float w = __shfl_sync(0xffffffffu, w_l, s2);
+    const float4 x = __ldcg(reinterpret_cast<const float4 *>(p.part_o + slot(s2) * kHeadDim) + lane);
+    acc.x += w * x.x;
+    acc.y += w * x.y;
+    acc.z += w * x.z;
+    acc.w += w * x.w;
+  }
+  reinterpret_cast<uint2 *>(p.out + orow * kHeadDim)[lane] =
+      make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[orow] = wsum > 0.f ? (Mu + log2f(wsum)) * kLn2 : -CUDART_INF_F;
+}
+
 template <int FMT>
 cudaError_t configure_one() {
   // setmaxnreg moves registers within the CTA's launch allotment: the split
@@ -76,6 +122,12 @@ cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
   else
     prefill_tc_kernel<PKV_KV_BF16><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap,
                                                                               vmap, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_merge(const PrefillParams &p, int num_groups, cudaStream_t s) {
+  if (num_groups == 0) return cudaSuccess;
+  prefill_merge_kernel<<<num_groups * 32, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

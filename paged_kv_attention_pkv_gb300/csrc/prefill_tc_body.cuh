@@ -149,12 +149,19 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
   const int n0 = it.n_rows < R ? it.n_rows : R;
   const int n1 = it.n_rows - n0;
   const bool two = n1 > 0;
-  const int kend0 = it.hist + (it.row0 + n0 - 1) / G + 1;
-  const int kend1 = two ? it.hist + (it.row0 + R + n1 - 1) / G + 1 : kend0;
-  const int k_end = it.k_end;                   // = kend1
-  const int nt0 = (kend0 + 127) / 128;
-  const int nt1 = two ? (kend1 + 127) / 128 : 0;
-  const int n_tiles = (k_end + 127) / 128;      // = max(nt0, nt1)
+  // This item covers keys [kb, k_end): the whole causal range, or one range
+  // of a split item (kb a multiple of 128 and of the block size, at or below
+  // every row's position, so each row sees at least one key here).  Local
+  // tile j holds keys kb + 128 j ...; the producers and converters count keys
+  // from kb (kspan of them) and read the block table from block kb / bs.
+  const int kb = it.k_begin;
+  const int k_end = it.k_end;
+  const int kspan = k_end - kb;
+  const int kend0 = min(it.hist + (it.row0 + n0 - 1) / G + 1, k_end);
+  const int kend1 = two ? min(it.hist + (it.row0 + R + n1 - 1) / G + 1, k_end) : kend0;
+  const int nt0 = (kend0 - kb + 127) / 128;
+  const int nt1 = two ? (kend1 - kb + 127) / 128 : 0;
+  const int n_tiles = (k_end - kb + 127) / 128;   // = max(nt0, nt1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -208,13 +215,13 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     uint8_t *ring = smem + (is_k ? kOffK : kOffV);
     uint64_t *full = is_k ? k_full : v_full;
     uint64_t *empty = is_k ? k_empty : v_empty;
-    const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride + kb / p.bs;
     const int br = p.bs < 128 ? p.bs : 128;
     const int nbox = 128 / br;  // <= 8
     auto tile_rows = [&](int j) {
       const int key = j * 128 + lane * br;
       int32_t y = p.rows_total;
-      if (lane < nbox && j < n_tiles && key < k_end) {
+      if (lane < nbox && j < n_tiles && key < kspan) {
         const int32_t blk = __ldg(bt + key / p.bs);
         if (blk >= 0 && blk < p.num_blocks)
           y = (blk * p.hkv + it.kv_head) * p.bs + key % p.bs;
@@ -247,7 +254,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       uint8_t *dst = ring + s * kTile;
       int n = 0;
       for (int r = 0; r < 128; r += br)
-        if (j * 128 + r < k_end) ++n;
+        if (j * 128 + r < kspan) ++n;
       if (lane == 0) mbar_arrive_expect_tx(&full[s], n * br * 128 * 2);
       for (int bx = 0; bx < n; ++bx) {
         const int32_t y = __shfl_sync(0xffffffffu, y_cur, bx);
@@ -262,7 +269,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     // ---------------- TMA producer, E4M3 pools: Q, the E4M3 K ring, the
     // E4M3 V staging ring (one box per block, no column halves), and each
     // tile's block scales for the softmax and the converters ----
-    const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride + kb / p.bs;
     const int br = p.bs < 128 ? p.bs : 128;
     const int nbox = 128 / br;  // <= 8
     // lane b < nbox: pool row of box b of tile j, and its block's scales
@@ -270,7 +277,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       const int key = j * 128 + lane * br;
       int32_t y = p.rows_total;
       sk = sv = 1.f;
-      if (lane < nbox && j < n_tiles && key < k_end) {
+      if (lane < nbox && j < n_tiles && key < kspan) {
         const int32_t blk = __ldg(bt + key / p.bs);
         if (blk >= 0 && blk < p.num_blocks) {
           y = (blk * p.hkv + it.kv_head) * p.bs + key % p.bs;
@@ -311,7 +318,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       if (lane == 0) mbar_arrive(&sc_ready[j % kScaleRing]);
       int n = 0;
       for (int r = 0; r < 128; r += br)
-        if (j * 128 + r < k_end) ++n;
+        if (j * 128 + r < kspan) ++n;
       // K tile j once the QKs of tile j - kKst are done
       const int s = j % kKst;
       if (j >= kKst &&
@@ -367,7 +374,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       for (int i = 0; i < 2; ++i) {
         const int k = rbase + lane + 32 * i;   // key row in the tile
         const uint32_t sw = k & 7;
-        if (j * 128 + k >= k_end) {
+        if (j * 128 + k >= kspan) {
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -406,7 +413,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     // ring (2 deep), the NVFP4 V staging tile (1 deep), and each tile's block
     // scales.  A group of min(bs, 64) rows is contiguous in the pool (codes
     // then micro scales), so one box of 9/8 rows per row brings both ----
-    const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride + kb / p.bs;
     const int gs = p.bs < kNvfp4Group ? p.bs : kNvfp4Group;
     const int ngrp = 128 / gs;  // <= 8
     const int tile_rows = p.bs / 8 * 9, group_rows = gs / 8 * 9;
@@ -415,7 +422,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       const int key = j * 128 + lane * gs;
       int32_t y = p.rows_total;
       sk = sv = 1.f;
-      if (lane < ngrp && j < n_tiles && key < k_end) {
+      if (lane < ngrp && j < n_tiles && key < kspan) {
         const int32_t blk = __ldg(bt + key / p.bs);
         if (blk >= 0 && blk < p.num_blocks) {
           y = (blk * p.hkv + it.kv_head) * tile_rows + (key % p.bs) / gs * group_rows;
@@ -455,7 +462,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       if (lane == 0) mbar_arrive(&sc_ready[j % kScaleRing]);
       int n = 0;
       for (int r = 0; r < 128; r += gs)
-        if (j * 128 + r < k_end) ++n;
+        if (j * 128 + r < kspan) ++n;
       // K tile j into staging j & 1 once the converters are done with j - 2
       const int k2 = j & 1;
       if (j >= 2 &&
@@ -503,7 +510,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         const int k = rbase + 8 * ps;   // key row in the tile
         const uint32_t sw = k & 7;
         uint32_t o[16];
-        if (j * 128 + k >= k_end) {
+        if (j * 128 + k >= kspan) {
 #pragma unroll
           for (int q = 0; q < 16; ++q) o[q] = 0u;
         } else {
@@ -690,7 +697,9 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     const uint32_t col_s = t * 128, col_o = 256 + t * 128;
     const int rowg = it.row0 + R * t + r;
     const bool row_ok = r < nrow;
-    const int pos = it.hist + rowg / G;   // padded rows see every key
+    // this row's position relative to the item's first key (padded rows
+    // see every key)
+    const int pos = it.hist + rowg / G - kb;
     float c = p.scale_log2;
     float m = -CUDART_INF_F;              // running max, log2 units
     float l = 0.f;
@@ -776,7 +785,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         break;
       }
       tc_fence_after();
-      const int key0 = j * 128;
+      const int key0 = j * 128;   // relative to kb, like pos
       // one pass: the whole S row in registers (one TMEM load)
       float s[128];
       tmem_ld128(lane_addr + col_s, s);
@@ -872,8 +881,8 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       // them.  Q tile 0 does it when it reaches that tile (its PV comes
       // first), otherwise Q tile 1.  (E4M3 and NVFP4 pools: the converters write
       // those rows as zeros.)
-      if (!CONV && j == n_tiles - 1 && k_end - key0 < 128 && (t == 0 || nt0 < n_tiles)) {
-        const int vvalid = k_end - key0;
+      if (!CONV && j == n_tiles - 1 && kspan - key0 < 128 && (t == 0 || nt0 < n_tiles)) {
+        const int vvalid = kspan - key0;
         const int vs = j % kVst;
         if (!__all_sync(0xffffffffu, mbar_wait(&v_full[vs], (j / kVst) & 1))) {
           ok = false;
@@ -894,20 +903,31 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       tc_fence_before();
       mbar_arrive(&p_full[t]);
     }
-    // ---- epilogue: O / l -> bf16
+    // ---- epilogue: O / l -> bf16; an item split over key ranges writes
+    // this range's partial (O / l in fp32, log-sum-exp in log2 units) for
+    // prefill_merge_kernel instead
     if (ntl > 0) {
       const int J = ntl - 1;
       if (__all_sync(0xffffffffu, ok && mbar_wait(&o_done[t], J & 1))) {
         tc_fence_after();
+        const bool split = it.part >= 0;
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int64_t orow = static_cast<int64_t>(it.tok0 + rowg / G) * p.hq +
                              it.kv_head * G + rowg % G;
+        // this row's line in the range's partial slot
+        const int64_t pline = static_cast<int64_t>(split ? it.part : 0) * kDecCols + t * 128 + r;
         uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kHeadDim);
+        float4 *pdst = reinterpret_cast<float4 *>(p.part_o + pline * kHeadDim);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float v[64];
           tmem_ld64(lane_addr + col_o + 64 * hh, v);
-          if (row_ok) {
+          if (row_ok && split) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pdst[16 * hh + i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv,
+                                              v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+          } else if (row_ok) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               dst[8 * hh + i] = make_uint4(pack_bf16(v[8 * i] * inv, v[8 * i + 1] * inv),
@@ -916,8 +936,11 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
                                            pack_bf16(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
           }
         }
-        if (row_ok && p.lse != nullptr)
-          p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
+        const float lse2 = l > 0.f ? m + log2f(l) : -CUDART_INF_F;
+        if (row_ok && split)
+          p.part_lse[pline] = lse2;
+        else if (row_ok && p.lse != nullptr)
+          p.lse[orow] = lse2 * kLn2;
       } else {
         record_error(p.err, kErrTimeout);
       }

@@ -127,6 +127,13 @@ SWEEP = [
     ("fp8_prefill_gqa96", 96, 1, 32, [1, 3, 5], [64, 700, 5], "fp8"),
     ("nvfp4_prefill_gqa12", 96, 8, 16, [11, 25], [400, 25], "nvfp4"),
     ("nvfp4_prefill_gqa96", 96, 1, 32, [1, 3, 5], [64, 700, 5], "nvfp4"),
+    # few prefill tiles: key ranges split over the SMs, merged by the last
+    # range to finish (boundaries at or below each tile's first position)
+    ("split_q16_long", 32, 8, 16, [16], [8208], "bf16"),
+    ("split_gqa3", 24, 8, 16, [300, 1], [2300, 900], "bf16"),
+    ("split_bs256", 8, 2, 256, [33, 2], [3000, 700], "bf16"),
+    ("split_fp8", 32, 8, 64, [40], [6000], "fp8"),
+    ("split_nvfp4", 32, 8, 16, [40, 1], [6000, 3000], "nvfp4"),
 ]
 
 

@@ -17,13 +17,15 @@ def _plan(spec, num_sms=152):
     return items, parts, qsl
 
 
-@pytest.mark.parametrize("index", range(5))
-def test_plan_covers_the_workloads(index):
-    spec = workloads.config_spec(index)
-    items, parts, qsl = _plan(spec)
+PF_PART_SLOTS = 32     # a split prefill item's partial: 256 rows = 32 decode slots
+
+
+def _check_plan(spec, num_sms=152):
+    items, parts, qsl = _plan(spec, num_sms)
     G = spec.hq // spec.hkv
     dec_keys = {}
     rows = {}
+    ranges = {}
     slots = []
     for w in items:
         i, h = w["seq"], w["kv_head"]
@@ -32,6 +34,8 @@ def test_plan_covers_the_workloads(index):
         if w["kind"] == 0 and q * G <= 8:
             assert w["row0"] == 0 and w["n_rows"] == q * G
             dec_keys.setdefault((i, h), []).append((w["k_begin"], w["k_end"], w))
+            if w["part"] >= 0:
+                slots.append(w["part"])
         else:
             assert q * G > 8
             # G <= 128 uses tensor-core tiles (every pool format), larger
@@ -39,12 +43,12 @@ def test_plan_covers_the_workloads(index):
             assert w["kind"] == (1 if G <= 128 else 0)
             if w["kind"] == 0:
                 assert w["n_rows"] <= 8 and w["row0"] % 8 == 0 and w["part"] == -1
-            assert w["k_begin"] == 0
-            last_tok = (w["row0"] + w["n_rows"] - 1) // G
-            assert w["k_end"] == L - q + last_tok + 1          # causal reach
-            rows.setdefault((i, h), []).append((w["row0"], w["n_rows"]))
-        if w["part"] >= 0:
-            slots.append(w["part"])
+                assert w["k_begin"] == 0
+            ranges.setdefault((i, h, w["row0"], w["n_rows"]), []).append(w)
+            if w["k_begin"] == 0:
+                rows.setdefault((i, h), []).append((w["row0"], w["n_rows"]))
+            if w["part"] >= 0:
+                slots.extend(range(w["part"], w["part"] + PF_PART_SLOTS))
     # decode: the ranges of each (request, KV head) tile [0, L) in order
     for (i, h), rs in dec_keys.items():
         rs.sort()
@@ -58,6 +62,25 @@ def test_plan_covers_the_workloads(index):
                 assert w["part"] == -1 and w["pair"] == -1
             else:
                 assert w["part"] == w["pair"] + k          # contiguous slots
+    # prefill: the key ranges of each row tile cover its causal reach in
+    # order, split at multiples of 128 no later than the tile's first query
+    # position (every row sees a key of every range)
+    for (i, h, row0, n_rows), ws in ranges.items():
+        ws.sort(key=lambda w: w["k_begin"])
+        hist = spec.seq_lens[i] - spec.q_lens[i]
+        reach = hist + (row0 + n_rows - 1) // G + 1
+        assert ws[0]["k_begin"] == 0 and ws[-1]["k_end"] == reach
+        ns = len(ws)
+        for k, w in enumerate(ws):
+            assert w["n_split"] == ns
+            assert w["k_begin"] % max(128, spec.block_size) == 0
+            assert w["k_begin"] <= hist + row0 // G
+            if k + 1 < ns:
+                assert w["k_end"] == ws[k + 1]["k_begin"]
+            if ns == 1:
+                assert w["part"] == -1 and w["pair"] == -1
+            else:
+                assert w["part"] == w["pair"] + PF_PART_SLOTS * k
     # prefill: tiles of each (request, KV head) cover rows [0, q*G)
     for (i, h), rs in rows.items():
         rs.sort()
@@ -67,6 +90,40 @@ def test_plan_covers_the_workloads(index):
     # every (request, KV head) pair with tokens appears
     seen = set(dec_keys) | set(rows)
     assert len(seen) == sum(1 for q in spec.q_lens if q > 0) * spec.hkv
+    return items, parts
+
+
+@pytest.mark.parametrize("index", range(5))
+def test_plan_covers_the_workloads(index):
+    items, _ = _check_plan(workloads.config_spec(index))
+    if index in (2, 3):
+        # thousands of prefill tiles fill the machine: no key-range splits
+        assert all(w["part"] == -1 for w in items if w["kind"] == 1)
+
+
+@pytest.mark.parametrize("hq,hkv,q_lens,seq_lens", [
+    (32, 8, [16], [32784]),                  # a few new tokens over a long history
+    (32, 8, [64], [4160]),
+    (8, 2, [64], [1064]),                    # the tiny prefill workload's shape
+    (24, 8, [300], [2300]),                  # G = 3: rows in whole tokens
+    (40, 8, [5, 77], [9000, 20077]),         # G = 5
+    (32, 8, [1] * 6 + [48], [5000] * 6 + [40048]),   # decodes beside a small prefill
+    (32, 8, [20], [100]),                    # short history: too few tiles to split
+])
+def test_small_prefills_split_their_key_ranges(hq, hkv, q_lens, seq_lens):
+    spec = workloads.custom_spec("split", hq, hkv, 16, q_lens, seq_lens)
+    items, parts = _check_plan(spec)
+    pre = [w for w in items if w["kind"] == 1]
+    tiles = sum((w["k_end"] - w["k_begin"] + 127) // 128 for w in pre)
+    if max(seq_lens) >= 4096:
+        # split: about one range per SM, each of at least two 128-key tiles
+        assert any(w["n_split"] > 1 for w in pre)
+        assert len(pre) <= 2 * 152 and parts <= 16384
+        assert all((w["k_end"] - w["k_begin"] + 127) // 128 >= 1 for w in pre)
+        assert max((w["k_end"] - w["k_begin"] + 127) // 128 for w in pre) <= \
+            max(2, -(-2 * tiles // 152))
+    if max(seq_lens) <= 128:
+        assert all(w["n_split"] == 1 for w in pre)
 
 
 def test_plan_orders_longest_first():
