@@ -463,7 +463,7 @@ def time_per_call(index, device: str, calls: int = 20, warmup: int = 5) -> dict:
     before each call, outside its events.  The library's own per-kernel
     events give the device time of the kernels alone."""
     import paged_kv_attention_pkv_gb300 as pkv
-    spec = W.config_spec(index)
+    spec = W.config_spec(index) if isinstance(index, int) else index
     batch = W.generate(spec, device)
     h = make_handle(batch, pkv.FLAG_TIMING)
     m = device_meta(batch)
@@ -511,7 +511,12 @@ def time_per_call(index, device: str, calls: int = 20, warmup: int = 5) -> dict:
 
 def secondary(args, world, peaks, device):
     out = []
-    out.append({"per_call": [time_per_call(0, device), time_per_call(1, device)]})
+    # one session's post-tool-call prefill alone: 64 new tokens over a
+    # 48000-token history (the median of the post-tool-call workload)
+    one_session = W.custom_spec("one_session_post_tool_prefill_q64_h48000", 32, 8, 16,
+                                [64], [48064], seed=1002)
+    out.append({"per_call": [time_per_call(0, device), time_per_call(1, device),
+                             time_per_call(one_session, device)]})
     out.append({"cuda_graph": [time_graph(0, 500, device), time_graph(1, 200, device)]})
     nvfp4 = dataclasses.replace(W.config_spec(4), name="c5_nvfp4_long_decode",
                                 kv_dtype="nvfp4")

@@ -190,7 +190,13 @@ pkv_status pkv_rope_write_slots(pkv_handle *h, void *q, const void *k_new,
  * Requests with more than 8 query rows per KV head (q_i * G > 8) run on the
  * tensor-core prefill kernel when G <= 128 (every pool format); with
  * G > 128 the decode kernel takes their rows 8 at a time (same results within
- * tolerance, at memory-bound speed).
+ * tolerance, at memory-bound speed).  When a step holds fewer tensor-core
+ * prefill items than half the multiprocessors, their key ranges are split
+ * into runs of whole 128-key tiles (boundaries at multiples of the block
+ * size too, at or below each item's first query position); each range
+ * writes an fp32 partial and a second kernel merges them with log-sum-exp
+ * weights (the combine of decode splits), inside the same timed launch
+ * window.
  */
 pkv_status pkv_attention_varlen(pkv_handle *h, const void *q,
                                 const void *k_cache, const void *v_cache,
@@ -311,16 +317,21 @@ typedef struct {
     int32_t hist;        /* l_hist = L - q of the request */
     int32_t k_begin;     /* first key position */
     int32_t k_end;       /* one past the last key position */
-    int32_t part;        /* partial-result slot, or -1: writes the output */
-    int32_t pair;        /* combine ticket index, or -1 */
-    int32_t n_split;     /* splits of this (request, KV head) */
+    int32_t part;        /* partial-result slot, or -1: writes the output.
+                            A split prefill item's partial takes 32
+                            consecutive slots (256 rows of 8) */
+    int32_t pair;        /* slot of the first range of the split (decode:
+                            its combine ticket), or -1 */
+    int32_t n_split;     /* key ranges of this (request, KV head, rows) */
 } pkv_work_item;
 
 /*
  * Plan a step on the host without a GPU: the work items the kernels of
  * pkv_attention_varlen would run for these lengths on a device with
  * `num_sms` multiprocessors.  Items of each kind are in launch order
- * (longest first; the prefill items of one (request, KV head) adjacent).  *num_items receives the count; if it exceeds
+ * (longest first; the prefill items of one (request, KV head) adjacent,
+ * after the first ranges of split prefill items, which lead the prefill
+ * items).  *num_items receives the count; if it exceeds
  * max_items only the first max_items are stored.  *num_partials receives the
  * split partial slots used.  Errors: PKV_ERR_INVALID_ARG for inconsistent
  * metadata (same checks as pkv_attention_varlen).
@@ -333,7 +344,8 @@ pkv_status pkv_plan(const pkv_config *config, const int32_t *query_start_loc_hos
 
 /* Kernel kinds reported by pkv_timing_read.  A step holding both decodes
  * and prefill chunks (bf16 pools, query groups of at most 128) runs as
- * one PKV_KERNEL_MIXED launch; otherwise decode and prefill launch apart. */
+ * one PKV_KERNEL_MIXED launch; otherwise decode and prefill launch apart.
+ * The merge of split prefill ranges is timed with the launch it follows. */
 enum {
     PKV_KERNEL_APPEND = 0,
     PKV_KERNEL_DECODE = 1,

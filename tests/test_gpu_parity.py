@@ -287,6 +287,17 @@ def test_run_to_run_deterministic():
     assert torch.equal(lse1, lse2)
 
 
+def test_split_prefill_is_deterministic():
+    """Key ranges of split prefill items merge in a fixed order: two runs of
+    the same step give the same bits."""
+    s = spec("det_split", 32, 8, 16, [16, 40], [8208, 3000])
+    b = W.generate(s, DEV)
+    out1, lse1 = U.gpu_step(b)
+    out2, lse2 = U.gpu_step(b, append=False)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+
+
 def test_chunked_prefill_matches_one_shot():
     """The same 200 new tokens as one chunk or as chunks of 70/1/129, each
     appended first and attending to history + earlier chunks."""
