@@ -271,48 +271,81 @@ def time_workload(index, steps: int, warmup: int, world: int, peaks: dict,
 
 def time_e2e(h, batch, m, out, steps, stream, world):
     """Same step through the public API with the step's inputs in pinned host
-    memory: H2D of q, new K/V, slots and metadata, the step, D2H of out."""
+    memory: H2D of q, new K/V, slots and metadata, the step, D2H of out.
+    Copies run on two copy streams, double-buffered as a serving loop would
+    run them: step i+1's inputs go up while step i computes, step i's output
+    comes back while step i+1 computes.  The timed region opens before the
+    first upload and closes after the last download."""
     src = {"q": batch.q, "k_new": batch.k_new, "v_new": batch.v_new, "slots": m["slots"],
            "qsl": m["qsl"], "lens": m["lens"], "bt": m["bt"]}
     # the step's inputs packed into one pinned buffer (256-byte aligned
-    # fields) and brought over with one copy; the device views alias one
-    # device buffer
+    # fields), brought over with one copy into one of two device buffers
     offs, total = {}, 0
     for k, v in src.items():
         offs[k] = total
         total += (v.numel() * v.element_size() + 255) // 256 * 256
     host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
-    dev_buf = torch.empty(total, dtype=torch.uint8, device=batch.q.device)
-    dev = {}
+    dev_bufs = [torch.empty(total, dtype=torch.uint8, device=batch.q.device) for _ in range(2)]
+    devs = [{}, {}]
     for k, v in src.items():
         n = v.numel() * v.element_size()
         host_buf[offs[k]:offs[k] + n].copy_(v.contiguous().view(-1).view(torch.uint8).cpu())
-        dev[k] = dev_buf[offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        for b in range(2):
+            devs[b][k] = dev_bufs[b][offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
+    outs = [out, torch.empty_like(out)]
+    out_hosts = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in src.values())
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = out_hosts[0].numel() * out_hosts[0].element_size()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()   # noqa: E731
+    uploaded = [ev(), ev()]     # inputs of buffer b are on the device
+    consumed = [ev(), ev()]     # the step reading buffer b (and writing out b) is done
+    fetched = [ev(), ev()]      # out b is back on the host
 
-    def step():
-        dev_buf.copy_(host_buf, non_blocking=True)
-        h.write_slots(dev["k_new"], dev["v_new"], dev["slots"], batch.k_cache,
-                      batch.v_cache, batch.k_scale, batch.v_scale, stream=stream)
-        h.attention_varlen(dev["q"], batch.k_cache, batch.v_cache, dev["qsl"], dev["lens"],
-                           dev["bt"], batch.qsl, batch.seq_lens, out=out,
-                           k_scale=batch.k_scale, v_scale=batch.v_scale, stream=stream)
-        out_host.copy_(out, non_blocking=True)
+    def upload(i):
+        b = i & 1
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(consumed[b])
+            dev_bufs[b].copy_(host_buf, non_blocking=True)
+            uploaded[b].record(up)
 
-    for _ in range(3):
-        step()
+    def run(n):
+        upload(0)
+        for i in range(n):
+            b = i & 1
+            if i + 1 < n:
+                upload(i + 1)
+            stream.wait_event(uploaded[b])
+            if i >= 2:
+                stream.wait_event(fetched[b])
+            d = devs[b]
+            h.write_slots(d["k_new"], d["v_new"], d["slots"], batch.k_cache,
+                          batch.v_cache, batch.k_scale, batch.v_scale, stream=stream)
+            h.attention_varlen(d["q"], batch.k_cache, batch.v_cache, d["qsl"], d["lens"],
+                               d["bt"], batch.qsl, batch.seq_lens, out=outs[b],
+                               k_scale=batch.k_scale, v_scale=batch.v_scale, stream=stream)
+            consumed[b].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(consumed[b])
+                out_hosts[b].copy_(outs[b], non_blocking=True)
+                fetched[b].record(down)
+        for b in range(min(n, 2)):
+            stream.wait_event(fetched[b])
+
+    run(3)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(steps):
-        step()
+    up.wait_stream(stream)
+    run(steps)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), world)
-    return {"ms_per_step": ms / steps, "h2d": h2d, "d2h": d2h, "steps": steps}
+    return {"ms_per_step": ms / steps, "h2d": h2d, "d2h": d2h, "steps": steps,
+            "copies": "two copy streams, double-buffered (uploads of step i+1 and the "
+                      "download of step i overlap step i+1's kernels)"}
 
 
 def roofline_decode(res, peaks, traffic):
