@@ -31,6 +31,12 @@
 //               running max in log2 units that only moves when it grows by
 //               more than 8 (O is rescaled rarely), writes P, and finally
 //               normalises O.
+//
+// A step with few items has their key ranges split into runs of whole tiles
+// (one item per run); each run writes O / l and its log-sum-exp as a partial
+// and prefill_merge_kernel combines the runs of each item, the log-sum-exp
+// merge of split attention (page "vLLM Agentic 推理｜面向 Agent 负载的推理
+// 优化", section 4.3.3).
 #include "prefill_tc_body.cuh"
 
 namespace pkv {
