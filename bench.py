@@ -251,7 +251,8 @@ def time_workload(index, steps: int, warmup: int, world: int, peaks: dict,
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     per_kind = {}
     for kind, name in ((pkv.KERNEL_APPEND, "append"), (pkv.KERNEL_DECODE, "decode"),
-                       (pkv.KERNEL_PREFILL, "prefill"), (pkv.KERNEL_MIXED, "mixed")):
+                       (pkv.KERNEL_PREFILL, "prefill"), (pkv.KERNEL_MIXED, "mixed"),
+                       (pkv.KERNEL_MERGE, "merge")):
         n, tot = h.timing_read(kind)
         if n:
             per_kind[name] = (n, tot / n)
@@ -529,7 +530,7 @@ def time_per_call(index, device: str, calls: int = 20, warmup: int = 5) -> dict:
             spans.append(e0.elapsed_time(e1) * 1e3)
         kernels_us = 0.0
         for kind in (pkv.KERNEL_APPEND, pkv.KERNEL_DECODE, pkv.KERNEL_PREFILL,
-                     pkv.KERNEL_MIXED):
+                     pkv.KERNEL_MIXED, pkv.KERNEL_MERGE):
             n, tot = h.timing_read(kind)
             if n:
                 kernels_us += tot / n * 1e3
@@ -590,11 +591,14 @@ def secondary(args, world, peaks, device):
                               "flops_per_launch": work["prefill_flops"]}
         if work["decode_bytes"]:
             n, avg = r["kinds"]["decode"]
+            # the decode kernel and the merge of its split ranges
+            avg += r["kinds"].get("merge", (0, 0.0))[1]
             gb = work["decode_bytes"] / (avg * 1e-3) / 1e9
             ent["decode"] = {"value": round(gb, 1), "unit": "GB/s", "bound": "hbm",
                              "frac": round(gb / peaks["hbm_gbs"], 4),
                              "peak": peaks["hbm_gbs"],
-                             "bytes_per_launch": work["decode_bytes"]}
+                             "bytes_per_launch": work["decode_bytes"],
+                             "ms": round(avg, 4), "includes": "decode kernel + range merge"}
         if work["prefill_flops"] and work["decode_bytes"]:
             t_ideal = (work["decode_bytes"] / (peaks["hbm_gbs"] * 1e9) +
                        work["prefill_flops"] / (peaks["bf16_tflops"] * 1e12))

@@ -107,7 +107,7 @@ typedef struct {
 
 /*
  * Create a handle on CUDA device `device` and allocate its workspace (work
- * list, split partials, combine tickets, error word: a few tens of MB,
+ * list, split partials, error word: a few tens of MB,
  * sized from max_num_seqs and max_num_tokens).  *out receives the handle, or
  * NULL on failure.  Errors: PKV_ERR_INVALID_ARG (NULL pointers, bad config),
  * PKV_ERR_UNSUPPORTED (head_dim or block_size not handled), PKV_ERR_CUDA (no
@@ -195,8 +195,8 @@ pkv_status pkv_rope_write_slots(pkv_handle *h, void *q, const void *k_new,
  * into runs of whole 128-key tiles (boundaries at multiples of the block
  * size too, at or below each item's first query position); each range
  * writes an fp32 partial and a second kernel merges them with log-sum-exp
- * weights (the combine of decode splits), inside the same timed launch
- * window.
+ * weights, as it merges the key ranges of split decode items
+ * (PKV_KERNEL_MERGE).
  */
 pkv_status pkv_attention_varlen(pkv_handle *h, const void *q,
                                 const void *k_cache, const void *v_cache,
@@ -320,8 +320,7 @@ typedef struct {
     int32_t part;        /* partial-result slot, or -1: writes the output.
                             A split prefill item's partial takes 32
                             consecutive slots (256 rows of 8) */
-    int32_t pair;        /* slot of the first range of the split (decode:
-                            its combine ticket), or -1 */
+    int32_t pair;        /* slot of the first range of the split, or -1 */
     int32_t n_split;     /* key ranges of this (request, KV head, rows) */
 } pkv_work_item;
 
@@ -330,8 +329,8 @@ typedef struct {
  * pkv_attention_varlen would run for these lengths on a device with
  * `num_sms` multiprocessors.  Items of each kind are in launch order
  * (longest first; the prefill items of one (request, KV head) adjacent,
- * after the first ranges of split prefill items, which lead the prefill
- * items).  *num_items receives the count; if it exceeds
+ * after the first ranges of split items, which lead the decode and the
+ * prefill items).  *num_items receives the count; if it exceeds
  * max_items only the first max_items are stored.  *num_partials receives the
  * split partial slots used.  Errors: PKV_ERR_INVALID_ARG for inconsistent
  * metadata (same checks as pkv_attention_varlen).
@@ -345,13 +344,16 @@ pkv_status pkv_plan(const pkv_config *config, const int32_t *query_start_loc_hos
 /* Kernel kinds reported by pkv_timing_read.  A step holding both decodes
  * and prefill chunks (bf16 pools, query groups of at most 128) runs as
  * one PKV_KERNEL_MIXED launch; otherwise decode and prefill launch apart.
- * The merge of split prefill ranges is timed with the launch it follows. */
+ * PKV_KERNEL_MERGE: the merge of split key ranges (decode pairs and prefill
+ * row tiles), one window after the attention launches of a step that split
+ * any ranges. */
 enum {
     PKV_KERNEL_APPEND = 0,
     PKV_KERNEL_DECODE = 1,
     PKV_KERNEL_PREFILL = 2,
     PKV_KERNEL_MIXED = 3,
-    PKV_KERNEL_KINDS = 4
+    PKV_KERNEL_MERGE = 4,
+    PKV_KERNEL_KINDS = 5
 };
 
 /*
@@ -381,8 +383,8 @@ pkv_status pkv_timing_read(pkv_handle *h, int32_t kind, int32_t *launches,
  * exactly as for pkv_attention_varlen (same layouts and meaning, minus the
  * device copies of query_start_loc and seq_lens, which are not read) and a
  * config describing the pools (max_num_seqs, max_num_tokens and flags are
- * ignored).  Nothing is allocated: the work list, split partials and combine
- * tickets live in one fixed array of about 4.3 MB compiled into the library,
+ * ignored).  Nothing is allocated: the work list, split partials and the
+ * error word live in one fixed array of about 4.3 MB compiled into the library,
  * which every GPU that loads the library keeps until the process exits.
  * Limits: at most 2048 work items and 1024 split partials per call (the split
  * size grows to fit; a batch with more than 2048 (request, KV head) pairs is
@@ -391,7 +393,8 @@ pkv_status pkv_timing_read(pkv_handle *h, int32_t kind, int32_t *launches,
  *    the kernel's shared-memory limit; make that first call before any stream
  *    capture.
  *  - Every call shares the array and leaves its contents behind; each call
- *    clears what must start at zero.  Calls whose GPU work overlaps (on
+ *    clears what must start at zero.  A call runs the decode kernel and,
+ *    when it split any key range, the merge kernel.  Calls whose GPU work overlaps (on
  *    different streams, or from different threads) race on it: serialise
  *    them.
  *  - Returns PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED (prefill rows,

@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                 7: "PKV_ERR_WORKSPACE"}
 KV_BF16, KV_FP8_E4M3, KV_NVFP4 = 0, 1, 2
 FLAG_VALIDATE, FLAG_TIMING, FLAG_SEPARATE = 1, 2, 4
-KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL, KERNEL_MIXED = 0, 1, 2, 3
+KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL, KERNEL_MIXED, KERNEL_MERGE = 0, 1, 2, 3, 4
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ["pkv_create", "pkv_write_slots", "pkv_attention_varlen",

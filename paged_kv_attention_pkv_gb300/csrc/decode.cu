@@ -9,8 +9,10 @@
 // 16 rows are keys (S^T = K Q^T), so a KV head's rows are read once for the
 // whole group (GQA, same page section 4.3.1).  Ranges of one (request, KV
 // head) are merged through their log-sum-exp (same page, section 4.3.3 step
-// 4; section 5.2 "Split Attention + Combine"): the last CTA to finish a range
-// does the merge, in range order, so results do not depend on timing.
+// 4; section 5.2 "Split Attention + Combine") by decode_merge_kernel, in
+// range order, so results do not depend on timing.  (A merge by the last CTA
+// to finish, inside this kernel, measured slower: it lengthened the tail and
+// changed how the decode loop was compiled.)
 //
 // Data movement: each of the 4 warps owns a ring of 3 stages in shared
 // memory.  Lane 0 fills a stage with 2D TMA tile copies of the (block, KV
@@ -47,7 +49,68 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasNvfp4)
   decode_item_nvfp4<kDecWarps>(kmap, vmap, p, p.items[blockIdx.x], smem, threadIdx.x, 0);
 }
 
+// Merges the key ranges of split decode items.  The first ranges of the
+// split (request, KV head) pairs lead the item list; block b takes pair b,
+// warp n its row n (up to kDecCols rows), lane l head dims 4l .. 4l + 3.
+// Weights 2^(lse_s - max) / sum over the ranges (lanes striding over the
+// ranges for the max and the sum), then the ranges' rows accumulated with
+// independent loads.
+__global__ void __launch_bounds__(kDecCols * 32) decode_merge_kernel(const DecodeParams p) {
+  const pkv_work_item it = p.items[blockIdx.x];
+  const int n = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (n >= it.n_rows) return;
+  const int ns = it.n_split;
+  const float *lse_p = p.part_lse + static_cast<int64_t>(it.pair) * kDecCols + n;
+  const float *o_p = p.part_o + (static_cast<int64_t>(it.pair) * kDecCols + n) * kHeadDim;
+  constexpr int64_t kSlotFloats = int64_t(kDecCols) * kHeadDim;
+  // lane l holds the log-sum-exp of range l (the first 32 ranges: one load
+  // serves the max, the sum and the weights of most merges)
+  const float lse0 = lane < ns ? __ldcg(lse_p + lane * kDecCols) : -CUDART_INF_F;
+  float M = lse0;
+  for (int s2 = lane + 32; s2 < ns; s2 += 32) M = fmaxf(M, __ldcg(lse_p + s2 * kDecCols));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float Mu = M == -CUDART_INF_F ? 0.f : M;
+  float Ls = lane < ns ? exp2f(lse0 - Mu) : 0.f;
+  for (int s2 = lane + 32; s2 < ns; s2 += 32) Ls += exp2f(__ldcg(lse_p + s2 * kDecCols) - Mu);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+  const float winv = Ls > 0.f ? 1.f / Ls : 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < ns; s0 += 32) {
+    const int s2 = s0 + lane;
+    const float lse_s = s0 == 0 ? lse0 : (s2 < ns ? __ldcg(lse_p + s2 * kDecCols) : -CUDART_INF_F);
+    const float w_l = s2 < ns ? exp2f(lse_s - Mu) * winv : 0.f;
+    const int cnt = ns - s0 < 32 ? ns - s0 : 32;
+#pragma unroll 8
+    for (int k = 0; k < cnt; ++k) {
+      const float w = __shfl_sync(0xffffffffu, w_l, k);
+      const float4 x = __ldcg(reinterpret_cast<const float4 *>(o_p + (s0 + k) * kSlotFloats) + lane);
+      acc.x += w * x.x;
+      acc.y += w * x.y;
+      acc.z += w * x.z;
+      acc.w += w * x.w;
+    }
+  }
+  const int r = it.row0 + n;
+  const int64_t row = static_cast<int64_t>(it.tok0 + r / p.group) * p.hq +
+                      it.kv_head * p.group + r % p.group;
+  if (p.out_f32 != nullptr)
+    reinterpret_cast<float4 *>(p.out_f32 + row * kHeadDim)[lane] = acc;
+  else
+    reinterpret_cast<uint2 *>(p.out + row * kHeadDim)[lane] =
+        make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[row] = Ls > 0.f ? (Mu + log2f(Ls)) * kLn2 : -CUDART_INF_F;
+}
+
 }  // namespace
+
+cudaError_t launch_decode_merge(const DecodeParams &p, int num_groups, cudaStream_t s) {
+  if (num_groups == 0) return cudaSuccess;
+  decode_merge_kernel<<<num_groups, kDecCols * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
                           const DecodeParams &p, int num_items, int kv_dtype,

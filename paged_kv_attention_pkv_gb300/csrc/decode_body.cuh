@@ -49,13 +49,14 @@ __device__ __forceinline__ int fp8_dmap(int mt, int dr) {
 }
 
 // End of a decode item, shared by the storage formats: merge the NW warps'
-// (max, sum, O) through shared memory, normalise, and write the rows (or
-// this range's partial, the last range to finish then merging all ranges).
+// (max, sum, O) through shared memory, normalise, and write the rows, or
+// this range's partial (O / l and the log-sum-exp), which decode_merge_kernel
+// combines with the other ranges of the (request, KV head).
 // `dmap(mt, dr)` is the head-dim index of row dr of m-tile mt of the O^T
 // accumulator; `acc_scale` undoes a power-of-two factor carried in acc.
 template <int NW, typename DMap>
 __device__ __forceinline__ void decode_finish(const DecodeParams &p, const pkv_work_item &it,
-                                              uint8_t *smem, int32_t *flag, const int tid,
+                                              uint8_t *smem, const int tid,
                                               const int bar, float m0, float m1, float l0,
                                               float l1, const float (&acc)[8][4],
                                               const float acc_scale, DMap dmap) {
@@ -126,33 +127,6 @@ __device__ __forceinline__ void decode_finish(const DecodeParams &p, const pkv_w
       if (d == 0) p.part_lse[static_cast<int64_t>(it.part) * kDecCols + n] = lse2;
     }
   }
-  if (it.part < 0) return;
-
-  // ---- last range of this (request, KV head) to finish merges all ranges
-  __threadfence();
-  sync();
-  if (tid == 0) {
-    const int prev = atomicAdd(p.tickets + it.pair, 1);
-    *flag = (prev == it.n_split - 1);
-  }
-  sync();
-  if (*flag == 0) return;
-  __threadfence();
-  for (int n = n_first; n < it.n_rows; n += n_step) {
-    float M = -CUDART_INF_F;
-    for (int s2 = 0; s2 < it.n_split; ++s2)
-      M = fmaxf(M, __ldcg(p.part_lse + static_cast<int64_t>(it.pair + s2) * kDecCols + n));
-    const float Mu = M == -CUDART_INF_F ? 0.f : M;
-    float Ls = 0.f, o = 0.f;
-    for (int s2 = 0; s2 < it.n_split; ++s2) {
-      const int64_t slot = it.pair + s2;
-      const float w = exp2f(__ldcg(p.part_lse + slot * kDecCols + n) - Mu);
-      Ls += w;
-      o += w * __ldcg(p.part_o + (slot * kDecCols + n) * kHeadDim + d);
-    }
-    write_row(n, Ls > 0.f ? o / Ls : 0.f, Ls > 0.f ? Mu + log2f(Ls) : -CUDART_INF_F);
-  }
-  if (tid == 0) p.tickets[it.pair] = 0;  // ready for the next step
 }
 
 // One decode work item processed by NW warps (threads tid = 0 .. 32 NW - 1
@@ -168,7 +142,6 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
   constexpr int kDecWarps = NW;
   uint64_t *bars = reinterpret_cast<uint64_t *>(
       smem + kDecWarps * kDecStages * kDecStageBytes);
-  int32_t *flag = reinterpret_cast<int32_t *>(bars + kDecWarps * kDecStages);
   auto sync = [&]() { named_barrier(bar, NW * 32); };
 
   const int warp = tid >> 5;
@@ -504,7 +477,7 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       mbar_wait(&full[i % kDecStages], (i / kDecStages) & 1);
   }
 
-  decode_finish<NW>(p, it, smem, flag, tid, bar, m0, m1, l0, l1, acc, 1.f,
+  decode_finish<NW>(p, it, smem, tid, bar, m0, m1, l0, l1, acc, 1.f,
                     [](int mt, int dr) { return FP8 ? fp8_dmap(mt, dr) : 16 * mt + dr; });
 }
 

@@ -63,7 +63,6 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
   constexpr int KS = kNvKeys;
   constexpr int S = kDecStagesNvfp4;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * S * kDecStageBytesNvfp4);
-  int32_t *flag = reinterpret_cast<int32_t *>(bars + NW * S);
   auto sync = [&]() { named_barrier(bar, NW * 32); };
   const int warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2;
@@ -361,7 +360,7 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
     const int issued = my_n < consumed + S ? my_n : consumed + S;
     for (int i = consumed; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1);
   }
-  decode_finish<NW>(p, it, smem, flag, tid, bar, m0, m1, l0, l1, acc, 1.f / kNvPScale,
+  decode_finish<NW>(p, it, smem, tid, bar, m0, m1, l0, l1, acc, 1.f / kNvPScale,
                     [](int mt, int dr) { return nvfp4_dmap(mt, dr); });
 }
 

@@ -7,9 +7,9 @@
 // pre-reserves HBM for its KV cache), code that must not allocate after
 // start-up for latency reasons, or host code that is not allowed to create a
 // handle (pkv_create allocates its workspace).  This entry point takes only
-// the caller's inputs and outputs; the work list, the split partials, the
-// combine tickets and the error word come from g_scratch below, which every
-// GPU that loads the library holds until the process exits.
+// the caller's inputs and outputs; the work list, the split partials and
+// the error word come from g_scratch below, which every GPU that loads the
+// library holds until the process exits.
 #include <algorithm>
 #include <mutex>
 
@@ -33,8 +33,7 @@ constexpr size_t kItemsOff = 0;
 constexpr size_t kPartOOff = align256(kItemsOff + sizeof(pkv_work_item) * kStaticItems);
 constexpr size_t kPartLseOff =
     align256(kPartOOff + sizeof(float) * size_t(kStaticPartials) * kDecCols * kHeadDim);
-constexpr size_t kTicketsOff = align256(kPartLseOff + sizeof(float) * size_t(kStaticPartials) * kDecCols);
-constexpr size_t kErrOff = align256(kTicketsOff + sizeof(int32_t) * kStaticPartials);
+constexpr size_t kErrOff = align256(kPartLseOff + sizeof(float) * size_t(kStaticPartials) * kDecCols);
 constexpr size_t kScratchBytes = align256(kErrOff + sizeof(int32_t));  // ~4.3 MB
 
 // The scratch.  In host code this name is only a stand-in: its device address
@@ -220,10 +219,15 @@ extern "C" pkv_status pkv_decode_static(
     if (a.kv_head != b.kv_head) return a.kv_head < b.kv_head;
     return a.k_begin < b.k_begin;
   });
+  // the first range of each split pair leads the list: the merge kernel
+  // takes its groups from there
+  const int groups = static_cast<int>(
+      std::stable_partition(g_items, g_items + n,
+                            [](const pkv_work_item &w) { return w.part >= 0 && w.part == w.pair; }) -
+      g_items);
   if (n == 0) return PKV_OK;
-  // tickets and the error word must start at zero; the rest is overwritten
-  if (cudaMemsetAsync(scratch + kTicketsOff, 0, sizeof(int32_t) * std::max(part, 1), s) != cudaSuccess ||
-      cudaMemsetAsync(scratch + kErrOff, 0, sizeof(int32_t), s) != cudaSuccess ||
+  // the error word must start at zero; the rest is overwritten
+  if (cudaMemsetAsync(scratch + kErrOff, 0, sizeof(int32_t), s) != cudaSuccess ||
       cudaMemcpyAsync(scratch + kItemsOff, g_items, sizeof(pkv_work_item) * n,
                       cudaMemcpyHostToDevice, s) != cudaSuccess)
     return PKV_ERR_CUDA;
@@ -239,7 +243,6 @@ extern "C" pkv_status pkv_decode_static(
   p.lse = lse;
   p.part_o = reinterpret_cast<float *>(scratch + kPartOOff);
   p.part_lse = reinterpret_cast<float *>(scratch + kPartLseOff);
-  p.tickets = reinterpret_cast<int32_t *>(scratch + kTicketsOff);
   p.err = reinterpret_cast<int32_t *>(scratch + kErrOff);
   p.hq = c->num_q_heads;
   p.hkv = H;
@@ -251,6 +254,8 @@ extern "C" pkv_status pkv_decode_static(
   p.num_blocks = c->num_blocks;
   p.scale_log2 = c->softmax_scale * 1.4426950408889634f;
   p.validate = 0;
-  return launch_decode(kmap, vmap, p, n, c->kv_dtype, s) == cudaSuccess ? PKV_OK
-                                                                         : PKV_ERR_CUDA;
+  return launch_decode(kmap, vmap, p, n, c->kv_dtype, s) == cudaSuccess &&
+                 launch_decode_merge(p, groups, s) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
 }

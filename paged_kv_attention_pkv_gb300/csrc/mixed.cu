@@ -10,9 +10,9 @@
 // memory, so an SM keeps as many K/V bytes in flight as two 4-warp decode
 // CTAs) and lets the other 4 warps exit.  Decode CTAs are scheduled last and
 // fill the SMs that prefill tiles free at different times, so the tail of
-// the prefill work overlaps the memory-bound decode work.  Decode ranges of
-// one (request, KV head) are merged by the last CTA to finish, as in the
-// standalone decode kernel.
+// the prefill work overlaps the memory-bound decode work.  Split decode
+// ranges (and prefill ranges) are merged by the merge kernels launched after
+// this one.
 #include "decode_body.cuh"
 #include "prefill_tc_body.cuh"
 

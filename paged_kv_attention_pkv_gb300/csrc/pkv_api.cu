@@ -75,7 +75,6 @@ struct pkv_handle {
   int max_items = 0;
   float *d_part_o = nullptr;
   float *d_part_lse = nullptr;
-  int32_t *d_tickets = nullptr;
   int32_t *d_err = nullptr;
   uint8_t *h_stage[2] = {nullptr, nullptr};   // pinned staging (double buffer)
   cudaEvent_t staged[2] = {nullptr, nullptr};
@@ -143,6 +142,7 @@ std::string check_config(const pkv_config *c, pkv_status *st) {
 struct Plan {
   std::vector<pkv_work_item> dec, pre;
   int partials = 0;
+  int dec_groups = 0;   // split decode pairs: their first ranges lead `dec`
   int pre_groups = 0;   // split prefill items: their first ranges lead `pre`
 };
 
@@ -364,6 +364,13 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
     std::vector<pkv_work_item> sorted(n);
     for (size_t k = 0; k < n; ++k) sorted[k] = plan->dec[order[k]];
     plan->dec.swap(sorted);
+    // the first range of each split pair leads the list (the merge kernel
+    // takes its groups from there); these are full-length ranges, so the
+    // longest-first order barely moves
+    const auto lead = std::stable_partition(
+        plan->dec.begin(), plan->dec.end(),
+        [](const pkv_work_item &w) { return w.part >= 0 && w.part == w.pair; });
+    plan->dec_groups = static_cast<int>(lead - plan->dec.begin());
   }
   // Prefill tiles of one (request, KV head) read the same K/V stream: keep
   // them adjacent so the CTAs running together share it through L2, and
@@ -473,6 +480,18 @@ void timing_end(pkv_handle *h, int kind, cudaStream_t s) {
   ++r.count;
 }
 
+// The merges of split key ranges (decode pairs, then prefill row tiles),
+// after the attention kernels of the step, timed as one PKV_KERNEL_MERGE.
+pkv_status launch_merges(pkv_handle *h, const DecodeParams &dp, const PrefillParams &pp,
+                         const Plan &plan, cudaStream_t s) {
+  if (plan.dec_groups == 0 && plan.pre_groups == 0) return PKV_OK;
+  timing_begin(h, PKV_KERNEL_MERGE, s);
+  cudaError_t e = launch_decode_merge(dp, plan.dec_groups, s);
+  if (e == cudaSuccess) e = launch_prefill_merge(pp, plan.pre_groups, s);
+  timing_end(h, PKV_KERNEL_MERGE, s);
+  return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "merge launch");
+}
+
 }  // namespace
 
 extern "C" {
@@ -551,15 +570,13 @@ pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out) {
   bool ok = cudaMalloc(&h->d_work, h->work_bytes) == cudaSuccess &&
             cudaMalloc(&h->d_part_o, sizeof(float) * size_t(kMaxPartials) * kDecCols * kHeadDim) == cudaSuccess &&
             cudaMalloc(&h->d_part_lse, sizeof(float) * size_t(kMaxPartials) * kDecCols) == cudaSuccess &&
-            cudaMalloc(&h->d_tickets, sizeof(int32_t) * kMaxPartials) == cudaSuccess &&
             cudaMalloc(&h->d_err, sizeof(int32_t)) == cudaSuccess &&
             cudaMallocHost(&h->h_stage[0], h->work_bytes) == cudaSuccess &&
             cudaMallocHost(&h->h_stage[1], h->work_bytes) == cudaSuccess &&
             cudaEventCreateWithFlags(&h->staged[0], cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&h->staged[1], cudaEventDisableTiming) == cudaSuccess;
   if (ok) {
-    ok = cudaMemset(h->d_tickets, 0, sizeof(int32_t) * kMaxPartials) == cudaSuccess &&
-         cudaMemset(h->d_err, 0, sizeof(int32_t)) == cudaSuccess;
+    ok = cudaMemset(h->d_err, 0, sizeof(int32_t)) == cudaSuccess;
   }
   if (ok && (config->flags & PKV_FLAG_TIMING)) {
     h->timing = true;
@@ -586,7 +603,6 @@ pkv_status pkv_destroy(pkv_handle *h) {
   cudaFree(h->d_graph_work);
   cudaFree(h->d_part_o);
   cudaFree(h->d_part_lse);
-  cudaFree(h->d_tickets);
   cudaFree(h->d_err);
   for (int i = 0; i < 2; ++i) {
     if (h->h_stage[i]) cudaFreeHost(h->h_stage[i]);
@@ -792,7 +808,6 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   dp.lse = lse;
   dp.part_o = h->d_part_o;
   dp.part_lse = h->d_part_lse;
-  dp.tickets = h->d_tickets;
   dp.err = h->d_err;
   dp.hq = c.num_q_heads;
   dp.hkv = c.num_kv_heads;
@@ -841,10 +856,9 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     // a mixed step: one launch for both kinds of work
     timing_begin(h, PKV_KERNEL_MIXED, s);
     e = launch_mixed(qmap, h->pf_k, h->pf_v, h->dec_k, h->dec_v, pp, dp, n_pre, n_dec, s);
-    if (e == cudaSuccess) e = launch_prefill_merge(pp, plan.pre_groups, s);
     timing_end(h, PKV_KERNEL_MIXED, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "mixed-step launch");
-    return PKV_OK;
+    return launch_merges(h, dp, pp, plan, s);
   }
   if (n_dec > 0) {
     timing_begin(h, PKV_KERNEL_DECODE, s);
@@ -855,11 +869,10 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
   if (n_pre > 0) {
     timing_begin(h, PKV_KERNEL_PREFILL, s);
     e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, pp, n_pre, c.kv_dtype, s);
-    if (e == cudaSuccess) e = launch_prefill_merge(pp, plan.pre_groups, s);
     timing_end(h, PKV_KERNEL_PREFILL, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
   }
-  return PKV_OK;
+  return launch_merges(h, dp, pp, plan, s);
 }
 
 }  // namespace

@@ -64,7 +64,6 @@ struct DecodeParams {
   float *lse;
   float *part_o;     // [slots][kDecCols][128]
   float *part_lse;   // [slots][kDecCols], log2 domain
-  int32_t *tickets;  // indexed by an item's first partial slot
   int32_t *err;
   int32_t hq, hkv, group, bs;
   int32_t rows_total;   // num_blocks * hkv * bs (rows of the pool maps)
@@ -154,8 +153,10 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
 cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p,
                               int num_items, int kv_dtype, cudaStream_t s);
-// Merges the ranges of the first num_groups items of p.items (the first
-// ranges of the split prefill items) into bf16 rows and log-sum-exps.
+// Merge the key ranges of split items: the first num_groups items of
+// p.items are the first ranges of the split (request, KV head) pairs (decode)
+// or row tiles (prefill); rows and log-sum-exps go to the outputs.
+cudaError_t launch_decode_merge(const DecodeParams &p, int num_groups, cudaStream_t s);
 cudaError_t launch_prefill_merge(const PrefillParams &p, int num_groups, cudaStream_t s);
 cudaError_t launch_check(const CheckParams &p, cudaStream_t s);
 cudaError_t launch_lse_merge(const float *parts_o, const float *parts_lse, int num_parts,
