@@ -87,6 +87,14 @@ def _check_plan(spec, num_sms=152):
         assert rs[0][0] == 0
         assert sum(n for _, n in rs) == spec.q_lens[i] * G
     assert sorted(slots) == list(range(parts))
+    # the merge kernels take their groups from the head of each kind's list:
+    # the first range of every split pair (decode) or row tile (prefill)
+    # comes before any other item of that kind
+    for kind in (0, 1):
+        ws = [w for w in items if w["kind"] == kind]
+        lead = [w["part"] >= 0 and w["part"] == w["pair"] for w in ws]
+        n_lead = sum(lead)
+        assert all(lead[:n_lead]) and not any(lead[n_lead:])
     # every (request, KV head) pair with tokens appears
     seen = set(dec_keys) | set(rows)
     assert len(seen) == sum(1 for q in spec.q_lens if q > 0) * spec.hkv
