@@ -61,18 +61,26 @@ CASES = {
     "small-fp8": (4, [0]),                    # one ~0.6-1M-token FP8 request
     "small-nvfp4": (4, [0, 1]),               # two such requests, NVFP4 KV
     "small-prefill-fp8": (2, [4, 5]),         # two post-tool-call sessions, E4M3 KV
-    "small-mixed": (3, list(range(0, 120, 8)) + [120, 127]),
+    "small-mixed": (3, [0, 40, 80, 119, 127]),   # 4 decodes + the 392-token chunk, ~2 GB
+    # the whole post-tool-call step, for captures of its 26K-token KV append
+    # (216 MB bf16, 162 MB E4M3, 138 MB NVFP4 per launch)
+    "append-c3": (2, list(range(16))),
+    "append-c3-fp8": (2, list(range(16))),
+    "append-c3-nvfp4": (2, list(range(16))),
 }
-CASE_KV = {"small-nvfp4": "nvfp4", "small-prefill-fp8": "fp8"}
+CASE_KV = {"small-nvfp4": "nvfp4", "small-prefill-fp8": "fp8", "append-c3-fp8": "fp8",
+           "append-c3-nvfp4": "nvfp4"}
 
 
 def case_spec(name: str) -> W.Spec:
     index, seqs = CASES[name]
     full = W.config_spec(index)
     kv = CASE_KV.get(name, full.kv_dtype)
+    whole = seqs == list(range(full.num_seqs))
     return W.Spec(f"{full.name}[{name}]", full.hq, full.hkv, full.block_size,
                   kv, [full.q_lens[i] for i in seqs],
-                  [full.seq_lens[i] for i in seqs], full.seed)
+                  [full.seq_lens[i] for i in seqs], full.seed,
+                  shared_prefix=full.shared_prefix if whole else None)
 
 
 def dist_env():

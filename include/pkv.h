@@ -26,6 +26,9 @@
  *  - A KV pool is [num_blocks][Hkv][block_size][128] elements: bf16, or E4M3
  *    codes (OCP FP8, "FN" variant) with one fp32 scale per (block, KV head)
  *    in a [num_blocks][Hkv] array; an element's value is e4m3(code) * scale.
+ *    E4M3 block scales must be at most 16 (values up to 7168; the kernels
+ *    round values times scales to f16); validate mode checks this for every
+ *    block in use and reports PKV_ERR_DEVICE_CHECK.
  *    NVFP4 pools (the compressed KV format of page "vLLM 优化
  *    DeepSeek-V4.1-Flash：智能体吞吐提升 5 倍", section Kernels) are
  *    [num_blocks][Hkv][block_size * 72] bytes: per (block, KV head), rows in
@@ -33,7 +36,8 @@
  *    (OCP FP4 E2M1, element 2j in the low nibble of byte j) followed by their
  *    8 micro-scale bytes each (E4M3, one per 16 elements); with the fp32
  *    (block, KV head) scale an element's value is e2m1(code) * e4m3(micro
- *    scale) * scale.  NVFP4 scales must be at most 16.
+ *    scale) * scale.  NVFP4 block scales must be at most 16 as well
+ *    (checked the same way).
  *    Logical position p of request i lives in block block_tables[i][p / bs]
  *    at row p % bs; its slot is block * bs + p % bs.
  *  - Query token t (0-based) of request i, which has q_i new tokens and
@@ -222,10 +226,13 @@ pkv_status pkv_attention_varlen(pkv_handle *h, const void *q,
  * pkv_attention_partial: shard `shard` (0 <= shard < num_shards) of one step,
  * decode rows only (q_i * G <= 8; a request with more rows returns
  * PKV_ERR_UNSUPPORTED).  Arguments as for pkv_attention_varlen, except:
- *  interleave  tokens per run, a positive multiple of the decode stage (16
- *              keys for bf16 pools, 32 for E4M3, 64 for NVFP4; the pages'
- *              default of 1 is
- *              not supported on the GPU and returns PKV_ERR_UNSUPPORTED);
+ *  interleave  tokens per run, >= 1 (the pages' default is 1).  A multiple
+ *              of the decode stage (16 keys for bf16 pools, 32 for E4M3, 64
+ *              for NVFP4) lets the shard read only its own keys; any other
+ *              value makes the shard walk the request's whole context and
+ *              mask the keys it does not own (same result, the pool read
+ *              once per shard: on real ranks each rank's pool holds only
+ *              its own tokens and the plain decode reads them);
  *  out         [num_tokens][Hq][128] fp32, device: the shard's softmax-
  *              normalised partial output (0 where the shard owns no visible
  *              key);
@@ -288,6 +295,21 @@ pkv_status pkv_graph_prepare(pkv_handle *h, const int32_t *query_start_loc_host,
  * PKV_ERR_TIMEOUT, or PKV_ERR_CUDA if the device reported an error.
  */
 pkv_status pkv_check_device_errors(pkv_handle *h);
+
+/*
+ * Self-test of failure detection.  Every wait inside the kernels (on a copy
+ * or an MMA completing) gives up after 1 s, records PKV_ERR_TIMEOUT in the
+ * handle's error word and lets the kernel wind down, so a lost completion
+ * is reported instead of hanging the GPU.  This call exercises that path
+ * without breaking anything: it launches one CTA on `stream` that waits,
+ * through the same bounded-wait code, on a barrier nothing arrives at and no
+ * copy or MMA completes, with a limit of limit_ns nanoseconds
+ * (1 .. 1000000000).  The wait runs out and the timeout is recorded, so the
+ * next pkv_check_device_errors returns PKV_ERR_TIMEOUT (and clears the
+ * word); the handle stays usable.  Errors: PKV_ERR_INVALID_ARG (limit_ns out
+ * of range), PKV_ERR_CUDA.
+ */
+pkv_status pkv_wait_selftest(pkv_handle *h, uint64_t limit_ns, void *stream);
 
 /* Static description of a status code; never NULL. */
 const char *pkv_status_string(pkv_status status);
@@ -389,18 +411,25 @@ pkv_status pkv_timing_read(pkv_handle *h, int32_t kind, int32_t *launches,
  * Limits: at most 2048 work items and 1024 split partials per call (the split
  * size grows to fit; a batch with more than 2048 (request, KV head) pairs is
  * rejected with PKV_ERR_WORKSPACE).
- *  - The first call on a device looks up the array's device address and sets
- *    the kernel's shared-memory limit; make that first call before any stream
- *    capture.
+ *  - Set-up: the first call on a device looks up the array's device address
+ *    (which loads the library's device code there and, with CUDA's lazy
+ *    module loading, is when the array gets its memory), sets the kernels'
+ *    shared-memory limits and clears the error word, synchronously.  A call
+ *    with num_seqs = 0 and num_tokens = 0 does only that: make it at
+ *    start-up, before the caller reserves the rest of device memory and
+ *    before any stream capture.
  *  - Every call shares the array and leaves its contents behind; each call
- *    clears what must start at zero.  A call runs the decode kernel and,
- *    when it split any key range, the merge kernel.  Calls whose GPU work overlaps (on
- *    different streams, or from different threads) race on it: serialise
- *    them.
+ *    overwrites the work list and partials it uses.  A call runs the decode
+ *    kernel and, when it split any key range, the merge kernel.  Calls whose
+ *    GPU work overlaps (on different streams, or from different threads)
+ *    race on it: serialise them.
+ *  - The kernels record a block-table entry outside the pool (its keys read
+ *    as zeros) and a device-side wait that gave up in an error word inside
+ *    the array; it accumulates over calls until pkv_decode_static_errors
+ *    reads and clears it.
  *  - Returns PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED (prefill rows,
  *    head_dim or block_size not handled), PKV_ERR_WORKSPACE or PKV_ERR_CUDA.
- *    It does not update pkv_last_error() and performs no device-side
- *    validation.
+ *    It does not update pkv_last_error().
  */
 pkv_status pkv_decode_static(const pkv_config *config, const void *q,
                              const void *k_cache, const void *v_cache,
@@ -411,6 +440,18 @@ pkv_status pkv_decode_static(const pkv_config *config, const void *q,
                              const int32_t *seq_lens_host, int32_t num_seqs,
                              int32_t num_tokens, void *out, float *lse,
                              void *stream);
+
+/*
+ * Read and clear the error word of pkv_decode_static on the current device,
+ * after the work already enqueued on `stream` (a cudaStream_t; NULL = legacy
+ * default stream) has finished: waits for that stream, copies the word into
+ * host memory of the library and clears it, allocating nothing.  Returns
+ * PKV_OK, PKV_ERR_DEVICE_CHECK (a block-table entry in use was outside the
+ * pool), PKV_ERR_TIMEOUT (a device-side wait gave up) or PKV_ERR_CUDA.
+ * Like every pkv_decode_static call, it must not overlap another one's GPU
+ * work.  The pages describe nothing like it (see pkv_decode_static).
+ */
+pkv_status pkv_decode_static_errors(void *stream);
 
 #ifdef __cplusplus
 }

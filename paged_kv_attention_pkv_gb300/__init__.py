@@ -31,7 +31,9 @@ KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL, KERNEL_MIXED, KERNEL_MERGE = 0, 1,
 EXPORTS = ["pkv_create", "pkv_write_slots", "pkv_attention_varlen",
            "pkv_check_device_errors", "pkv_status_string", "pkv_last_error",
            "pkv_destroy", "pkv_plan", "pkv_timing_reset", "pkv_timing_read",
-           "pkv_decode_static", "pkv_graph_prepare", "pkv_attention_partial",
+           "pkv_decode_static", "pkv_decode_static_errors", "pkv_wait_selftest",
+           "pkv_graph_prepare",
+           "pkv_attention_partial",
            "pkv_lse_merge", "pkv_rope_write_slots",
            # host block pool (include/pkv_blocks.h)
            "pkv_blocks_create", "pkv_blocks_destroy", "pkv_blocks_lookup",
@@ -124,6 +126,10 @@ def load(path: str | None = None):
     lib.pkv_decode_static.restype = ctypes.c_int
     lib.pkv_decode_static.argtypes = [ctypes.POINTER(Config), vp, vp, vp, vp, vp, vp,
                                       i32, vp, vp, i32, i32, vp, vp, vp]
+    lib.pkv_decode_static_errors.restype = ctypes.c_int
+    lib.pkv_decode_static_errors.argtypes = [vp]
+    lib.pkv_wait_selftest.restype = ctypes.c_int
+    lib.pkv_wait_selftest.argtypes = [vp, ctypes.c_uint64, vp]
     if path is None:
         _lib = lib
     return lib
@@ -304,6 +310,12 @@ class Handle:
         """pkv_check_device_errors: raise PkvError if the device recorded one."""
         self._check(self._lib.pkv_check_device_errors(self._h))
 
+    def wait_selftest(self, limit_ns: int, stream=None) -> None:
+        """pkv_wait_selftest: one bounded wait that runs out after limit_ns;
+        the next check_device_errors reports the timeout."""
+        self._check(self._lib.pkv_wait_selftest(self._h, int(limit_ns),
+                                                _stream(stream, self.device)))
+
     def timing_reset(self) -> None:
         self._check(self._lib.pkv_timing_reset(self._h))
 
@@ -426,3 +438,21 @@ def decode_static(config: Config, q, k_cache, v_cache, block_tables,
     if st != PKV_OK:
         raise PkvError(st, status_string(st))
     return out, lse
+
+
+def decode_static_setup(config: Config) -> None:
+    """pkv_decode_static with no requests: the one-time set-up on the current
+    device (module load, kernel limits, error word cleared)."""
+    st = load().pkv_decode_static(ctypes.byref(config), None, None, None, None, None,
+                                  None, 0, None, None, 0, 0, None, None, None)
+    if st != PKV_OK:
+        raise PkvError(st, status_string(st))
+
+
+def decode_static_errors(stream=None, device=None) -> None:
+    """pkv_decode_static_errors: raise PkvError if the error word of the
+    allocation-free decode holds anything (then cleared)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    st = load().pkv_decode_static_errors(_stream(stream, dev))
+    if st != PKV_OK:
+        raise PkvError(st, status_string(st))

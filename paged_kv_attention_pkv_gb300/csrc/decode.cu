@@ -28,7 +28,10 @@
 namespace pkv {
 namespace {
 
-template <bool FP8>
+// MASK: the masked context-parallel shard view (interleaves shorter than a
+// stage), a separate instantiation so that the plain decode carries no test
+// for it.
+template <bool FP8, bool MASK>
 __global__ void __launch_bounds__(kDecWarps * 32, FP8 ? 3 : 2)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap,
@@ -36,9 +39,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, FP8 ? 3 : 2)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  decode_item<FP8, kDecWarps>(kmap, vmap, p, p.items[blockIdx.x], smem, threadIdx.x, 0);
+  decode_item<FP8, kDecWarps, MASK>(kmap, vmap, p, p.items[blockIdx.x], smem, threadIdx.x, 0);
 }
 
+template <bool MASK>
 __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasNvfp4)
     decode_nvfp4_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap,
@@ -46,7 +50,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, kDecCtasNvfp4)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  decode_item_nvfp4<kDecWarps>(kmap, vmap, p, p.items[blockIdx.x], smem, threadIdx.x, 0);
+  decode_item_nvfp4<kDecWarps, MASK>(kmap, vmap, p, p.items[blockIdx.x], smem, threadIdx.x, 0);
 }
 
 // Merges the key ranges of split decode items.  The first ranges of the
@@ -104,11 +108,101 @@ __global__ void __launch_bounds__(kDecCols * 32) decode_merge_kernel(const Decod
     p.lse[row] = Ls > 0.f ? (Mu + log2f(Ls)) * kLn2 : -CUDART_INF_F;
 }
 
+// The same merge for steps whose pairs have more than 32 ranges (one long
+// request split over the whole machine): walked by one warp, a row's ranges
+// cost one dependent L2 round trip per 8 of them.  Here a CTA takes one row
+// (blockIdx.y) of one pair and its 8 warps take contiguous runs of the
+// ranges; the maximum, the weight sum and the per-warp sums are combined in
+// a fixed order, so the result does not depend on timing.
+constexpr int kWideMergeWarps = 8;
+
+__global__ void __launch_bounds__(kWideMergeWarps * 32, 2)
+    decode_merge_wide_kernel(const DecodeParams p) {
+  const pkv_work_item it = p.items[blockIdx.x];
+  const int n = blockIdx.y;
+  if (n >= it.n_rows) return;   // the whole CTA
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ns = it.n_split;
+  const float *lse_p = p.part_lse + static_cast<int64_t>(it.pair) * kDecCols + n;
+  const float *o_p = p.part_o + (static_cast<int64_t>(it.pair) * kDecCols + n) * kHeadDim;
+  constexpr int64_t kSlotFloats = int64_t(kDecCols) * kHeadDim;
+  constexpr int kThreads = kWideMergeWarps * 32;
+  __shared__ float red[kWideMergeWarps];
+  __shared__ float4 part[kWideMergeWarps][32];
+  // largest log-sum-exp over the ranges
+  float M = -CUDART_INF_F;
+  for (int s2 = tid; s2 < ns; s2 += kThreads) M = fmaxf(M, __ldcg(lse_p + s2 * kDecCols));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int w = 1; w < kWideMergeWarps; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+  const float Mu = M == -CUDART_INF_F ? 0.f : M;
+  // sum of the weights 2^(lse_s - max)
+  float Ls = 0.f;
+  for (int s2 = tid; s2 < ns; s2 += kThreads) Ls += exp2f(__ldcg(lse_p + s2 * kDecCols) - Mu);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+  if (lane == 0) red[warp] = Ls;
+  __syncthreads();
+  Ls = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWideMergeWarps; ++w) Ls += red[w];
+  const float winv = Ls > 0.f ? 1.f / Ls : 0.f;
+  // this warp's run of ranges, lane l holding head dims 4l .. 4l + 3
+  const int per = (ns + kWideMergeWarps - 1) / kWideMergeWarps;
+  const int s_lo = warp * per, s_hi = min(ns, s_lo + per);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = s_lo; s0 < s_hi; s0 += 32) {
+    const int s2 = s0 + lane;
+    const float w_l = s2 < s_hi ? exp2f(__ldcg(lse_p + s2 * kDecCols) - Mu) * winv : 0.f;
+    const int cnt = s_hi - s0 < 32 ? s_hi - s0 : 32;
+#pragma unroll 8
+    for (int k = 0; k < cnt; ++k) {
+      const float w = __shfl_sync(0xffffffffu, w_l, k);
+      const float4 x = __ldcg(reinterpret_cast<const float4 *>(o_p + (s0 + k) * kSlotFloats) + lane);
+      acc.x += w * x.x;
+      acc.y += w * x.y;
+      acc.z += w * x.z;
+      acc.w += w * x.w;
+    }
+  }
+  part[warp][lane] = acc;
+  __syncthreads();
+  if (warp != 0) return;
+  acc = part[0][lane];
+#pragma unroll
+  for (int w = 1; w < kWideMergeWarps; ++w) {
+    const float4 x = part[w][lane];
+    acc.x += x.x;
+    acc.y += x.y;
+    acc.z += x.z;
+    acc.w += x.w;
+  }
+  const int r = it.row0 + n;
+  const int64_t row = static_cast<int64_t>(it.tok0 + r / p.group) * p.hq +
+                      it.kv_head * p.group + r % p.group;
+  if (p.out_f32 != nullptr)
+    reinterpret_cast<float4 *>(p.out_f32 + row * kHeadDim)[lane] = acc;
+  else
+    reinterpret_cast<uint2 *>(p.out + row * kHeadDim)[lane] =
+        make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[row] = Ls > 0.f ? (Mu + log2f(Ls)) * kLn2 : -CUDART_INF_F;
+}
+
 }  // namespace
 
-cudaError_t launch_decode_merge(const DecodeParams &p, int num_groups, cudaStream_t s) {
+cudaError_t launch_decode_merge(const DecodeParams &p, int num_groups, int max_split,
+                                cudaStream_t s) {
   if (num_groups == 0) return cudaSuccess;
-  decode_merge_kernel<<<num_groups, kDecCols * 32, 0, s>>>(p);
+  if (max_split > 32)
+    decode_merge_wide_kernel<<<dim3(num_groups, kDecCols), kWideMergeWarps * 32, 0, s>>>(p);
+  else
+    decode_merge_kernel<<<num_groups, kDecCols * 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -117,27 +211,42 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
                           cudaStream_t s) {
   if (num_items == 0) return cudaSuccess;
   const bool fp8 = kv_dtype == PKV_KV_FP8_E4M3;
-  if (kv_dtype == PKV_KV_NVFP4)
-    decode_nvfp4_kernel<<<num_items, kDecWarps * 32, kDecSmemBytesNvfp4, s>>>(kmap, vmap, p);
-  else if (fp8)
-    decode_kernel<true><<<num_items, kDecWarps * 32, kDecSmemBytesFp8, s>>>(kmap, vmap, p);
-  else
-    decode_kernel<false><<<num_items, kDecWarps * 32, kDecSmemBytes, s>>>(kmap, vmap, p);
+  const dim3 grid(num_items), block(kDecWarps * 32);
+  if (kv_dtype == PKV_KV_NVFP4) {
+    if (p.dcp_mask)
+      decode_nvfp4_kernel<true><<<grid, block, kDecSmemBytesNvfp4, s>>>(kmap, vmap, p);
+    else
+      decode_nvfp4_kernel<false><<<grid, block, kDecSmemBytesNvfp4, s>>>(kmap, vmap, p);
+  } else if (fp8) {
+    if (p.dcp_mask)
+      decode_kernel<true, true><<<grid, block, kDecSmemBytesFp8, s>>>(kmap, vmap, p);
+    else
+      decode_kernel<true, false><<<grid, block, kDecSmemBytesFp8, s>>>(kmap, vmap, p);
+  } else {
+    if (p.dcp_mask)
+      decode_kernel<false, true><<<grid, block, kDecSmemBytes, s>>>(kmap, vmap, p);
+    else
+      decode_kernel<false, false><<<grid, block, kDecSmemBytes, s>>>(kmap, vmap, p);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t configure_decode() {
-  cudaError_t e = cudaFuncSetAttribute(decode_nvfp4_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kDecSmemBytesNvfp4);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kDecSmemBytesFp8);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_kernel<false>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kDecSmemBytes);
+  const void *kernels[] = {
+      reinterpret_cast<const void *>(decode_nvfp4_kernel<false>),
+      reinterpret_cast<const void *>(decode_nvfp4_kernel<true>),
+      reinterpret_cast<const void *>(decode_kernel<true, false>),
+      reinterpret_cast<const void *>(decode_kernel<true, true>),
+      reinterpret_cast<const void *>(decode_kernel<false, false>),
+      reinterpret_cast<const void *>(decode_kernel<false, true>)};
+  const int bytes[] = {kDecSmemBytesNvfp4, kDecSmemBytesNvfp4, kDecSmemBytesFp8,
+                       kDecSmemBytesFp8,   kDecSmemBytes,      kDecSmemBytes};
+  for (int k = 0; k < 6; ++k) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernels[k], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes[k]);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace pkv

@@ -34,19 +34,35 @@ __device__ __forceinline__ int32_t pool_row(const int32_t *bt, int32_t key,
   return (blk * p.hkv + kvh) * p.bs + key % p.bs;
 }
 
-// Global key of an item-local key: the identity, or the shard view (see
-// DecodeParams).  Keys of one stage stay consecutive.
-__device__ __forceinline__ int32_t global_key(const DecodeParams &p, int32_t x) {
-  if (p.dcp_n <= 1) return x;
-  return ((x / p.dcp_k) * p.dcp_n + p.dcp_r) * p.dcp_k + x % p.dcp_k;
-}
-
 // Physical head-dim index of a row of the O^T accumulator in the E4M3 path
 // (row dr of m-tile mt): the V fragments are built from 4-byte words, so each
 // thread's 4 consecutive bytes feed rows (g, g+8) of two adjacent m-tiles.
 __device__ __forceinline__ int fp8_dmap(int mt, int dr) {
   return 4 * ((dr & 7) + 8 * (mt >> 1)) + 2 * (mt & 1) + (dr >> 3);
 }
+
+// Global key of an item-local key: the identity, or the shard view (see
+// DecodeParams).  Keys of one stage stay consecutive.
+__device__ __forceinline__ int32_t global_key(const DecodeParams &p, int32_t x) {
+  if (p.dcp_n <= 1 || p.dcp_mask) return x;
+  return ((x / p.dcp_k) * p.dcp_n + p.dcp_r) * p.dcp_k + x % p.dcp_k;
+}
+
+// Masked shard view: does this shard own global key gk?
+__device__ __forceinline__ bool shard_owns(const DecodeParams &p, int32_t gk) {
+  return (gk / p.dcp_k) % p.dcp_n == p.dcp_r;
+}
+
+// Quantised pools fold V's block scale s_v into P before P is rounded to
+// f16 for the PV MMAs.  Block scales of real KV are small (E4M3: amax / 448,
+// often 1e-3 .. 1e-5), which would push P * s_v into f16 subnormals.  So P is
+// computed as 2^(s - m + kPExp) instead of 2^(s - m): a constant offset on
+// the online-softmax running max (the row sums carry the same 2^kPExp, so
+// O / l is unchanged, and the log-sum-exp is taken against m - kPExp).  With
+// block scales at most kQuantScaleMax = 16, P * s_v <= 2^11 * 16 = 2^15 stays
+// a finite f16, and scales down to 1e-7 keep P * s_v normal for P >= 3e-4
+// (smaller weights lose relative precision, and matter less in proportion).
+constexpr float kPExp = 11.f;
 
 // End of a decode item, shared by the storage formats: merge the NW warps'
 // (max, sum, O) through shared memory, normalise, and write the rows, or
@@ -131,8 +147,10 @@ __device__ __forceinline__ void decode_finish(const DecodeParams &p, const pkv_w
 
 // One decode work item processed by NW warps (threads tid = 0 .. 32 NW - 1
 // of the CTA); `smem` is 1024-byte aligned and holds NW rings plus their
-// mbarriers; `bar` is the named barrier these warps synchronise on.
-template <bool FP8, int NW>
+// mbarriers; `bar` is the named barrier these warps synchronise on.  MASK:
+// the masked context-parallel shard view (DecodeParams::dcp_mask), compiled
+// only into the kernels that serve it.
+template <bool FP8, int NW, bool MASK = false>
 __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                             const DecodeParams &p, const pkv_work_item it,
                                             uint8_t *smem, const int tid, const int bar) {
@@ -156,6 +174,7 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
   }
   fence_mbar_init();
   sync();
+  const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
 
   const int kb = it.k_begin;
   const int ke = it.k_end;
@@ -163,7 +182,6 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
   const int my_n = n_total > warp ? (n_total - warp + kDecWarps - 1) / kDecWarps : 0;
   uint8_t *ring = smem + warp * kDecStages * kDecStageBytes;
   uint64_t *full = bars + warp * kDecStages;
-  const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
   const int br = p.bs < KS ? p.bs : KS;  // rows per TMA box
 
   // Fill ring slot for this warp's i-th stage (lane 0 only).
@@ -295,6 +313,7 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
   int32_t blk_next[Tile::kSubs];
   stage_blocks(0, blk_next);
 
+
   int consumed = 0;
   bool timed_out = false;
   for (int i = 0; i < my_n; ++i) {
@@ -369,6 +388,10 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       s[sub][1] = (kr0 < ke && gr0 <= pos1) ? s[sub][1] * sc1 : -CUDART_INF_F;
       s[sub][2] = (kr1 < ke && gr1 <= pos0) ? s[sub][2] * sc0 : -CUDART_INF_F;
       s[sub][3] = (kr1 < ke && gr1 <= pos1) ? s[sub][3] * sc1 : -CUDART_INF_F;
+      if constexpr (MASK) {   // masked shard view: keys another shard owns
+        if (!shard_owns(p, gr0)) s[sub][0] = s[sub][1] = -CUDART_INF_F;
+        if (!shard_owns(p, gr1)) s[sub][2] = s[sub][3] = -CUDART_INF_F;
+      }
       tm0 = fmaxf(tm0, fmaxf(s[sub][0], s[sub][2]));
       tm1 = fmaxf(tm1, fmaxf(s[sub][1], s[sub][3]));
     }
@@ -381,6 +404,7 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
     const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
     const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
     const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+    const float mp0 = FP8 ? mu0 - kPExp : mu0, mp1 = FP8 ? mu1 - kPExp : mu1;
     m0 = mn0;
     m1 = mn1;
     l0 *= al0;
@@ -396,8 +420,8 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
     for (int sub = 0; sub < Tile::kSubs; ++sub) {
       const int k16 = key0 + 16 * sub;
       if (k16 >= ke) break;
-      const float p0 = exp2f(s[sub][0] - mu0), p1 = exp2f(s[sub][1] - mu1);
-      const float p2 = exp2f(s[sub][2] - mu0), p3 = exp2f(s[sub][3] - mu1);
+      const float p0 = exp2f(s[sub][0] - mp0), p1 = exp2f(s[sub][1] - mp1);
+      const float p2 = exp2f(s[sub][2] - mp0), p3 = exp2f(s[sub][3] - mp1);
       l0 += p0 + p2;
       l1 += p1 + p3;
       const float pv_scale = FP8 ? sv_sub[sub] : 1.f;
@@ -477,7 +501,9 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       mbar_wait(&full[i % kDecStages], (i / kDecStages) & 1);
   }
 
-  decode_finish<NW>(p, it, smem, tid, bar, m0, m1, l0, l1, acc, 1.f,
+  // P carried 2^kPExp: the effective running maxima are m - kPExp
+  decode_finish<NW>(p, it, smem, tid, bar, FP8 ? m0 - kPExp : m0, FP8 ? m1 - kPExp : m1, l0,
+                    l1, acc, 1.f,
                     [](int mt, int dr) { return FP8 ? fp8_dmap(mt, dr) : 16 * mt + dr; });
 }
 

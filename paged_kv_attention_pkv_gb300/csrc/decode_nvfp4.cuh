@@ -14,7 +14,8 @@
 // Codes are converted to f16 in hardware and multiplied by their micro scale
 // in f16, which is exact (a 2-bit by 4-bit significand product), so the MMAs
 // see e2m1 * e4m3 exactly; the fp32 block scales are folded into the score
-// scale (K) and into P (V), as for E4M3 pools.  Queries enter the f16 MMAs
+// scale (K) and into P (V, with P's exponent offset kPExp), as for E4M3
+// pools.  Queries enter the f16 MMAs
 // scaled by a power of two per column (largest |q| in [2^14, 2^15)), undone
 // in the score scale.
 //
@@ -52,9 +53,7 @@ __device__ __forceinline__ int nvfp4_dmap(int mt, int dr) {
   return 16 * (dr & 7) + 8 * (mt >> 2) + 2 * (mt & 3) + (dr >> 3);
 }
 
-constexpr float kNvPScale = 4096.f;   // P * scale_v * 2^12 stays a normal f16
-
-template <int NW>
+template <int NW, bool MASK = false>
 __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
                                                   const CUtensorMap &vmap,
                                                   const DecodeParams &p,
@@ -267,6 +266,10 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
       s[sub][1] = (kr0 < ke && gr0 <= pos1) ? s[sub][1] * sc1 : -CUDART_INF_F;
       s[sub][2] = (kr1 < ke && gr1 <= pos0) ? s[sub][2] * sc0 : -CUDART_INF_F;
       s[sub][3] = (kr1 < ke && gr1 <= pos1) ? s[sub][3] * sc1 : -CUDART_INF_F;
+      if constexpr (MASK) {   // masked shard view: keys another shard owns
+        if (!shard_owns(p, gr0)) s[sub][0] = s[sub][1] = -CUDART_INF_F;
+        if (!shard_owns(p, gr1)) s[sub][2] = s[sub][3] = -CUDART_INF_F;
+      }
       tm0 = fmaxf(tm0, fmaxf(s[sub][0], s[sub][2]));
       tm1 = fmaxf(tm1, fmaxf(s[sub][1], s[sub][3]));
     }
@@ -279,6 +282,7 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
     const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
     const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
     const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+    const float mp0 = mu0 - kPExp, mp1 = mu1 - kPExp;
     m0 = mn0;
     m1 = mn1;
     l0 *= al0;
@@ -294,12 +298,12 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
     for (int sub = 0; sub < kSubs; ++sub) {
       const int k16 = key0 + 16 * sub;
       if (k16 >= ke) break;
-      const float p0 = exp2f(s[sub][0] - mu0), p1 = exp2f(s[sub][1] - mu1);
-      const float p2 = exp2f(s[sub][2] - mu0), p3 = exp2f(s[sub][3] - mu1);
+      const float p0 = exp2f(s[sub][0] - mp0), p1 = exp2f(s[sub][1] - mp1);
+      const float p2 = exp2f(s[sub][2] - mp0), p3 = exp2f(s[sub][3] - mp1);
       l0 += p0 + p2;
       l1 += p1 + p3;
       // ---- P^T as the B operand (f16, V's block scale folded in)
-      const float pv_scale = sv_sub[sub] * kNvPScale;
+      const float pv_scale = sv_sub[sub];
       const uint32_t b0 = movmatrix_trans(pack_f16(p0 * pv_scale, p1 * pv_scale));
       const uint32_t b1 = movmatrix_trans(pack_f16(p2 * pv_scale, p3 * pv_scale));
       // ---- O^T += V^T P^T: this thread's micro block g of rows A, B, C, D
@@ -360,7 +364,8 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
     const int issued = my_n < consumed + S ? my_n : consumed + S;
     for (int i = consumed; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1);
   }
-  decode_finish<NW>(p, it, smem, tid, bar, m0, m1, l0, l1, acc, 1.f / kNvPScale,
+  // P carried 2^kPExp: the effective running maxima are m - kPExp
+  decode_finish<NW>(p, it, smem, tid, bar, m0 - kPExp, m1 - kPExp, l0, l1, acc, 1.f,
                     [](int mt, int dr) { return nvfp4_dmap(mt, dr); });
 }
 

@@ -43,7 +43,10 @@ static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
 std::mutex g_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_scratch on the current device (set up on first use).
+// Device address of g_scratch on the current device.  The first use on a
+// device loads the module there (lazy loading gives its device variables
+// memory only then), sets the kernels' shared-memory limits and clears the
+// error word, synchronously.
 cudaError_t scratch_address(int device, uint8_t **out) {
   std::lock_guard<std::mutex> lock(g_mutex);
   if (g_scratch_ptr[device] == nullptr) {
@@ -52,10 +55,19 @@ cudaError_t scratch_address(int device, uint8_t **out) {
     if (e != cudaSuccess) return e;
     e = configure_decode();
     if (e != cudaSuccess) return e;
+    e = cudaMemset(static_cast<uint8_t *>(p) + kErrOff, 0, sizeof(int32_t));
+    if (e != cudaSuccess) return e;
     g_scratch_ptr[device] = p;
   }
   *out = static_cast<uint8_t *>(g_scratch_ptr[device]);
   return cudaSuccess;
+}
+
+// Current device, checked against the per-device table.
+cudaError_t current_device(int *dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e == cudaSuccess && (*dev < 0 || *dev >= kMaxDevices)) e = cudaErrorInvalidDevice;
+  return e;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
@@ -129,7 +141,14 @@ extern "C" pkv_status pkv_decode_static(
   const bool nvfp4 = c->kv_dtype == PKV_KV_NVFP4;
   if (c->num_blocks * c->num_kv_heads * bs * (nvfp4 ? 9 : 8) / 8 >= (int64_t(1) << 31) - 4096)
     return PKV_ERR_UNSUPPORTED;
-  if (num_seqs == 0) return num_tokens == 0 ? PKV_OK : PKV_ERR_INVALID_ARG;
+  int dev = 0;
+  if (current_device(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (num_seqs == 0) {
+    // nothing to run: the call only sets the device up (a warm-up)
+    if (num_tokens != 0) return PKV_ERR_INVALID_ARG;
+    uint8_t *unused = nullptr;
+    return scratch_address(dev, &unused) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  }
   if (!q || !k_cache || !v_cache || !block_tables || !qsl || !lens || !out)
     return PKV_ERR_INVALID_ARG;
   const bool fp8 = c->kv_dtype == PKV_KV_FP8_E4M3;
@@ -150,8 +169,7 @@ extern "C" pkv_status pkv_decode_static(
   }
 
   // split size: fill the machine, then grow until the static scratch holds it
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices) return PKV_ERR_CUDA;
+  int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int64_t chunk = std::max<int64_t>(1024, (keys / (8 * std::max(sms, 1)) + kSplitAlign - 1) /
                                               kSplitAlign * kSplitAlign);
@@ -226,9 +244,11 @@ extern "C" pkv_status pkv_decode_static(
                             [](const pkv_work_item &w) { return w.part >= 0 && w.part == w.pair; }) -
       g_items);
   if (n == 0) return PKV_OK;
-  // the error word must start at zero; the rest is overwritten
-  if (cudaMemsetAsync(scratch + kErrOff, 0, sizeof(int32_t), s) != cudaSuccess ||
-      cudaMemcpyAsync(scratch + kItemsOff, g_items, sizeof(pkv_work_item) * n,
+  int max_split = 1;
+  for (int k = 0; k < n; ++k) max_split = std::max(max_split, int(g_items[k].n_split));
+  // the error word keeps what earlier calls recorded until
+  // pkv_decode_static_errors reads it; the rest is overwritten
+  if (cudaMemcpyAsync(scratch + kItemsOff, g_items, sizeof(pkv_work_item) * n,
                       cudaMemcpyHostToDevice, s) != cudaSuccess)
     return PKV_ERR_CUDA;
 
@@ -255,7 +275,23 @@ extern "C" pkv_status pkv_decode_static(
   p.scale_log2 = c->softmax_scale * 1.4426950408889634f;
   p.validate = 0;
   return launch_decode(kmap, vmap, p, n, c->kv_dtype, s) == cudaSuccess &&
-                 launch_decode_merge(p, groups, s) == cudaSuccess
+                 launch_decode_merge(p, groups, max_split, s) == cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
+}
+
+extern "C" pkv_status pkv_decode_static_errors(void *stream) {
+  int dev = 0;
+  if (current_device(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  uint8_t *scratch = nullptr;
+  if (scratch_address(dev, &scratch) != cudaSuccess) return PKV_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t word = 0;
+  if (cudaMemcpyAsync(&word, scratch + kErrOff, sizeof word, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaMemsetAsync(scratch + kErrOff, 0, sizeof(int32_t), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (word & kErrTimeout) return PKV_ERR_TIMEOUT;
+  return word != 0 ? PKV_ERR_DEVICE_CHECK : PKV_OK;
 }

@@ -305,11 +305,35 @@ __global__ void __launch_bounds__(256) check_kernel(CheckParams p) {
   const int64_t nb = (L + p.bs - 1) / p.bs;
   for (int64_t j = threadIdx.x; j < nb; j += blockDim.x) {
     const int32_t b = p.block_tables[static_cast<int64_t>(i) * p.bt_stride + j];
-    if (b < 0 || b >= p.num_blocks) record_error(p.err, kErrBadBlock);
+    if (b < 0 || b >= p.num_blocks) {
+      record_error(p.err, kErrBadBlock);
+    } else if (p.k_scale != nullptr) {
+      for (int h = 0; h < p.hkv; ++h) {
+        const int64_t si = static_cast<int64_t>(b) * p.hkv + h;
+        if (!(p.k_scale[si] <= kQuantScaleMax) || !(p.v_scale[si] <= kQuantScaleMax))
+          record_error(p.err, kErrBadScale);
+      }
+    }
   }
 }
 
+// Self-test of the bounded waits: one thread waits, through mbar_wait, on
+// an mbarrier that nothing arrives at and no copy or MMA completes, so the
+// wait runs out after limit_ns and the timeout is recorded like any other.
+__global__ void wait_selftest_kernel(int32_t *err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) mbar_init(&bar, 1);
+  fence_mbar_init();
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, limit_ns)) record_error(err, kErrTimeout);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(int32_t *err, uint64_t limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope_append(const RopeAppendParams &p, int kv_dtype, bool neox,
                                cudaStream_t s) {

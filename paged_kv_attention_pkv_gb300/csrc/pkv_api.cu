@@ -143,13 +143,16 @@ struct Plan {
   std::vector<pkv_work_item> dec, pre;
   int partials = 0;
   int dec_groups = 0;   // split decode pairs: their first ranges lead `dec`
+  int dec_max_split = 1;   // most ranges of one decode pair
   int pre_groups = 0;   // split prefill items: their first ranges lead `pre`
 };
 
-// Keys of a sequence of L keys that context-parallel shard r of n owns when
-// tokens are dealt out in runs of k: run j goes to shard j % n.
+// Keys an item list walks for a sequence of L keys: all of them, or, for
+// context-parallel shard r of n with tokens dealt out in runs of k (run j
+// to shard j % n), the shard's own keys; with dcp[3] set (runs shorter than
+// a decode stage) every key, the others masked in the kernel.
 int64_t shard_keys(int64_t L, const int32_t *dcp) {
-  if (dcp == nullptr || dcp[0] <= 1) return L;
+  if (dcp == nullptr || dcp[0] <= 1 || dcp[3]) return L;
   const int64_t n = dcp[0], r = dcp[1], k = dcp[2];
   const int64_t runs = L / k, rem = L % k;
   return (runs / n) * k + (runs % n > r ? k : 0) + (runs % n == r ? rem : 0);
@@ -371,6 +374,8 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
         plan->dec.begin(), plan->dec.end(),
         [](const pkv_work_item &w) { return w.part >= 0 && w.part == w.pair; });
     plan->dec_groups = static_cast<int>(lead - plan->dec.begin());
+    plan->dec_max_split = 1;
+    for (const auto &w : plan->dec) plan->dec_max_split = std::max(plan->dec_max_split, int(w.n_split));
   }
   // Prefill tiles of one (request, KV head) read the same K/V stream: keep
   // them adjacent so the CTAs running together share it through L2, and
@@ -486,7 +491,7 @@ pkv_status launch_merges(pkv_handle *h, const DecodeParams &dp, const PrefillPar
                          const Plan &plan, cudaStream_t s) {
   if (plan.dec_groups == 0 && plan.pre_groups == 0) return PKV_OK;
   timing_begin(h, PKV_KERNEL_MERGE, s);
-  cudaError_t e = launch_decode_merge(dp, plan.dec_groups, s);
+  cudaError_t e = launch_decode_merge(dp, plan.dec_groups, plan.dec_max_split, s);
   if (e == cudaSuccess) e = launch_prefill_merge(pp, plan.pre_groups, s);
   timing_end(h, PKV_KERNEL_MERGE, s);
   return e == cudaSuccess ? PKV_OK : cuda_fail(h, e, "merge launch");
@@ -790,6 +795,11 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     cp.bs = bs;
     cp.num_blocks = c.num_blocks;
     cp.err = h->d_err;
+    if (fp8 || nvfp4) {
+      cp.k_scale = k_scale;
+      cp.v_scale = v_scale;
+      cp.hkv = c.num_kv_heads;
+    }
     if ((e = launch_check(cp, s)) != cudaSuccess) return cuda_fail(h, e, "check launch");
   }
 
@@ -823,6 +833,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     dp.dcp_n = dcp[0];
     dp.dcp_r = dcp[1];
     dp.dcp_k = dcp[2];
+    dp.dcp_mask = dcp[0] > 1 ? dcp[3] : 0;
   }
   dp.out_f32 = out_f32;
   PrefillParams pp{};
@@ -907,12 +918,13 @@ pkv_status pkv_attention_partial(pkv_handle *h, const void *q, const void *k_cac
                                                        : kDecKeysBf16;
   if (num_shards < 1 || shard < 0 || shard >= num_shards)
     return fail(h, PKV_ERR_INVALID_ARG, fmt("shard %d of %d", shard, num_shards));
-  if (interleave < stage || interleave % stage != 0)
-    return fail(h, PKV_ERR_UNSUPPORTED,
-                fmt("interleave %d: must be a positive multiple of %d keys", interleave, stage));
+  if (interleave < 1)
+    return fail(h, PKV_ERR_INVALID_ARG, fmt("interleave %d: must be at least 1", interleave));
   if (out == nullptr || lse == nullptr)
     return fail(h, PKV_ERR_INVALID_ARG, "a partial needs out and lse");
-  const int32_t dcp[3] = {num_shards, shard, interleave};
+  // runs that fill whole decode stages are read compactly; shorter ones
+  // (the pages' interleave of 1) by walking every key and masking the rest
+  const int32_t dcp[4] = {num_shards, shard, interleave, interleave % stage != 0 ? 1 : 0};
   return attention_step(h, q, k_cache, v_cache, k_scale, v_scale, query_start_loc, seq_lens,
                         block_tables, block_table_stride, qsl_host, lens_host, num_seqs,
                         num_tokens, nullptr, lse, stream, dcp, out);
@@ -1024,6 +1036,20 @@ pkv_status pkv_graph_prepare(pkv_handle *h, const int32_t *qsl_host,
   return PKV_OK;
 }
 
+pkv_status pkv_wait_selftest(pkv_handle *h, uint64_t limit_ns, void *stream) {
+  if (h == nullptr) return PKV_ERR_INVALID_ARG;
+  h->last_error.clear();
+  if (limit_ns < 1 || limit_ns > kWaitLimitNs)
+    return fail(h, PKV_ERR_INVALID_ARG,
+                fmt("limit_ns %llu outside [1, %llu]", (unsigned long long)limit_ns,
+                    (unsigned long long)kWaitLimitNs));
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  e = launch_wait_selftest(h->d_err, limit_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "wait self-test launch");
+  return PKV_OK;
+}
+
 pkv_status pkv_check_device_errors(pkv_handle *h) {
   if (h == nullptr) return PKV_ERR_INVALID_ARG;
   cudaError_t e = cudaSetDevice(h->device);
@@ -1041,6 +1067,7 @@ pkv_status pkv_check_device_errors(pkv_handle *h) {
     if (word & kErrBadSlot) what += " slot outside the pool;";
     if (word & kErrMismatch) what += " device metadata differs from the host mirrors;";
     if (word & kErrBadPosition) what += " rotary position outside the cos/sin cache;";
+    if (word & kErrBadScale) what += " E4M3/NVFP4 block scale above 16 (or NaN);";
     return fail(h, PKV_ERR_DEVICE_CHECK, "device check:" + what);
   }
   return PKV_OK;

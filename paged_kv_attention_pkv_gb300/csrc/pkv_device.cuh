@@ -24,6 +24,9 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// 2^e as a float, exactly, for integer e in [-126, 127].
+__device__ __forceinline__ float exp2_int(int e) { return __int_as_float((e + 127) << 23); }
+
 __device__ __forceinline__ void record_error(int32_t *err, int32_t bit) {
   if (err != nullptr) atomicOr(err, bit);
 }
@@ -72,13 +75,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait until the phase with `parity` of `bar` has completed.  Gives up after
-// kWaitLimitNs and returns false; the caller records kErrTimeout and winds
-// down instead of hanging the GPU.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// limit_ns (the kernels use kWaitLimitNs) and returns false; the caller
+// records kErrTimeout and winds down instead of hanging the GPU.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_test(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
   return true;
 }

@@ -19,7 +19,14 @@ enum : int32_t {
   kErrTimeout = 4,      // a bounded wait gave up
   kErrMismatch = 8,     // device metadata differs from the host mirrors
   kErrBadPosition = 16, // a rotary position is outside the cos/sin cache
+  kErrBadScale = 32,    // a quantised pool's block scale in use is above the cap (or NaN)
 };
+
+// Block scales of E4M3 and NVFP4 pools must not exceed this: the kernels
+// round values times block scales to f16 (decode: P * s_v <= 2^11 * 16; the
+// prefill's V conversion: at most 448 * 16 or 6 * 448 * 16 = 43008, all
+// below 65504).
+constexpr float kQuantScaleMax = 16.f;
 
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
@@ -70,11 +77,14 @@ struct DecodeParams {
   int64_t num_blocks;
   float scale_log2;     // softmax_scale * log2(e)
   int32_t validate;
-  // Context-parallel shard view: keys are a shard's own keys when dcp_n > 1
-  // (item-local key x is global key ((x / dcp_k) * dcp_n + dcp_r) * dcp_k +
-  // x % dcp_k; dcp_k a multiple of the stage's key count), and results go
-  // to out_f32 (fp32, normalised) instead of out when out_f32 is set.
-  int32_t dcp_n, dcp_r, dcp_k;
+  // Context-parallel shard view (dcp_n > 1): shard dcp_r of dcp_n owns the
+  // runs j of dcp_k keys with j % dcp_n == dcp_r.  When dcp_k is a multiple
+  // of the stage's key count, items walk the shard's own keys (item-local
+  // key x is global key ((x / dcp_k) * dcp_n + dcp_r) * dcp_k + x % dcp_k);
+  // otherwise (dcp_mask) items walk every key and the scores of keys the
+  // shard does not own are masked.  Results go to out_f32 (fp32,
+  // normalised) instead of out when out_f32 is set.
+  int32_t dcp_n, dcp_r, dcp_k, dcp_mask;
   float *out_f32;
   // NVFP4 pools (byte addresses of the micro scales); rows_total then counts
   // the pools' 64-byte rows
@@ -142,6 +152,11 @@ struct CheckParams {
   int32_t bs;
   int64_t num_blocks;
   int32_t *err;
+  // E4M3 and NVFP4 pools: block scales of every block in use are checked
+  // against kQuantScaleMax (NULL: not checked)
+  const float *k_scale;
+  const float *v_scale;
+  int32_t hkv;
 };
 
 // Launchers (each returns the launch's cudaError_t).
@@ -155,10 +170,14 @@ cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
                               int num_items, int kv_dtype, cudaStream_t s);
 // Merge the key ranges of split items: the first num_groups items of
 // p.items are the first ranges of the split (request, KV head) pairs (decode)
-// or row tiles (prefill); rows and log-sum-exps go to the outputs.
-cudaError_t launch_decode_merge(const DecodeParams &p, int num_groups, cudaStream_t s);
+// or row tiles (prefill); rows and log-sum-exps go to the outputs.  max_split
+// is the largest number of ranges of a decode pair (above 32, each row's
+// ranges are spread over a CTA's warps).
+cudaError_t launch_decode_merge(const DecodeParams &p, int num_groups, int max_split,
+                                cudaStream_t s);
 cudaError_t launch_prefill_merge(const PrefillParams &p, int num_groups, cudaStream_t s);
 cudaError_t launch_check(const CheckParams &p, cudaStream_t s);
+cudaError_t launch_wait_selftest(int32_t *err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_lse_merge(const float *parts_o, const float *parts_lse, int num_parts,
                              int64_t num_rows, __nv_bfloat16 *out, float *lse,
                              cudaStream_t s);

@@ -95,21 +95,27 @@ def gpu_rows(out: torch.Tensor, lse: torch.Tensor, sub: dict, rows=None):
 # scaled x8 so a few keys dominate each softmax) cannot meet a purely
 # absolute bound: rounding the output to bf16 alone costs up to half an ulp,
 # 2^-8 |x| (0.0156 at |x| = 4), and rounding P to bf16 about 2^-9 |x| more.
-# Each element is therefore checked against max_abs + 2^-7 |ref| (derived,
-# not given; for the long-context workloads |ref| << 1 and this is the plain
-# gate).  Peaked variants also relax the mean to mean_abs + 2^-8 mean|ref|.
-PEAKED_ELEM_REL = 2.0 ** -7
+# Small cases (`scaled=True`) therefore check each element against
+# max_abs + 3 * 2^-9 |ref| (derived from those two roundings, not given);
+# peaked variants also relax the mean to mean_abs + 2^-8 mean|ref|.  The
+# full-size workloads, whose outputs are << 1, are held to the plain gate.
+SCALED_ELEM_REL = 3.0 * 2.0 ** -9
 PEAKED_MEAN_REL = 2.0 ** -8
 
 
 def check(got, ref, got_lse, ref_lse, kind: str = "bf16", what: str = "",
-          peaked: bool = False):
-    """Raise AssertionError unless got matches the oracle within TOL[kind]."""
+          peaked: bool = False, scaled: bool = False):
+    """Raise AssertionError unless got matches the oracle within TOL[kind].
+
+    With scaled=False (the full-size workloads) this is the gate as stated:
+    max-abs, mean-abs, per-row relative L2 and log-sum-exp bounds, nothing
+    proportional to |ref|."""
     t = TOL[kind]
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     err = np.abs(got - ref)
-    excess = err - (t["max_abs"] + PEAKED_ELEM_REL * np.abs(ref))
+    rel_elem = SCALED_ELEM_REL if (scaled or peaked) else 0.0
+    excess = err - (t["max_abs"] + rel_elem * np.abs(ref))
     assert excess.max() <= 0, f"{what}: element error {err.flat[excess.argmax()]:.3e} " \
         f"at |ref| {np.abs(ref).flat[excess.argmax()]:.3e}"
     mean_bound = t["mean_abs"] + (PEAKED_MEAN_REL * np.abs(ref).mean() if peaked else 0.0)
@@ -131,4 +137,4 @@ def full_parity(batch: W.Batch, flags: int = pkv.FLAG_VALIDATE, what: str = "",
     out, lse = gpu_step(batch, flags=flags)
     ref, ref_lse = oracle_subset(sub, batch.spec)
     got, got_lse = gpu_rows(out, lse, sub)
-    return check(got, ref, got_lse, ref_lse, batch.spec.kv_dtype, what, peaked)
+    return check(got, ref, got_lse, ref_lse, batch.spec.kv_dtype, what, peaked, scaled=True)

@@ -46,6 +46,7 @@ def test_null_handles_are_safe():
     assert lib.pkv_destroy(None) == 0
     assert lib.pkv_timing_reset(None) == 0
     assert lib.pkv_check_device_errors(None) == 1
+    assert lib.pkv_wait_selftest(None, 1000, None) == 1
     assert lib.pkv_write_slots(None, None, None, None, 0, None, None, None, None, None) == 1
 
 

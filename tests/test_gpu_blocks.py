@@ -81,7 +81,7 @@ def test_pool_tables_feed_prefill_prefix_hits_and_decode():
                            np.concatenate(slots))
         ref, ref_lse = oracle.attention(kc0, vc0, W.bf16_bits(q), qsl, lens, bt, 1 / math.sqrt(D))
         got = out.double().cpu().numpy().reshape(-1, D)
-        U.check(got, ref, None, None, "bf16", "pool-driven step")
+        U.check(got, ref, None, None, "bf16", "pool-driven step", scaled=True)
         return tables
 
     t1 = step([(1, reqs[1], len(reqs[1]))])                  # prefill of request 1

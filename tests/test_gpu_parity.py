@@ -1,8 +1,10 @@
 """CUDA path against the fp64 oracle, through the C ABI (GPU only).
 
-Small cases compare every output row; the five workloads run at full size
-and compare sampled rows the oracle computes one by one (always including
-the first and last rows of each sequence and rows at tile boundaries).
+Small cases compare every output row.  The five workloads run at full size,
+in the launch configuration bench.py times: every output row of the decode
+batch and of the long-context E4M3 decode, and every request of the
+post-tool-call prefill and of the mixed step on at least 64 rows (the first
+and last query tokens, both sides of the Q-tile boundaries, random ones).
 """
 import dataclasses
 
@@ -164,7 +166,7 @@ def test_mixed_step_launch_modes(separate, kv):
     h.close()
     ref, ref_lse = U.oracle_subset(sub, s)
     got, got_lse = U.gpu_rows(out, lse, sub)
-    U.check(got, ref, got_lse, ref_lse, kv, f"mixed_modes {kv}")
+    U.check(got, ref, got_lse, ref_lse, kv, f"mixed_modes {kv}", scaled=True)
     if separate or kv == "fp8":
         assert counts == {pkv.KERNEL_DECODE: 1, pkv.KERNEL_PREFILL: 1, pkv.KERNEL_MIXED: 0}
     else:
@@ -186,71 +188,174 @@ def test_prefix_shared_blocks():
     U.full_parity(b, what="shared")
 
 
-# ---- the five workloads at full size, sampled rows ---------------------------------
+# ---- the five workloads at full size ------------------------------------------------
+#
+# The step runs once on the GPU as bench.py launches it; its outputs are kept
+# on the host and the batch is dropped.  The pools are then drawn again from
+# the same seeds (the generator is deterministic), so the oracle reads the
+# generator's contents and does its own append: none of its inputs passes
+# through the CUDA path.  The oracle evaluates the chosen rows group by group
+# (a few requests at a time, bounded host memory).
 
-def _sampled(batch, seq_ids, kv_heads, token_pick=None, what=""):
-    sub = W.subset(batch, seq_ids, kv_heads)
-    hq = len(sub["heads"])
-    rows = None
-    if token_pick is not None:
-        toks = []
-        for r, i in enumerate(seq_ids):
-            a = int(sub["qsl"][r])
-            q = int(sub["qsl"][r + 1]) - a
-            toks.extend(a + t for t in token_pick(q) if 0 <= t < q)
-        toks = np.unique(np.asarray(toks, np.int64))
-        rows = (toks[:, None] * hq + np.arange(hq)[None, :]).reshape(-1)
-    out, lse = U.gpu_step(batch)
-    ref, ref_lse = U.oracle_subset(sub, batch.spec, rows=rows)
-    got, got_lse = U.gpu_rows(out, lse, sub, rows)
-    return U.check(got, ref, got_lse, ref_lse, batch.spec.kv_dtype, what)
+def _workload_outputs(spec):
+    b = W.generate(spec, DEV)
+    out, lse = U.gpu_step(b)
+    res = out.cpu(), lse.cpu()
+    del b, out, lse
+    torch.cuda.empty_cache()
+    return res
 
 
-def _edge_tokens(q, G, rng=np.random.default_rng(3)):
-    per_tile = max(1, 64 // G)
-    picks = {0, 1, q - 2, q - 1, per_tile - 1, per_tile, 2 * per_tile}
-    picks |= set(rng.integers(0, q, 6).tolist())
+def _edge_tokens(q, G, seed, n_random=4):
+    """Query tokens to check in a request of q new tokens: the first and last
+    ones, both sides of every Q-tile boundary of the first and last prefill
+    items (tiles of G * floor(128 / G) rows, two per item) and n_random more."""
+    per_tile = max(1, 128 // G)
+    picks = {0, 1, q - 2, q - 1}
+    for k in (1, 2, 3):
+        for c in (k * per_tile, q - k * per_tile):
+            picks |= {c - 1, c}
+    rng = np.random.default_rng(seed)
+    picks |= set(rng.integers(0, q, n_random).tolist())
     return sorted(p for p in picks if 0 <= p < q)
 
 
+def _rows(sub, G, token_pick=None, all_heads=True):
+    """Row indices (token * Hq_sub + head) of a subset: the tokens
+    token_pick(q, request) of each request (all with None), with all query
+    heads, or one query head per KV head (the head within the group rotates
+    with the token)."""
+    hq = len(sub["heads"])
+    rows = []
+    for r in range(len(sub["qsl"]) - 1):
+        a = int(sub["qsl"][r])
+        q = int(sub["qsl"][r + 1]) - a
+        toks = range(q) if token_pick is None else token_pick(q, r)
+        for t in toks:
+            if all_heads:
+                rows.extend((a + t) * hq + h for h in range(hq))
+            else:
+                rows.extend((a + t) * hq + kvh * G + (t + kvh) % G for kvh in range(hq // G))
+    return np.asarray(rows, np.int64)
+
+
+def _check_groups(spec, outputs, groups, token_pick=None, all_heads=True, what=""):
+    """Regenerate the pools and compare the rows of each group of requests
+    with the oracle; returns the worst figures over all groups."""
+    out, lse = outputs
+    b = W.generate(spec, DEV)
+    G = spec.hq // spec.hkv
+    worst = dict(max_abs=0.0, mean_abs=0.0, rel=0.0, lse=0.0, rows=0)
+    for grp in groups:
+        sub = W.subset(b, list(grp))
+        pick = None if token_pick is None else (lambda q, r: token_pick(q, grp[r]))
+        rows = _rows(sub, G, pick, all_heads)
+        ref, ref_lse = U.oracle_subset(sub, spec, rows=rows)
+        got, got_lse = U.gpu_rows(out, lse, sub, rows)
+        st = U.check(got, ref, got_lse, ref_lse, spec.kv_dtype, f"{what} requests {grp}")
+        for k in ("max_abs", "mean_abs", "rel", "lse"):
+            worst[k] = max(worst[k], st[k])
+        worst["rows"] += len(rows)
+    del b
+    torch.cuda.empty_cache()
+    print(f"{what}: {worst}")
+    return worst
+
+
+def _chunks(ids, n):
+    ids = list(ids)
+    return [ids[i:i + n] for i in range(0, len(ids), n)]
+
+
 def test_decode_batch_full_size():
-    b = W.generate(W.config_spec(1), DEV)
-    L = b.seq_lens
-    seqs = sorted({int(L.argmin()), int(L.argmax()), 0, 17, 40, 63})
-    _sampled(b, seqs, None, what="c2")
+    """Decode batch: every output row (64 requests x 32 heads)."""
+    spec = W.config_spec(1)
+    res = _workload_outputs(spec)
+    _check_groups(spec, res, _chunks(range(spec.num_seqs), 16), what="c2")
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8", "nvfp4"])
 def test_post_tool_prefill_full_size(kv):
     """The post-tool-call prefill as bench.py times it (bf16, and the E4M3 /
-    NVFP4 KV variants of its secondary lines): sessions 0 (shared prefix), 3
-    and 9, two KV heads, edge and random tokens."""
-    b = W.generate(dataclasses.replace(W.config_spec(2), kv_dtype=kv), DEV)
-    G = 4
-    _sampled(b, [0, 3, 9], [0, 5], token_pick=lambda q: _edge_tokens(q, G), what=f"c3 {kv}")
+    NVFP4 KV variants of its secondary lines): all 16 sessions, each on the
+    first, last, tile-boundary and random query tokens; every query head
+    with bf16 KV, one query head per KV head (rotating within the group)
+    with quantised KV."""
+    spec = dataclasses.replace(W.config_spec(2), kv_dtype=kv)
+    res = _workload_outputs(spec)
+    G = spec.hq // spec.hkv
+    _check_groups(spec, res, _chunks(range(spec.num_seqs), 4),
+                  token_pick=lambda q, i: _edge_tokens(q, G, 100 + i),
+                  all_heads=kv == "bf16", what=f"c3 {kv}")
 
 
 def test_mixed_step_full_size():
-    b = W.generate(W.config_spec(3), DEV)
-    G = 8
-    # decodes 0, 57, 119 and prefill chunks 120 (2048 tokens) and 127 (392)
-    _sampled(b, [0, 57, 119, 120, 127], [0, 7],
-             token_pick=lambda q: _edge_tokens(q, G), what="c4")
+    """Mixed step: every row of the 120 decodes (64 heads each) and, for each
+    of the 8 prefill chunks, the first, last, tile-boundary and random
+    tokens on one query head per KV head (>= 128 rows per chunk)."""
+    spec = W.config_spec(3)
+    res = _workload_outputs(spec)
+    G = spec.hq // spec.hkv
+    _check_groups(spec, res, _chunks(range(120), 20), what="c4 decodes")
+    _check_groups(spec, res, _chunks(range(120, 128), 2),
+                  token_pick=lambda q, i: _edge_tokens(q, G, 200 + i),
+                  all_heads=False, what="c4 chunks")
 
 
 def test_fp8_long_decode_full_size():
-    b = W.generate(W.config_spec(4), DEV)
-    L = b.seq_lens
-    _sampled(b, [int(L.argmin())], [0, 5], what="c5")
+    """Long-context decode with E4M3 KV: every output row (8 requests of
+    512K-1M keys x 64 heads), the longest request included."""
+    spec = W.config_spec(4)
+    res = _workload_outputs(spec)
+    _check_groups(spec, res, _chunks(range(spec.num_seqs), 2), what="c5")
 
 
 def test_nvfp4_long_decode_full_size():
-    """The long-context decode with NVFP4 KV as bench.py times it: the
-    shortest and the longest request, two KV heads each."""
-    full = W.config_spec(4)
-    b = W.generate(dataclasses.replace(full, kv_dtype="nvfp4"), DEV)
-    L = b.seq_lens
-    _sampled(b, [int(L.argmin()), int(L.argmax())], [0, 5], what="c5 nvfp4")
+    """The long-context decode with NVFP4 KV as bench.py times it: every row
+    of the shortest and the longest request, and one query head per KV head
+    of the other six."""
+    spec = dataclasses.replace(W.config_spec(4), kv_dtype="nvfp4")
+    res = _workload_outputs(spec)
+    L = np.asarray(spec.seq_lens)
+    ends = sorted({int(L.argmin()), int(L.argmax())})
+    rest = [i for i in range(spec.num_seqs) if i not in ends]
+    _check_groups(spec, res, [[i] for i in ends], what="c5 nvfp4 shortest/longest")
+    _check_groups(spec, res, _chunks(rest, 3), token_pick=lambda q, i: [0],
+                  all_heads=False, what="c5 nvfp4 others")
+
+
+# ---- quantised KV at realistic magnitudes ------------------------------------------------
+#
+# KV entries of real models are far from N(0, 1): with K and V drawn with
+# standard deviation sigma, E4M3 block scales are about 1e-2 sigma (1e-3 to
+# 1e-5 here) and NVFP4 block scales about 1.5e-3 sigma.  The queries are
+# drawn with 1/sigma so that the scores keep their N(0, 1) spread.  Decode
+# (64K and 100K keys) and tensor-core prefill rows (40 tokens over 70K keys),
+# every row, with the relative-L2 and log-sum-exp checks.
+
+@pytest.mark.parametrize("kv", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("sigma", [1e-1, 1e-2, 1e-3])
+def test_quantised_kv_at_small_magnitudes(kv, sigma):
+    s = spec(f"mag_{kv}_{sigma:g}", 8, 2, 64, [1, 1, 40, 1], [65536, 100000, 70040, 3000],
+             kv=kv)
+    b = W.generate(s, DEV, q_scale=1.0 / sigma, kv_sigma=sigma)
+    st = U.full_parity(b, what=f"{kv} sigma {sigma:g}")
+    print(f"{kv} sigma {sigma:g}: {st}")
+
+
+def test_fp8_value_scales_that_jump_between_blocks():
+    """E4M3 pools whose V block scales differ by factors of 2^-16 .. 1 from
+    block to block (and K scales by 2^-2 .. 2^2): decode and prefill rows,
+    every row."""
+    s = spec("jump_fp8", 8, 2, 16, [1, 1, 30, 1], [20000, 7000, 9000, 33], kv="fp8")
+    b = W.generate(s, DEV, q_scale=0.5)
+    g = torch.Generator(device="cpu").manual_seed(77)
+    ev = torch.randint(-16, 1, b.v_scale.shape, generator=g).to(DEV)
+    ek = torch.randint(-2, 3, b.k_scale.shape, generator=g).to(DEV)
+    b.v_scale.mul_(torch.pow(2.0, ev.float()))
+    b.k_scale.mul_(torch.pow(2.0, ek.float()))
+    st = U.full_parity(b, what="jump_fp8", peaked=True)
+    print(f"jump_fp8: {st}")
 
 
 # ---- invariances -------------------------------------------------------------------
@@ -285,6 +390,23 @@ def test_run_to_run_deterministic():
     out2, lse2 = U.gpu_step(b, append=False)
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
     assert torch.equal(lse1, lse2)
+
+
+def test_single_long_request_many_ranges():
+    """One 600K-token decode split over the whole machine (over 100 key
+    ranges per (request, KV head) pair, merged by the wide merge kernel):
+    every row against the oracle, and the same bits on a second run."""
+    s = spec("long_one", 32, 8, 16, [1], [600_000])
+    b = W.generate(s, DEV)
+    sub = W.subset(b, [0])
+    out1, lse1 = U.gpu_step(b)
+    out2, lse2 = U.gpu_step(b, append=False)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+    ref, ref_lse = U.oracle_subset(sub, b.spec)
+    got, got_lse = U.gpu_rows(out1, lse1, sub)
+    st = U.check(got, ref, got_lse, ref_lse, "bf16", "long_one")
+    print(f"long_one: {st}")
 
 
 def test_split_prefill_is_deterministic():
@@ -374,6 +496,52 @@ def test_validate_mode_reports_bad_slots_and_mirror_mismatch():
         h.check_device_errors()
     assert e.value.status == 5 and "mirror" in str(e.value)
     h.check_device_errors()                      # the word was cleared
+    h.close()
+
+
+@pytest.mark.parametrize("kv", ["fp8", "nvfp4"])
+def test_validate_mode_reports_scales_above_the_cap(kv):
+    """E4M3 and NVFP4 block scales must be at most 16; validate mode checks
+    every block in use before the attention kernels and reports
+    PKV_ERR_DEVICE_CHECK."""
+    s = spec("bigscale", 8, 2, 16, [1, 5], [40, 60], kv=kv)
+    b = W.generate(s, DEV)
+    h = U.make_handle(b)
+    m = U.device_meta(b)
+    h.write_slots(b.k_new, b.v_new, m["slots"], b.k_cache, b.v_cache, b.k_scale, b.v_scale)
+    h.check_device_errors()
+    b.v_scale[int(b.block_tables[1, 2]), 1] = 20.0
+    h.attention_varlen(b.q, b.k_cache, b.v_cache, m["qsl"], m["lens"], m["bt"], b.qsl,
+                       b.seq_lens, k_scale=b.k_scale, v_scale=b.v_scale)
+    with pytest.raises(pkv.PkvError) as e:
+        h.check_device_errors()
+    assert e.value.status == 5 and "scale" in str(e.value)
+    h.close()
+
+
+def test_a_device_wait_that_runs_out_is_reported():
+    """Failure detection without a fault: pkv_wait_selftest waits, through
+    the kernels' bounded-wait helper, on a barrier nothing arrives at; the
+    wait gives up after 10 us, the timeout comes back from
+    pkv_check_device_errors as PKV_ERR_TIMEOUT, the word is cleared, and the
+    handle still computes a correct step."""
+    s = spec("timeout", 8, 2, 16, [1, 20], [300, 700])
+    b = W.generate(s, DEV)
+    h = U.make_handle(b)
+    h.check_device_errors()
+    h.wait_selftest(10_000)
+    with pytest.raises(pkv.PkvError) as e:
+        h.check_device_errors()
+    assert e.value.status == 6
+    h.check_device_errors()                      # cleared
+    with pytest.raises(pkv.PkvError) as e:       # the limit is checked on the host
+        h.wait_selftest(0)
+    assert e.value.status == 1
+    sub = W.subset(b, [0, 1])
+    out, lse = U.gpu_step(b, handle=h)
+    ref, ref_lse = U.oracle_subset(sub, b.spec)
+    got, got_lse = U.gpu_rows(out, lse, sub)
+    U.check(got, ref, got_lse, ref_lse, "bf16", "after timeout", scaled=True)
     h.close()
 
 

@@ -161,6 +161,17 @@ def test_plan_splits_fill_the_machine():
     assert len(items) >= 4 * 152 and parts <= 16384
 
 
+def test_one_long_request_splits_into_many_ranges():
+    """A lone 600K-token decode is cut into more than 32 ranges per (request,
+    KV head) pair (the case the wide merge kernel serves), every range a
+    multiple of 256 keys long except the last."""
+    spec = workloads.custom_spec("long_one", 32, 8, 16, [1], [600_000])
+    _check_plan(spec)
+    items, parts, _ = _plan(spec)
+    assert all(w["n_split"] > 32 for w in items)
+    assert parts == len(items)
+
+
 @pytest.mark.parametrize("qsl,lens,msg", [
     ([1, 2], [5], "query_start_loc_host[0]"),
     ([0, 3, 2], [5, 5], "decreases"),

@@ -211,25 +211,26 @@ def _layout(spec: Spec, perm_gen: torch.Generator, tail_entries: int):
     return tables, nblk, pool, poison_block, used
 
 
-def _fill_normal(t: torch.Tensor, g: torch.Generator, chunk_rows: int = 1 << 20):
-    """Fill a [rows, D] view with N(0,1) in chunks (bounded temporaries)."""
+def _fill_normal(t: torch.Tensor, g: torch.Generator, chunk_rows: int = 1 << 20,
+                 sigma: float = 1.0):
+    """Fill a [rows, D] view with N(0, sigma^2) in chunks (bounded temporaries)."""
     rows = t.shape[0]
     for r0 in range(0, rows, chunk_rows):
         r1 = min(rows, r0 + chunk_rows)
-        t[r0:r1] = torch.randn((r1 - r0, t.shape[1]), generator=g,
-                               device=t.device, dtype=torch.float32).to(t.dtype)
+        t[r0:r1] = (torch.randn((r1 - r0, t.shape[1]), generator=g, device=t.device,
+                                dtype=torch.float32) * sigma).to(t.dtype)
 
 
 def _fill_fp8_pool(codes: torch.Tensor, scales: torch.Tensor, g: torch.Generator,
-                   chunk_blocks: int = 2048):
-    """E4M3 pool from an N(0,1) source, one fp32 scale per (block, KV head):
-    scale = amax/448 over the block, codes = source/scale cast to E4M3 by
-    torch (a generator choice; the oracle reads the stored codes)."""
+                   chunk_blocks: int = 2048, sigma: float = 1.0):
+    """E4M3 pool from an N(0, sigma^2) source, one fp32 scale per (block, KV
+    head): scale = amax/448 over the block, codes = source/scale cast to E4M3
+    by torch (a generator choice; the oracle reads the stored codes)."""
     nb, hkv, bs, d = codes.shape
     for b0 in range(0, nb, chunk_blocks):
         b1 = min(nb, b0 + chunk_blocks)
         src = torch.randn((b1 - b0, hkv, bs, d), generator=g,
-                          device=codes.device, dtype=torch.float32)
+                          device=codes.device, dtype=torch.float32) * sigma
         amax = src.abs().amax(dim=(2, 3))
         sc = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
         q = (src / sc[:, :, None, None]).clamp(-E4M3_MAX, E4M3_MAX)
@@ -260,12 +261,12 @@ def nvfp4_row_bytes(bs: int, off: np.ndarray, head_dim: int = HEAD_DIM):
 
 
 def _fill_nvfp4_pool(tiles: torch.Tensor, scales: torch.Tensor, g: torch.Generator,
-                     chunk_blocks: int = 2048):
+                     chunk_blocks: int = 2048, sigma: float = 1.0):
     """NVFP4 tiles drawn directly as codes (no quantisation here): E2M1
     nibbles with Gaussian-like magnitude frequencies and random signs; micro
     scales the E4M3 codes (torch's cast) of U[1, 3] / (6 scale); the (block,
-    KV head) scale U[3.5, 4.5] / 2688, so that values look like a N(0, 1)
-    source quantised the usual way."""
+    KV head) scale sigma * U[3.5, 4.5] / 2688, so that values look like a
+    N(0, sigma^2) source quantised the usual way."""
     nb, hkv, tb = tiles.shape
     bs = tb // NVFP4_ROW
     gs = min(bs, NVFP4_GROUP)
@@ -284,13 +285,17 @@ def _fill_nvfp4_pool(tiles: torch.Tensor, scales: torch.Tensor, g: torch.Generat
         grp = tiles[b0:b1].view(n, hkv, bs // gs, gs * NVFP4_ROW)
         grp[..., :gs * 64] = codes.reshape(n, hkv, bs // gs, gs * 64)
         grp[..., gs * 64:] = ms.reshape(n, hkv, bs // gs, gs * 8)
-        scales[b0:b1] = sc
+        scales[b0:b1] = sc * sigma
 
 
 def generate(spec: Spec, device: str | torch.device = "cpu", q_scale: float = 1.0,
              tail_entries: int = 3, tail_fill: str = "poison_block",
-             unused_poison: bool = True) -> Batch:
+             unused_poison: bool = True, kv_sigma: float = 1.0) -> Batch:
     """Build one step's inputs for ``spec``.
+
+    K and V (pools and new rows) are drawn with standard deviation
+    ``kv_sigma`` (quantised pools: their block scales follow), queries with
+    ``q_scale``.
 
     History rows hold N(0,1) data; the rows of this step's new tokens and the
     rows past each sequence's end hold NaN poison until ``write_slots`` fills
@@ -328,16 +333,16 @@ def generate(spec: Spec, device: str | torch.device = "cpu", q_scale: float = 1.
     if nvfp4:
         k_scale = torch.empty((pool, hkv), dtype=torch.float32, device=device)
         v_scale = torch.empty_like(k_scale)
-        _fill_nvfp4_pool(k_cache, k_scale, _gen(spec.seed, S_K, gdev))
-        _fill_nvfp4_pool(v_cache, v_scale, _gen(spec.seed, S_V, gdev))
+        _fill_nvfp4_pool(k_cache, k_scale, _gen(spec.seed, S_K, gdev), sigma=kv_sigma)
+        _fill_nvfp4_pool(v_cache, v_scale, _gen(spec.seed, S_V, gdev), sigma=kv_sigma)
     elif fp8:
         k_scale = torch.empty((pool, hkv), dtype=torch.float32, device=device)
         v_scale = torch.empty_like(k_scale)
-        _fill_fp8_pool(k_cache, k_scale, _gen(spec.seed, S_K, gdev))
-        _fill_fp8_pool(v_cache, v_scale, _gen(spec.seed, S_V, gdev))
+        _fill_fp8_pool(k_cache, k_scale, _gen(spec.seed, S_K, gdev), sigma=kv_sigma)
+        _fill_fp8_pool(v_cache, v_scale, _gen(spec.seed, S_V, gdev), sigma=kv_sigma)
     else:
-        _fill_normal(k_cache.view(-1, d), _gen(spec.seed, S_K, gdev))
-        _fill_normal(v_cache.view(-1, d), _gen(spec.seed, S_V, gdev))
+        _fill_normal(k_cache.view(-1, d), _gen(spec.seed, S_K, gdev), sigma=kv_sigma)
+        _fill_normal(v_cache.view(-1, d), _gen(spec.seed, S_V, gdev), sigma=kv_sigma)
 
     def poison(cache, rows_blk, rows_off):
         if nvfp4:
@@ -384,10 +389,10 @@ def generate(spec: Spec, device: str | torch.device = "cpu", q_scale: float = 1.
 
     gq = _gen(spec.seed, S_Q, gdev)
     q = (torch.randn((T, hq, d), generator=gq, device=device) * q_scale).to(torch.bfloat16)
-    k_new = torch.randn((T, hkv, d), generator=_gen(spec.seed, S_KNEW, gdev),
-                        device=device).to(torch.bfloat16)
-    v_new = torch.randn((T, hkv, d), generator=_gen(spec.seed, S_VNEW, gdev),
-                        device=device).to(torch.bfloat16)
+    k_new = (torch.randn((T, hkv, d), generator=_gen(spec.seed, S_KNEW, gdev),
+                         device=device) * kv_sigma).to(torch.bfloat16)
+    v_new = (torch.randn((T, hkv, d), generator=_gen(spec.seed, S_VNEW, gdev),
+                         device=device) * kv_sigma).to(torch.bfloat16)
     return Batch(spec, qsl, seq_lens, tables.astype(np.int32), slots, pool,
                  poison_block, q, k_new, v_new, k_cache, v_cache, k_scale,
                  v_scale)
