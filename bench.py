@@ -197,13 +197,19 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ---------------------------------------------------------------- our arm --
 
-def make_handle(batch, flags):
+def make_handle(batch, flags, stage=True):
+    """A handle for the step; E4M3 / NVFP4 pools get K/V staging pools with
+    room for every request's context (the staged tensor-core prefill) unless
+    stage=False."""
     import paged_kv_attention_pkv_gb300 as pkv
     s = batch.spec
+    stage_tokens = (sum(W.cdiv(L, s.block_size) * s.block_size for L in s.seq_lens)
+                    if stage and s.kv_dtype != "bf16" else 0)
     cfg = pkv.make_config(s.hq, s.hkv, s.block_size, batch.num_blocks, s.num_seqs,
                           s.num_tokens, softmax_scale=s.softmax_scale, flags=flags,
                           kv_dtype={"bf16": pkv.KV_BF16, "fp8": pkv.KV_FP8_E4M3,
-                                    "nvfp4": pkv.KV_NVFP4}[s.kv_dtype])
+                                    "nvfp4": pkv.KV_NVFP4}[s.kv_dtype],
+                          stage_tokens=stage_tokens)
     return pkv.Handle(cfg, device=batch.q.device.index or 0)
 
 
@@ -217,13 +223,13 @@ def device_meta(batch):
 
 def time_workload(index, steps: int, warmup: int, world: int, peaks: dict,
                   device: str, sampler: ClockSampler | None = None, e2e: bool = False,
-                  separate: bool = False):
+                  separate: bool = False, stage: bool = True):
     import paged_kv_attention_pkv_gb300 as pkv
 
     spec = W.config_spec(index) if isinstance(index, int) else index
     batch = W.generate(spec, device)
     work = W.algorithmic_work(spec)
-    h = make_handle(batch, pkv.FLAG_TIMING | (pkv.FLAG_SEPARATE if separate else 0))
+    h = make_handle(batch, pkv.FLAG_TIMING | (pkv.FLAG_SEPARATE if separate else 0), stage)
     m = device_meta(batch)
     out = torch.empty_like(batch.q)
     stream = torch.cuda.current_stream()
@@ -260,7 +266,7 @@ def time_workload(index, steps: int, warmup: int, world: int, peaks: dict,
     per_kind = {}
     for kind, name in ((pkv.KERNEL_APPEND, "append"), (pkv.KERNEL_DECODE, "decode"),
                        (pkv.KERNEL_PREFILL, "prefill"), (pkv.KERNEL_MIXED, "mixed"),
-                       (pkv.KERNEL_MERGE, "merge")):
+                       (pkv.KERNEL_MERGE, "merge"), (pkv.KERNEL_STAGE, "stage")):
         n, tot = h.timing_read(kind)
         if n:
             per_kind[name] = (n, tot / n)
@@ -538,7 +544,7 @@ def time_per_call(index, device: str, calls: int = 20, warmup: int = 5) -> dict:
             spans.append(e0.elapsed_time(e1) * 1e3)
         kernels_us = 0.0
         for kind in (pkv.KERNEL_APPEND, pkv.KERNEL_DECODE, pkv.KERNEL_PREFILL,
-                     pkv.KERNEL_MIXED, pkv.KERNEL_MERGE):
+                     pkv.KERNEL_MIXED, pkv.KERNEL_MERGE, pkv.KERNEL_STAGE):
             n, tot = h.timing_read(kind)
             if n:
                 kernels_us += tot / n * 1e3
@@ -569,6 +575,17 @@ def secondary(args, world, peaks, device):
     for idx, steps in ((2, 10), (fp8_pf, 10), (nv_pf, 5), (3, 10), (4, 50), (nvfp4, 50)):
         r = time_workload(idx, steps, 3, world, peaks, device)
         spec, work = r["spec"], r["work"]
+        unstaged = None
+        if "stage" in r["kinds"]:
+            # the same step with no staging pools: the prefill kernel converts
+            # the E4M3 / NVFP4 codes itself
+            u = time_workload(idx, steps, 3, world, peaks, device, stage=False)
+            n, avg = u["kinds"]["prefill"]
+            tf = work["prefill_flops"] / (avg * 1e-3) / 1e12
+            unstaged = {"ms_per_step": round(u["ms"] / steps, 4),
+                        "kernel_ms": {k: round(v[1], 4) for k, v in u["kinds"].items()},
+                        "prefill": {"value": round(tf, 1), "unit": "TFLOP/s",
+                                    "frac": round(tf / peaks["bf16_tflops"], 4)}}
         ms_step = r["ms"] / steps
         ent = {"workload": spec.name, "ms_per_step": round(ms_step, 4),
                "kernel_ms": {k: round(v[1], 4) for k, v in r["kinds"].items()}}
@@ -588,15 +605,23 @@ def secondary(args, world, peaks, device):
                                              for k, v in r["kinds"].items()}}
         if work["prefill_flops"]:
             n, avg = r["kinds"]["prefill"]
+            # E4M3 / NVFP4 KV: the K/V staging kernel counts as prefill time
+            avg += r["kinds"].get("stage", (0, 0.0))[1]
             tf = work["prefill_flops"] / (avg * 1e-3) / 1e12
             peak = peaks["bf16_tflops"]
-            # E4M3 KV: QK runs as two FP8 MMAs (query hi + lo parts) and PV in
-            # f16; NVFP4 KV: both in f16; the tensor time of the bf16 kernel
+            # staged E4M3 / NVFP4 KV runs the bf16 kernel on bf16 K/V; unstaged,
+            # E4M3 KV runs QK as two FP8 MMAs (query hi + lo parts) and PV in
+            # f16, NVFP4 KV both in f16: the tensor time of the bf16 kernel
             # either way, so the same bf16 peak applies
             ent["prefill"] = {"value": round(tf, 1), "unit": "TFLOP/s", "bound": "tensor",
                               "frac": round(tf / peak, 4), "peak": peak,
                               "peak_source": f"{peaks['source']} (bf16_tflops)",
-                              "flops_per_launch": work["prefill_flops"]}
+                              "flops_per_launch": work["prefill_flops"],
+                              "ms": round(avg, 4),
+                              "includes": "K/V staging + prefill" if "stage" in r["kinds"]
+                              else "prefill"}
+            if unstaged:
+                ent["unstaged"] = unstaged
         if work["decode_bytes"]:
             n, avg = r["kinds"]["decode"]
             # the decode kernel and the merge of its split ranges

@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                 7: "PKV_ERR_WORKSPACE"}
 KV_BF16, KV_FP8_E4M3, KV_NVFP4 = 0, 1, 2
 FLAG_VALIDATE, FLAG_TIMING, FLAG_SEPARATE = 1, 2, 4
-KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL, KERNEL_MIXED, KERNEL_MERGE = 0, 1, 2, 3, 4
+KERNEL_APPEND, KERNEL_DECODE, KERNEL_PREFILL, KERNEL_MIXED, KERNEL_MERGE, KERNEL_STAGE = \
+    0, 1, 2, 3, 4, 5
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ["pkv_create", "pkv_write_slots", "pkv_attention_varlen",
@@ -52,7 +53,8 @@ class Config(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
                 ("num_blocks", ctypes.c_int64), ("max_num_seqs", ctypes.c_int32),
-                ("max_num_tokens", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("max_num_tokens", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("stage_tokens", ctypes.c_int64)]
 
 
 class WorkItem(ctypes.Structure):
@@ -165,12 +167,12 @@ def _stream(stream, device) -> ctypes.c_void_p:
 
 def make_config(num_q_heads, num_kv_heads, block_size, num_blocks, max_num_seqs,
                 max_num_tokens, kv_dtype=KV_BF16, softmax_scale=None, flags=0,
-                head_dim=128) -> Config:
+                head_dim=128, stage_tokens=0) -> Config:
     if softmax_scale is None:
         softmax_scale = head_dim ** -0.5
     return Config(num_q_heads, num_kv_heads, head_dim, block_size, kv_dtype,
                   float(softmax_scale), int(num_blocks), max_num_seqs,
-                  max_num_tokens, flags)
+                  max_num_tokens, flags, int(stage_tokens))
 
 
 def pool_shapes(config: Config):

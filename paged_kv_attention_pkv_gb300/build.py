@@ -14,7 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkv.so")
-SOURCES = ["pkv_api.cu", "kv_append.cu", "decode.cu", "decode_static.cu", "prefill_tc.cu", "mixed.cu", "lse_merge.cu", "blocks.cpp"]
+SOURCES = ["pkv_api.cu", "kv_append.cu", "decode.cu", "decode_static.cu", "prefill_tc.cu",
+           "mixed.cu", "lse_merge.cu", "stage_kv.cu", "blocks.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
          "-Xptxas", "-v", "--expt-relaxed-constexpr", "-Wno-deprecated-gpu-targets"]

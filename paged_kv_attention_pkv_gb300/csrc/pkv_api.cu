@@ -76,6 +76,13 @@ struct pkv_handle {
   float *d_part_o = nullptr;
   float *d_part_lse = nullptr;
   int32_t *d_err = nullptr;
+  // E4M3 / NVFP4 pools: K and V staged as bf16 for the tensor-core prefill
+  // (stage_kv.cu), stage_blocks blocks of [hkv][bs][128] each, K's block
+  // scales, and the pools' tensor maps
+  __nv_bfloat16 *d_stage_k = nullptr, *d_stage_v = nullptr;
+  float *d_stage_ks = nullptr;   // [stage_blocks][hkv]
+  int64_t stage_blocks = 0;
+  CUtensorMap stage_map_k{}, stage_map_v{};
   uint8_t *h_stage[2] = {nullptr, nullptr};   // pinned staging (double buffer)
   cudaEvent_t staged[2] = {nullptr, nullptr};
   int stage_cur = 0;
@@ -123,6 +130,7 @@ std::string check_config(const pkv_config *c, pkv_status *st) {
     return fmt("unknown kv_dtype %d", c->kv_dtype);
   if (c->flags & ~static_cast<uint32_t>(PKV_FLAG_VALIDATE | PKV_FLAG_TIMING | PKV_FLAG_SEPARATE))
     return fmt("unknown flag bits 0x%x", c->flags);
+  if (c->stage_tokens < 0) return "stage_tokens must be >= 0";
   *st = PKV_ERR_UNSUPPORTED;
   if (c->head_dim != kHeadDim) return fmt("head_dim %d is not supported (only 128)", c->head_dim);
   const int bs = c->block_size;
@@ -453,22 +461,69 @@ bool encode_q_map(CUtensorMap *m, const void *q, int hq, int group, int64_t toke
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// K/V staging of a step's tensor-core prefill requests over E4M3 / NVFP4
+// pools (stage_kv.cu): base[i] = first staging block of request i (-1: not
+// staged) and reqs = (request, first block, context length) per staged
+// request.  Returns the staging blocks used, or 0 when the step does not
+// stage (bf16 pools, no such request, or more blocks than the handle has).
+int64_t plan_staging(const pkv_config &c, int64_t capacity, const int32_t *qsl,
+                     const int32_t *lens, int B, std::vector<int32_t> *base,
+                     std::vector<int32_t> *reqs) {
+  base->assign(size_t(std::max(B, 0)), -1);
+  reqs->clear();
+  if (c.kv_dtype == PKV_KV_BF16 || capacity <= 0 || !prefill_uses_tc(c)) return 0;
+  const int G = c.num_q_heads / c.num_kv_heads;
+  int64_t next = 0;
+  for (int i = 0; i < B; ++i) {
+    const int64_t q = int64_t(qsl[i + 1]) - qsl[i];
+    if (q * G <= kDecCols) continue;
+    (*base)[i] = static_cast<int32_t>(std::min<int64_t>(next, INT32_MAX));
+    reqs->insert(reqs->end(), {i, (*base)[i], lens[i]});
+    next += (int64_t(lens[i]) + c.block_size - 1) / c.block_size;
+  }
+  if (next == 0 || next > capacity) {
+    base->assign(size_t(B), -1);
+    reqs->clear();
+    return 0;
+  }
+  return next;
+}
+
+// Offsets in the work buffer: the work items, the host mirrors (validate
+// mode), then the staging bases (per request) and staged requests (3 ints
+// each).
+size_t mirror_offset(int max_items);
+size_t stage_base_offset(int max_items, int max_seqs) {
+  return (mirror_offset(max_items) + sizeof(int32_t) * (2 * size_t(max_seqs) + 1) + 15) & ~size_t(15);
+}
+size_t stage_reqs_offset(int max_items, int max_seqs) {
+  return stage_base_offset(max_items, max_seqs) + sizeof(int32_t) * size_t(max_seqs);
+}
+
 // 16-token pools viewed as [2 halves][rows][64 columns] (the halves 128 B
 // apart, rows 256 B apart) with boxes of {64, 16, 2}: one box carries a whole
 // (block, KV head) tile of 4 KB as [half][16 rows][64], 128-byte swizzled.
 size_t items_bytes(int max_items) { return sizeof(pkv_work_item) * size_t(max_items); }
+size_t mirror_offset(int max_items) { return items_bytes(max_items); }
 
 // Lays out a plan's work items (decode items, then prefill tiles) at `dst`,
-// and the host mirrors at dst + mirror_off in validate mode; returns the
-// bytes of the work items.
+// the host mirrors at dst + mirror_off in validate mode, and the K/V staging
+// tables (when the step stages) at their offsets; returns the bytes of the
+// work items.
 size_t stage_plan(const Plan &plan, const int32_t *qsl_host, const int32_t *lens_host,
-                  int num_seqs, bool validate, size_t mirror_off, uint8_t *dst) {
+                  int num_seqs, bool validate, size_t mirror_off, uint8_t *dst,
+                  const std::vector<int32_t> &sbase, const std::vector<int32_t> &sreqs,
+                  size_t base_off, size_t reqs_off) {
   std::memcpy(dst, plan.dec.data(), items_bytes(plan.dec.size()));
   std::memcpy(dst + items_bytes(plan.dec.size()), plan.pre.data(), items_bytes(plan.pre.size()));
   if (validate) {
     std::memcpy(dst + mirror_off, qsl_host, sizeof(int32_t) * (num_seqs + 1));
     std::memcpy(dst + mirror_off + sizeof(int32_t) * (num_seqs + 1), lens_host,
                 sizeof(int32_t) * num_seqs);
+  }
+  if (!sreqs.empty()) {
+    std::memcpy(dst + base_off, sbase.data(), sizeof(int32_t) * sbase.size());
+    std::memcpy(dst + reqs_off, sreqs.data(), sizeof(int32_t) * sreqs.size());
   }
   return items_bytes(plan.dec.size() + plan.pre.size());
 }
@@ -571,7 +626,16 @@ pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out) {
     return PKV_ERR_INVALID_ARG;
   }
   h->max_items = static_cast<int>(max_items);
-  h->work_bytes = items_bytes(h->max_items) + sizeof(int32_t) * (2 * size_t(config->max_num_seqs) + 1);
+  h->work_bytes = stage_reqs_offset(h->max_items, config->max_num_seqs) +
+                  sizeof(int32_t) * 3 * size_t(config->max_num_seqs);
+  if (config->kv_dtype != PKV_KV_BF16 && config->stage_tokens > 0 && prefill_uses_tc(*config)) {
+    h->stage_blocks = (config->stage_tokens + config->block_size - 1) / config->block_size;
+    if (h->stage_blocks * config->num_kv_heads * config->block_size > kMaxPoolRows) {
+      g_create_error = "stage_tokens too large: the staging pools would exceed 2^31 - 4096 rows";
+      delete h;
+      return PKV_ERR_INVALID_ARG;
+    }
+  }
   bool ok = cudaMalloc(&h->d_work, h->work_bytes) == cudaSuccess &&
             cudaMalloc(&h->d_part_o, sizeof(float) * size_t(kMaxPartials) * kDecCols * kHeadDim) == cudaSuccess &&
             cudaMalloc(&h->d_part_lse, sizeof(float) * size_t(kMaxPartials) * kDecCols) == cudaSuccess &&
@@ -582,6 +646,18 @@ pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out) {
             cudaEventCreateWithFlags(&h->staged[1], cudaEventDisableTiming) == cudaSuccess;
   if (ok) {
     ok = cudaMemset(h->d_err, 0, sizeof(int32_t)) == cudaSuccess;
+  }
+  if (ok && h->stage_blocks > 0) {
+    const int64_t rows = h->stage_blocks * config->num_kv_heads * config->block_size;
+    const size_t bytes = size_t(rows) * kHeadDim * sizeof(__nv_bfloat16);
+    ok = cudaMalloc(&h->d_stage_k, bytes) == cudaSuccess &&
+         cudaMalloc(&h->d_stage_v, bytes) == cudaSuccess &&
+         cudaMalloc(&h->d_stage_ks, sizeof(float) * size_t(h->stage_blocks) *
+                                        config->num_kv_heads) == cudaSuccess &&
+         encode_pool_map(&h->stage_map_k, h->d_stage_k, false, rows,
+                         std::min(config->block_size, 128)) &&
+         encode_pool_map(&h->stage_map_v, h->d_stage_v, false, rows,
+                         std::min(config->block_size, 128));
   }
   if (ok && (config->flags & PKV_FLAG_TIMING)) {
     h->timing = true;
@@ -609,6 +685,9 @@ pkv_status pkv_destroy(pkv_handle *h) {
   cudaFree(h->d_part_o);
   cudaFree(h->d_part_lse);
   cudaFree(h->d_err);
+  cudaFree(h->d_stage_k);
+  cudaFree(h->d_stage_v);
+  cudaFree(h->d_stage_ks);
   for (int i = 0; i < 2; ++i) {
     if (h->h_stage[i]) cudaFreeHost(h->h_stage[i]);
     if (h->staged[i]) cudaEventDestroy(h->staged[i]);
@@ -761,7 +840,18 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     h->map_v_ptr = v_cache;
   }
 
-  // the work list (+ host mirrors for validate mode) in device memory
+  // E4M3 / NVFP4 pools: stage the tensor-core prefill requests' K and V as
+  // bf16 when they fit the handle's staging pools
+  std::vector<int32_t> sbase, sreqs;
+  const int64_t n_stage =
+      dcp == nullptr
+          ? plan_staging(c, h->stage_blocks, qsl_host, lens_host, num_seqs, &sbase, &sreqs)
+          : 0;
+  const size_t base_off = stage_base_offset(h->max_items, c.max_num_seqs);
+  const size_t reqs_off = stage_reqs_offset(h->max_items, c.max_num_seqs);
+
+  // the work list (+ host mirrors for validate mode, + staging tables) in
+  // device memory
   const bool validate = (c.flags & PKV_FLAG_VALIDATE) != 0;
   const size_t mirror_off = items_bytes(h->max_items);
   uint8_t *work = h->d_work;
@@ -773,11 +863,16 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     e = cudaEventSynchronize(h->staged[cur]);   // this buffer's previous copy is done
     if (e != cudaSuccess) return cuda_fail(h, e, "staging event");
     uint8_t *hs = h->h_stage[cur];
-    const size_t nbytes = stage_plan(plan, qsl_host, lens_host, num_seqs, validate, mirror_off, hs);
+    const size_t nbytes = stage_plan(plan, qsl_host, lens_host, num_seqs, validate, mirror_off,
+                                     hs, sbase, sreqs, base_off, reqs_off);
     e = cudaMemcpyAsync(h->d_work, hs, nbytes, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess && validate)
       e = cudaMemcpyAsync(h->d_work + mirror_off, hs + mirror_off,
                           sizeof(int32_t) * (2 * num_seqs + 1), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && n_stage > 0)
+      e = cudaMemcpyAsync(h->d_work + base_off, hs + base_off,
+                          reqs_off - base_off + sizeof(int32_t) * sreqs.size(),
+                          cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaEventRecord(h->staged[cur], s);
     if (e != cudaSuccess) return cuda_fail(h, e, "work-list upload");
   }
@@ -877,7 +972,39 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     timing_end(h, PKV_KERNEL_DECODE, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
   }
-  if (n_pre > 0) {
+  if (n_pre > 0 && n_stage > 0) {
+    // E4M3 / NVFP4 K and V converted once to bf16, then the prefill
+    StageParams sp{};
+    sp.k_pool = static_cast<const uint8_t *>(k_cache);
+    sp.v_pool = static_cast<const uint8_t *>(v_cache);
+    sp.k_scale = k_scale;
+    sp.v_scale = v_scale;
+    sp.block_tables = block_tables;
+    sp.bt_stride = block_table_stride;
+    sp.reqs = reinterpret_cast<const int32_t *>(work + reqs_off);
+    sp.n_reqs = static_cast<int32_t>(sreqs.size() / 3);
+    sp.k_stage = h->d_stage_k;
+    sp.v_stage = h->d_stage_v;
+    sp.k_stage_scale = h->d_stage_ks;
+    sp.hkv = c.num_kv_heads;
+    sp.bs = bs;
+    sp.num_blocks = c.num_blocks;
+    sp.err = h->d_err;
+    timing_begin(h, PKV_KERNEL_STAGE, s);
+    e = launch_stage_kv(sp, static_cast<int>(n_stage), c.kv_dtype, s);
+    timing_end(h, PKV_KERNEL_STAGE, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "K/V staging launch");
+    PrefillParams ps = pp;
+    ps.k_scale = h->d_stage_ks;
+    ps.v_scale = nullptr;
+    ps.stage_base = reinterpret_cast<const int32_t *>(work + base_off);
+    ps.num_blocks = n_stage;
+    ps.rows_total = static_cast<int32_t>(n_stage * c.num_kv_heads * bs);
+    timing_begin(h, PKV_KERNEL_PREFILL, s);
+    e = launch_prefill_tc(qmap, h->stage_map_k, h->stage_map_v, ps, n_pre, kFmtStaged, s);
+    timing_end(h, PKV_KERNEL_PREFILL, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
+  } else if (n_pre > 0) {
     timing_begin(h, PKV_KERNEL_PREFILL, s);
     e = launch_prefill_tc(qmap, h->pf_k, h->pf_v, pp, n_pre, c.kv_dtype, s);
     timing_end(h, PKV_KERNEL_PREFILL, s);
@@ -1026,7 +1153,11 @@ pkv_status pkv_graph_prepare(pkv_handle *h, const int32_t *qsl_host,
     return fail(h, PKV_ERR_OUT_OF_MEMORY, fmt("graph work list: %s", cudaGetErrorString(e)));
   std::vector<uint8_t> host(h->work_bytes, 0);
   const size_t mirror_off = items_bytes(h->max_items);
-  stage_plan(plan, qsl_host, lens_host, num_seqs, true, mirror_off, host.data());
+  std::vector<int32_t> sbase, sreqs;
+  plan_staging(c, h->stage_blocks, qsl_host, lens_host, num_seqs, &sbase, &sreqs);
+  stage_plan(plan, qsl_host, lens_host, num_seqs, true, mirror_off, host.data(), sbase, sreqs,
+             stage_base_offset(h->max_items, c.max_num_seqs),
+             stage_reqs_offset(h->max_items, c.max_num_seqs));
   // synchronous on purpose: the buffer must hold this plan before any replay
   if ((e = cudaMemcpy(h->d_graph_work, host.data(), h->work_bytes, cudaMemcpyHostToDevice)) != cudaSuccess)
     return cuda_fail(h, e, "graph work-list upload");

@@ -112,6 +112,36 @@ struct PrefillParams {
   // launch_prefill_merge
   float *part_o;
   float *part_lse;
+  // K/V staged as bf16 (stage_kv.cu, kernel format kFmtStaged): block j of
+  // request i is staging block stage_base[i] + j, k_scale holds the K scale
+  // of each staging (block, KV head), rows_total counts the staging pools'
+  // rows; NULL: blocks come from block_tables
+  const int32_t *stage_base;
+};
+
+// Kernel format of the tensor-core prefill over staged K/V (beyond the
+// pkv_kv_dtype values): bf16 tiles, K exact code values with a block scale
+// per 16-key group, V already scaled.
+constexpr int kFmtStaged = 3;
+
+// Staging of E4M3 / NVFP4 K and V as bf16 for the tensor-core prefill
+// (stage_kv.cu).  reqs[3 r .. 3 r + 2] = (request index, first staging
+// block, context length) for the staged requests, ascending by first block.
+struct StageParams {
+  const uint8_t *k_pool;
+  const uint8_t *v_pool;
+  const float *k_scale;
+  const float *v_scale;
+  const int32_t *block_tables;
+  int32_t bt_stride;
+  const int32_t *reqs;
+  int32_t n_reqs;
+  __nv_bfloat16 *k_stage;   // [staging blocks][hkv][bs][128]
+  __nv_bfloat16 *v_stage;
+  float *k_stage_scale;     // [staging blocks][hkv]
+  int32_t hkv, bs;
+  int64_t num_blocks;       // blocks of the quantised pools
+  int32_t *err;
 };
 
 struct AppendParams {
@@ -177,6 +207,8 @@ cudaError_t launch_decode_merge(const DecodeParams &p, int num_groups, int max_s
                                 cudaStream_t s);
 cudaError_t launch_prefill_merge(const PrefillParams &p, int num_groups, cudaStream_t s);
 cudaError_t launch_check(const CheckParams &p, cudaStream_t s);
+cudaError_t launch_stage_kv(const StageParams &p, int num_stage_blocks, int kv_dtype,
+                            cudaStream_t s);
 cudaError_t launch_wait_selftest(int32_t *err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_lse_merge(const float *parts_o, const float *parts_lse, int num_parts,
                              int64_t num_rows, __nv_bfloat16 *out, float *lse,

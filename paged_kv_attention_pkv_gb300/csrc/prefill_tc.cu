@@ -119,7 +119,10 @@ cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
                               const CUtensorMap &vmap, const PrefillParams &p,
                               int num_items, int kv_dtype, cudaStream_t s) {
   if (num_items == 0) return cudaSuccess;
-  if (kv_dtype == PKV_KV_NVFP4)
+  if (kv_dtype == kFmtStaged)
+    prefill_tc_kernel<kFmtStaged><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap,
+                                                                              vmap, p);
+  else if (kv_dtype == PKV_KV_NVFP4)
     prefill_tc_kernel<PKV_KV_NVFP4><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap,
                                                                                vmap, p);
   else if (kv_dtype == PKV_KV_FP8_E4M3)
@@ -140,6 +143,7 @@ cudaError_t launch_prefill_merge(const PrefillParams &p, int num_groups, cudaStr
 cudaError_t configure_prefill_tc() {
   cudaError_t e = configure_one<PKV_KV_BF16>();
   if (e == cudaSuccess) e = configure_one<PKV_KV_FP8_E4M3>();
+  if (e == cudaSuccess) e = configure_one<kFmtStaged>();
   return e != cudaSuccess ? e : configure_one<PKV_KV_NVFP4>();
 }
 

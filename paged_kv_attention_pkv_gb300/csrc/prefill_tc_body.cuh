@@ -108,7 +108,9 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 // One prefill work item processed by all kTcThreads threads of the CTA;
 // `smem` is 1024-byte aligned (kTcSmemBytes - 1024 bytes).  FMT is the pool
 // format (pkv_kv_dtype): bf16, E4M3 or NVFP4 codes with one fp32 scale per
-// (block, KV head).
+// (block, KV head); or kFmtStaged, E4M3 / NVFP4 K and V staged as bf16
+// (stage_kv.cu): the bf16 data path, with K's block scales (K holds exact
+// code values) applied per 16-key group as for the quantised pools.
 template <int FMT>
 __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
                                                 const CUtensorMap &kmap,
@@ -118,6 +120,10 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
   constexpr bool FP8 = FMT == PKV_KV_FP8_E4M3;
   constexpr bool NV = FMT == PKV_KV_NVFP4;
   constexpr bool CONV = FP8 || NV;    // converter warps, scale ring, Q converted
+  constexpr bool STG = FMT == kFmtStaged;
+  constexpr bool KSC = CONV || STG;   // K block scales per 16-key group (scale ring)
+  constexpr bool QCV = CONV;          // the softmax warps convert Q first (q_ready)
+  constexpr bool QF16 = NV;           // ... into f16 (QK in f16)
   constexpr int VST = NV ? kVstN : kVst;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint64_t *q_full = bars + 0;
@@ -178,16 +184,18 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
     }
+    if (QCV)
+      for (int i = 0; i < 2; ++i) mbar_init(&q_ready[i], 128);
     if (CONV) {
       for (int i = 0; i < 2; ++i) {
-        mbar_init(&q_ready[i], 128);
         mbar_init(&vs_full[i], 1);
         mbar_init(&vs_empty[i], 2);
         mbar_init(&ks_full[i], 1);
         mbar_init(&ks_empty[i], 2);
       }
-      for (int i = 0; i < kScaleRing; ++i) mbar_init(&sc_ready[i], 1);
     }
+    if (KSC)
+      for (int i = 0; i < kScaleRing; ++i) mbar_init(&sc_ready[i], 1);
     prefetch_tmap(&qmap);
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
@@ -218,11 +226,13 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride + kb / p.bs;
     const int br = p.bs < 128 ? p.bs : 128;
     const int nbox = 128 / br;  // <= 8
+    // staged K/V: a request's blocks are consecutive in the staging pool
+    const int32_t sbase = STG ? __ldg(p.stage_base + it.seq) + kb / p.bs : -1;
     auto tile_rows = [&](int j) {
       const int key = j * 128 + lane * br;
       int32_t y = p.rows_total;
       if (lane < nbox && j < n_tiles && key < kspan) {
-        const int32_t blk = __ldg(bt + key / p.bs);
+        const int32_t blk = STG ? sbase + key / p.bs : __ldg(bt + key / p.bs);
         if (blk >= 0 && blk < p.num_blocks)
           y = (blk * p.hkv + it.kv_head) * p.bs + key % p.bs;
         else if (is_k)
@@ -242,9 +252,28 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         tma_load_3d(smem + kOffQ + kTile + kHalf, &qmap, 64, it.kv_head * G, t1, q_full);
       }
     }
+    // staged K: lane g < 8 holds the block scale of key group g of a tile,
+    // loaded one tile ahead (like the box rows) so that no global load sits
+    // between the copies
+    auto tile_scale = [&](int j) {
+      const int key = j * 128 + 16 * lane;
+      return (STG && is_k && lane < 8 && j < n_tiles && key < kspan)
+                 ? __ldg(p.k_scale + static_cast<int64_t>(sbase + key / p.bs) * p.hkv + it.kv_head)
+                 : 1.f;
+    };
+    float sk_cur = tile_scale(0);
     int32_t y_cur = tile_rows(0);
     for (int j = 0; j < n_tiles; ++j) {
       const int32_t y_next = tile_rows(j + 1);
+      const float sk_next = tile_scale(j + 1);
+      if (STG && is_k) {
+        // tile j's K block scales for the softmax (the ring is 8 tiles deep;
+        // this warp runs at most kKst tiles ahead of it)
+        if (lane < 8) scales[(j % kScaleRing) * 16 + lane] = sk_cur;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sc_ready[j % kScaleRing]);
+      }
+      sk_cur = sk_next;
       const int s = j % nst;
       if (j >= nst &&
           !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((j / nst) - 1) & 1))) {
@@ -583,8 +612,8 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     if (lane == 0) {
       // E4M3 / NVFP4 pools: the softmax warps first turn Q tile t into E4M3
       // hi/lo parts / scaled f16
-      bool ok = CONV ? mbar_wait(&q_ready[0], 0) : mbar_wait(q_full, 0);
-      if (CONV) tc_fence_after();
+      bool ok = QCV ? mbar_wait(&q_ready[0], 0) : mbar_wait(q_full, 0);
+      if (QCV) tc_fence_after();
       // Descriptors are built once; tiles, stages and k-steps add constant
       // offsets to the start-address field (addresses stay < 256 KB, so the
       // 14-bit field never carries).  The issuing warp shares its SM
@@ -627,9 +656,9 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
           for (int ks = 0; ks < 8; ++ks) {
             const uint64_t off = ((ks >> 2) * kHalf + (ks & 3) * 32) >> 4;
             if (ks == 0)
-              tc_mma_first(d, a0, b0, NV ? kIdescQK16 : kIdescQK);
+              tc_mma_first(d, a0, b0, QF16 ? kIdescQK16 : kIdescQK);
             else
-              tc_mma_acc(d, a0 + off, b0 + off, NV ? kIdescQK16 : kIdescQK);
+              tc_mma_acc(d, a0 + off, b0 + off, QF16 ? kIdescQK16 : kIdescQK);
           }
         }
         tc_commit(&s_full[t]);
@@ -654,7 +683,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       };
       // prologue: QK of tile 0 for both Q tiles
       if (ok) ok = qk(0, 0);
-      if (CONV && ok && two) {
+      if (QCV && ok && two) {
         ok = mbar_wait(&q_ready[1], 0);
         tc_fence_after();
       }
@@ -704,14 +733,14 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     float m = -CUDART_INF_F;              // running max, log2 units
     float l = 0.f;
     bool ok = true;
-    if (CONV && ntl > 0) {
+    if (QCV && ntl > 0) {
       // E4M3 pools: this thread's Q row, scaled by a power of two sq (largest
       // |q sq| in [128, 256)), becomes hi + lo, both E4M3 (about bf16
       // precision), written in place over the row: hi into the tile's first
       // 128-byte half, lo into its second (each the 128B-swizzled K-major
-      // layout of a 128 x 128 E4M3 tile).  NVFP4 pools: the row becomes f16
-      // in place (largest |q sq| in [2^14, 2^15), the bf16 layout).  1/sq
-      // goes into this row's scale.
+      // layout of a 128 x 128 E4M3 tile).  NVFP4 pools and staged K/V: the
+      // row becomes f16 in place (largest |q sq| in [2^14, 2^15), the bf16
+      // layout).  1/sq goes into this row's scale.
       ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0));
       if (ok) {
         const uint32_t qt = smem_addr(smem + kOffQ + t * kTile);
@@ -733,11 +762,11 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
           amax = fmax3(amax, fabsf(__uint_as_float(w[i] << 16)),
                        fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
         const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
-        const int top = NV ? 14 : 7;
+        const int top = QF16 ? 14 : 7;
         const int k2 = top - e < 126 ? top - e : 126;
         const float sq = __uint_as_float(static_cast<uint32_t>(127 + k2) << 23);
         c *= __uint_as_float(static_cast<uint32_t>(127 - k2) << 23);
-        if constexpr (NV) {
+        if constexpr (QF16) {
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -753,7 +782,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
             }
         }
 #pragma unroll
-        for (int oc = 0; oc < (NV ? 0 : 8); ++oc) {   // 16 dims: words 8 oc .. 8 oc + 7
+        for (int oc = 0; oc < (QF16 ? 0 : 8); ++oc) {   // 16 dims: words 8 oc .. 8 oc + 7
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -800,7 +829,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       // score scale c * k_scale (positive), so maxima are taken per group
       float cg[8];
       float mt2;
-      if constexpr (CONV) {
+      if constexpr (KSC) {
         if (!__all_sync(0xffffffffu,
                         mbar_wait(&sc_ready[j % kScaleRing], (j / kScaleRing) & 1))) {
           ok = false;
@@ -851,7 +880,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         for (int k = 0; k < 32; ++k) {
           float x0, x1;
           fma2_bc(x0, x1, s[64 * hh + 2 * k], s[64 * hh + 2 * k + 1],
-                  CONV ? cg[(64 * hh + 2 * k) >> 4] : c, -m);
+                  KSC ? cg[(64 * hh + 2 * k) >> 4] : c, -m);
           const float e0 = ex2(x0), e1 = ex2(x1);
           add2(acc[(2 * k) & 7], acc[(2 * k + 1) & 7], e0, e1);
           // E4M3 and NVFP4 pools run PV in f16 (V converted to f16)

@@ -26,12 +26,23 @@ TOL = {
 KV_DTYPES = {"bf16": pkv.KV_BF16, "fp8": pkv.KV_FP8_E4M3, "nvfp4": pkv.KV_NVFP4}
 
 
-def make_handle(batch: W.Batch, flags: int = pkv.FLAG_VALIDATE) -> pkv.Handle:
+def stage_tokens_for(spec: W.Spec) -> int:
+    """Staging capacity that lets a step of `spec` stage every request's
+    context (E4M3 / NVFP4 pools; bf16 pools ignore it)."""
+    bs = spec.block_size
+    return sum(W.cdiv(L, bs) * bs for L in spec.seq_lens) if spec.kv_dtype != "bf16" else 0
+
+
+def make_handle(batch: W.Batch, flags: int = pkv.FLAG_VALIDATE, stage: bool = True) -> pkv.Handle:
+    """A handle for `batch`; quantised pools get staging pools large enough
+    for the whole step unless stage=False (the prefill kernel then converts
+    the codes itself)."""
     s = batch.spec
     cfg = pkv.make_config(s.hq, s.hkv, s.block_size, batch.num_blocks,
                           max(1, s.num_seqs), max(1, s.num_tokens),
                           kv_dtype=KV_DTYPES[s.kv_dtype],
-                          softmax_scale=s.softmax_scale, flags=flags)
+                          softmax_scale=s.softmax_scale, flags=flags,
+                          stage_tokens=stage_tokens_for(s) if stage else 0)
     return pkv.Handle(cfg)
 
 
@@ -46,9 +57,9 @@ def device_meta(batch: W.Batch) -> dict:
 
 
 def gpu_step(batch: W.Batch, handle: pkv.Handle | None = None,
-             flags: int = pkv.FLAG_VALIDATE, append: bool = True):
+             flags: int = pkv.FLAG_VALIDATE, append: bool = True, stage: bool = True):
     """write_slots + attention_varlen through the C ABI; returns (out, lse)."""
-    h = handle or make_handle(batch, flags)
+    h = handle or make_handle(batch, flags, stage)
     m = device_meta(batch)
     if append:
         h.write_slots(batch.k_new, batch.v_new, m["slots"], batch.k_cache,
@@ -131,10 +142,10 @@ def check(got, ref, got_lse, ref_lse, kind: str = "bf16", what: str = "",
 
 
 def full_parity(batch: W.Batch, flags: int = pkv.FLAG_VALIDATE, what: str = "",
-                peaked: bool = False):
+                peaked: bool = False, stage: bool = True):
     """Every row of a (small) batch against the oracle."""
     sub = W.subset(batch, list(range(batch.spec.num_seqs)))
-    out, lse = gpu_step(batch, flags=flags)
+    out, lse = gpu_step(batch, flags=flags, stage=stage)
     ref, ref_lse = oracle_subset(sub, batch.spec)
     got, got_lse = gpu_rows(out, lse, sub)
     return check(got, ref, got_lse, ref_lse, batch.spec.kv_dtype, what, peaked, scaled=True)

@@ -142,9 +142,51 @@ SWEEP = [
 @pytest.mark.parametrize("case", SWEEP, ids=lambda c: c[0])
 @pytest.mark.parametrize("q_scale", [1.0, 8.0], ids=["normal", "peaked"])
 def test_small_cases_every_row(case, q_scale):
+    """Quantised pools stage K/V as bf16 for their tensor-core prefill rows
+    (the handle has room for the whole step)."""
     name, hq, hkv, bs, ql, sl, kv = case
     b = W.generate(spec(name, hq, hkv, bs, ql, sl, kv=kv), DEV, q_scale=q_scale)
     U.full_parity(b, what=name, peaked=q_scale > 1.0)
+
+
+# quantised pools whose prefill rows run on the tensor cores
+FUSED = [c for c in SWEEP if c[6] != "bf16" and any(q * (c[1] // c[2]) > 8 for q in c[4])
+         and c[1] // c[2] <= 128]
+
+
+@pytest.mark.parametrize("case", FUSED, ids=lambda c: c[0])
+@pytest.mark.parametrize("q_scale", [1.0, 8.0], ids=["normal", "peaked"])
+def test_small_cases_unstaged_prefill(case, q_scale):
+    """The same cases with no staging pools: the prefill kernel converts the
+    E4M3 / NVFP4 codes itself (also the path of steps larger than the
+    staging pools)."""
+    name, hq, hkv, bs, ql, sl, kv = case
+    b = W.generate(spec(name, hq, hkv, bs, ql, sl, kv=kv), DEV, q_scale=q_scale)
+    U.full_parity(b, what=f"{name} unstaged", peaked=q_scale > 1.0, stage=False)
+
+
+@pytest.mark.parametrize("kv", ["fp8", "nvfp4"])
+def test_staging_is_used_when_it_fits(kv):
+    """A step whose prefill contexts fit the staging pools runs the staging
+    kernel and then the prefill; one that does not fit runs the prefill
+    alone (converting inside), both matching the oracle."""
+    s = spec(f"stage_fit_{kv}", 32, 8, 16, [40, 1, 70], [3000, 500, 900], kv=kv)
+    b = W.generate(s, DEV)
+    sub = W.subset(b, [0, 1, 2])
+    ref, ref_lse = U.oracle_subset(sub, s)
+    need = W.cdiv(3000, 16) * 16 + W.cdiv(900, 16) * 16     # the two prefill requests
+    for cap, staged in ((need, True), (need - 16, False)):
+        cfg = pkv.make_config(32, 8, 16, b.num_blocks, 3, s.num_tokens,
+                              kv_dtype=U.KV_DTYPES[kv], flags=pkv.FLAG_VALIDATE | pkv.FLAG_TIMING,
+                              stage_tokens=cap)
+        h = pkv.Handle(cfg)
+        b2 = W.generate(s, DEV)
+        out, lse = U.gpu_step(b2, handle=h)
+        assert h.timing_read(pkv.KERNEL_STAGE)[0] == (1 if staged else 0)
+        assert h.timing_read(pkv.KERNEL_PREFILL)[0] == 1
+        h.close()
+        got, got_lse = U.gpu_rows(out, lse, sub)
+        U.check(got, ref, got_lse, ref_lse, kv, f"stage_fit {kv} cap {cap}", scaled=True)
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
