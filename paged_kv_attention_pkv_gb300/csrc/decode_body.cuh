@@ -34,11 +34,13 @@ __device__ __forceinline__ int32_t pool_row(const int32_t *bt, int32_t key,
   return (blk * p.hkv + kvh) * p.bs + key % p.bs;
 }
 
-// Physical head-dim index of a row of the O^T accumulator in the E4M3 path
-// (row dr of m-tile mt): the V fragments are built from 4-byte words, so each
-// thread's 4 consecutive bytes feed rows (g, g+8) of two adjacent m-tiles.
-__device__ __forceinline__ int fp8_dmap(int mt, int dr) {
-  return 4 * ((dr & 7) + 8 * (mt >> 1)) + 2 * (mt & 1) + (dr >> 3);
+// E4M3 pools: key of MMA key slot r (0..15) of a 16-key sub-tile.  The V^T
+// fragments come from an 8-bit transposing ldmatrix, which gives lane
+// (g, t) keys 4t .. 4t+3 of a head dim: slots 2t, 2t+1 hold keys 4t, 4t+1
+// and slots 2t+8, 2t+9 keys 4t+2, 4t+3, so the QK MMA reads its K rows in
+// that order too (slot r of S^T is key fp8_key(r)).
+__device__ __forceinline__ int fp8_key(int r) {
+  return 4 * ((r & 7) >> 1) + 2 * (r >> 3) + (r & 1);
 }
 
 // Global key of an item-local key: the identity, or the shard view (see
@@ -289,6 +291,8 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       qf[ks][1] = v.y;
     }
   }
+  // the keys of this thread's two S^T rows (g, g+8) within a sub-tile
+  const int krow0 = FP8 ? fp8_key(g) : g, krow1 = FP8 ? fp8_key(g + 8) : g + 8;
   // causal limit of this thread's two columns (2t, 2t+1)
   const int c0 = it.row0 + 2 * t;
   const int pos0 = (2 * t < it.n_rows) ? it.hist + c0 / group : 0x7fffffff;
@@ -353,8 +357,8 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
         // are steps 2h, 2h+1 (words 0,1 -> a0,a2 of step 2h; 2,3 of 2h+1)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint4 x = lds128(kbase + swz128(16 * sub + g, 2 * t + h));
-          const uint4 y = lds128(kbase + swz128(16 * sub + g + 8, 2 * t + h));
+          const uint4 x = lds128(kbase + swz128(16 * sub + krow0, 2 * t + h));
+          const uint4 y = lds128(kbase + swz128(16 * sub + krow1, 2 * t + h));
           mma_e4m3(s[sub], x.x, y.x, x.y, y.y, qf[2 * h][0], qf[2 * h][1]);
           mma_e4m3(s[sub], x.x, y.x, x.y, y.y, qf[4 + 2 * h][0], qf[4 + 2 * h][1]);
           mma_e4m3(s[sub], x.z, y.z, x.w, y.w, qf[2 * h + 1][0], qf[2 * h + 1][1]);
@@ -382,8 +386,8 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
         sc0 *= sk_sub[sub] * inv_sq0;
         sc1 *= sk_sub[sub] * inv_sq1;
       }
-      const int kr0 = key0 + 16 * sub + g, kr1 = kr0 + 8;
-      const int gr0 = gkey0 + 16 * sub + g, gr1 = gr0 + 8;
+      const int kr0 = key0 + 16 * sub + krow0, kr1 = key0 + 16 * sub + krow1;
+      const int gr0 = gkey0 + 16 * sub + krow0, gr1 = gkey0 + 16 * sub + krow1;
       s[sub][0] = (kr0 < ke && gr0 <= pos0) ? s[sub][0] * sc0 : -CUDART_INF_F;
       s[sub][1] = (kr0 < ke && gr0 <= pos1) ? s[sub][1] * sc1 : -CUDART_INF_F;
       s[sub][2] = (kr1 < ke && gr1 <= pos0) ? s[sub][2] * sc0 : -CUDART_INF_F;
@@ -440,33 +444,38 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
                                 : 0xFFFFFFFFu;
       // ---- O^T += V^T P^T
       if constexpr (FP8) {
-        const int kA = 16 * sub + 2 * t;
-        // masks only on the item's last, partial sub-tile
+        // V^T fragments straight from the E4M3 tile: one 8-bit transposing
+        // ldmatrix gives two m-tiles (16 head dims each, lanes 0-15 address
+        // the sub-tile's 16 key rows in the first one's 16-byte chunk, lanes
+        // 16-31 in the second's); each register holds keys 4t .. 4t+3 of one
+        // head dim, converted exactly to f16 pairs for key slots (2t, 2t+1)
+        // and (2t+8, 2t+9) (see fp8_key).  Masks only on the item's last,
+        // partial sub-tile.
+        const uint32_t vrow = 16 * sub + (lane & 15);
         auto pv8 = [&](auto masked) {
+          uint32_t qlo = 0xFFFFFFFFu, qhi = 0xFFFFFFFFu;
+          if (decltype(masked)::value) {
+            const int kq = k16 + 4 * t;
+            qlo = (kq < ke ? 0x0000FFFFu : 0u) | (kq + 1 < ke ? 0xFFFF0000u : 0u);
+            qhi = (kq + 2 < ke ? 0x0000FFFFu : 0u) | (kq + 3 < ke ? 0xFFFF0000u : 0u);
+          }
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t ch = (g >> 2) + 2 * j;
-            const uint32_t bo = 4 * (g & 3);
-            const uint32_t wA = lds32(vbase + swz128(kA, ch) + bo);
-            const uint32_t wB = lds32(vbase + swz128(kA + 1, ch) + bo);
-            const uint32_t wC = lds32(vbase + swz128(kA + 8, ch) + bo);
-            const uint32_t wD = lds32(vbase + swz128(kA + 9, ch) + bo);
-            // pair the two keys' bytes per head-dim column, then convert
-            // in hardware: [A0 B0 A1 B1] and [A2 B2 A3 B3]
-            const uint32_t x01 = __byte_perm(wA, wB, 0x5140);
-            const uint32_t x23 = __byte_perm(wA, wB, 0x7362);
-            const uint32_t y01 = __byte_perm(wC, wD, 0x5140);
-            const uint32_t y23 = __byte_perm(wC, wD, 0x7362);
-            uint32_t a[8] = {e4m3x2lo_to_f16x2(x01), e4m3x2hi_to_f16x2(x01),
-                             e4m3x2lo_to_f16x2(y01), e4m3x2hi_to_f16x2(y01),
-                             e4m3x2lo_to_f16x2(x23), e4m3x2hi_to_f16x2(x23),
-                             e4m3x2lo_to_f16x2(y23), e4m3x2hi_to_f16x2(y23)};
-            if (decltype(masked)::value) {
+          for (int mp = 0; mp < 4; ++mp) {
+            uint32_t r[4];
+            ldsm_b8_x2_trans(vbase + swz128(vrow, 2 * mp + (lane >> 4)), r[0], r[1], r[2],
+                             r[3]);
 #pragma unroll
-              for (int u = 0; u < 8; ++u) a[u] &= (u & 2) ? mhi : mlo;
+            for (int h = 0; h < 2; ++h) {
+              uint32_t a0 = e4m3x2lo_to_f16x2(r[2 * h]), a2 = e4m3x2hi_to_f16x2(r[2 * h]);
+              uint32_t a1 = e4m3x2lo_to_f16x2(r[2 * h + 1]), a3 = e4m3x2hi_to_f16x2(r[2 * h + 1]);
+              if (decltype(masked)::value) {
+                a0 &= qlo;
+                a1 &= qlo;
+                a2 &= qhi;
+                a3 &= qhi;
+              }
+              mma_f16(acc[2 * mp + h], a0, a1, a2, a3, b0, b1);
             }
-            mma_f16(acc[2 * j], a[0], a[1], a[2], a[3], b0, b1);
-            mma_f16(acc[2 * j + 1], a[4], a[5], a[6], a[7], b0, b1);
           }
         };
         if (tail)
@@ -503,8 +512,7 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
 
   // P carried 2^kPExp: the effective running maxima are m - kPExp
   decode_finish<NW>(p, it, smem, tid, bar, FP8 ? m0 - kPExp : m0, FP8 ? m1 - kPExp : m1, l0,
-                    l1, acc, 1.f,
-                    [](int mt, int dr) { return FP8 ? fp8_dmap(mt, dr) : 16 * mt + dr; });
+                    l1, acc, 1.f, [](int mt, int dr) { return 16 * mt + dr; });
 }
 
 

@@ -130,6 +130,18 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0,
       : "r"(addr));
 }
 
+// Two 16 x 16 byte matrices, transposed: lanes 0-15 give the rows of the
+// first, lanes 16-31 of the second (16-byte aligned).  Lane 4c + t receives
+// rows 4t .. 4t+3 of column c in r0 (byte i = row 4t + i) and of column
+// c + 8 in r1 for the first matrix, the same of the second in r2, r3.
+__device__ __forceinline__ void ldsm_b8_x2_trans(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                                 uint32_t &r2, uint32_t &r3) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(addr));
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;"
