@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None, choices=sorted(CASES),
                     help="time a reduced workload only (for profiler captures)")
+    ap.add_argument("--no-stage", action="store_true",
+                    help="with --case: no K/V staging pools (E4M3 / NVFP4 prefill "
+                         "converts the codes inside the prefill kernel)")
     return ap.parse_args()
 
 
@@ -406,7 +409,7 @@ def cpu_baseline(min_seconds: float = 10.0):
 def run_case(args, local_rank):
     peaks = load_peaks()
     r = time_workload(case_spec(args.case), args.steps, args.warmup, 1, peaks,
-                      f"cuda:{local_rank}")
+                      f"cuda:{local_rank}", stage=not args.no_stage)
     work = r["work"]
     ent = {"case": r["spec"].name, "ms_per_step": r["ms"] / args.steps,
            "kernel_ms": {k: v[1] for k, v in r["kinds"].items()}, "work": work}
