@@ -108,17 +108,19 @@ typedef struct {
     int32_t max_num_tokens;    /* largest number of query tokens per step */
     uint32_t flags;            /* PKV_FLAG_* */
     int64_t stage_tokens;      /* E4M3 / NVFP4 pools: capacity, in tokens
-                                  (rounded up to whole blocks), of the K/V
+                                  (rounded up to whole blocks), of the
                                   staging pools for the tensor-core prefill
-                                  (see pkv_attention_varlen); 0 = none */
+                                  (V for E4M3, K and V for NVFP4; see
+                                  pkv_attention_varlen); 0 = none */
 } pkv_config;
 
 /*
  * Create a handle on CUDA device `device` and allocate its workspace (work
  * list, split partials, error word: a few tens of MB,
  * sized from max_num_seqs and max_num_tokens; with E4M3 / NVFP4 pools and
- * stage_tokens > 0 also the K and V staging pools, stage_tokens * Hkv * 512
- * bytes together).  *out receives the handle, or
+ * stage_tokens > 0 also the staging pools, stage_tokens * Hkv * 256
+ * bytes for E4M3 (V) and stage_tokens * Hkv * 516 for NVFP4 (K, V and K's
+ * block scales), rounded up to whole blocks).  *out receives the handle, or
  * NULL on failure.  Errors: PKV_ERR_INVALID_ARG (NULL pointers, bad config),
  * PKV_ERR_UNSUPPORTED (head_dim or block_size not handled), PKV_ERR_CUDA (no
  * such device), PKV_ERR_OUT_OF_MEMORY.
@@ -204,10 +206,10 @@ pkv_status pkv_rope_write_slots(pkv_handle *h, void *q, const void *k_new,
  * contexts of the step's tensor-core prefill requests (each rounded up to
  * whole blocks) fit the handle's staging pools (stage_tokens), a staging
  * kernel (PKV_KERNEL_STAGE) first converts every block they read to bf16
- * (K: its exact code values, the block scale kept apart for the scores; V:
- * value times block scale, rounded once), and the prefill kernel reads
- * those with bf16 MMAs; otherwise the prefill kernel converts the codes
- * itself.  When a step holds fewer tensor-core
+ * (NVFP4 K: its exact code values, the block scale kept apart for the
+ * scores; V: value times block scale, rounded once), and the prefill kernel
+ * reads those with bf16 MMAs (E4M3 K stays in the pool and feeds FP8 MMAs);
+ * otherwise the prefill kernel converts the codes itself.  When a step holds fewer tensor-core
  * prefill items than half the multiprocessors, their key ranges are split
  * into runs of whole 128-key tiles (boundaries at multiples of the block
  * size too, at or below each item's first query position); each range
@@ -381,8 +383,8 @@ pkv_status pkv_plan(const pkv_config *config, const int32_t *query_start_loc_hos
  * one PKV_KERNEL_MIXED launch; otherwise decode and prefill launch apart.
  * PKV_KERNEL_MERGE: the merge of split key ranges (decode pairs and prefill
  * row tiles), one window after the attention launches of a step that split
- * any ranges.  PKV_KERNEL_STAGE: the staging of E4M3 / NVFP4 K and V before
- * the tensor-core prefill. */
+ * any ranges.  PKV_KERNEL_STAGE: the staging of E4M3 V or NVFP4 K and V
+ * before the tensor-core prefill. */
 enum {
     PKV_KERNEL_APPEND = 0,
     PKV_KERNEL_DECODE = 1,

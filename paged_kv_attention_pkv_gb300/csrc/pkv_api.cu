@@ -76,9 +76,9 @@ struct pkv_handle {
   float *d_part_o = nullptr;
   float *d_part_lse = nullptr;
   int32_t *d_err = nullptr;
-  // E4M3 / NVFP4 pools: K and V staged as bf16 for the tensor-core prefill
-  // (stage_kv.cu), stage_blocks blocks of [hkv][bs][128] each, K's block
-  // scales, and the pools' tensor maps
+  // E4M3 / NVFP4 pools: V (and NVFP4 K) staged as bf16 for the tensor-core
+  // prefill (stage_kv.cu), stage_blocks blocks of [hkv][bs][128] each,
+  // NVFP4 K's block scales, and the pools' tensor maps
   __nv_bfloat16 *d_stage_k = nullptr, *d_stage_v = nullptr;
   float *d_stage_ks = nullptr;   // [stage_blocks][hkv]
   int64_t stage_blocks = 0;
@@ -648,16 +648,19 @@ pkv_status pkv_create(const pkv_config *config, int device, pkv_handle **out) {
     ok = cudaMemset(h->d_err, 0, sizeof(int32_t)) == cudaSuccess;
   }
   if (ok && h->stage_blocks > 0) {
+    // E4M3 pools stage V alone (the prefill reads E4M3 K with FP8 MMAs)
+    const bool with_k = config->kv_dtype == PKV_KV_NVFP4;
     const int64_t rows = h->stage_blocks * config->num_kv_heads * config->block_size;
     const size_t bytes = size_t(rows) * kHeadDim * sizeof(__nv_bfloat16);
-    ok = cudaMalloc(&h->d_stage_k, bytes) == cudaSuccess &&
-         cudaMalloc(&h->d_stage_v, bytes) == cudaSuccess &&
-         cudaMalloc(&h->d_stage_ks, sizeof(float) * size_t(h->stage_blocks) *
-                                        config->num_kv_heads) == cudaSuccess &&
-         encode_pool_map(&h->stage_map_k, h->d_stage_k, false, rows,
-                         std::min(config->block_size, 128)) &&
+    ok = cudaMalloc(&h->d_stage_v, bytes) == cudaSuccess &&
          encode_pool_map(&h->stage_map_v, h->d_stage_v, false, rows,
                          std::min(config->block_size, 128));
+    if (ok && with_k)
+      ok = cudaMalloc(&h->d_stage_k, bytes) == cudaSuccess &&
+           cudaMalloc(&h->d_stage_ks, sizeof(float) * size_t(h->stage_blocks) *
+                                          config->num_kv_heads) == cudaSuccess &&
+           encode_pool_map(&h->stage_map_k, h->d_stage_k, false, rows,
+                           std::min(config->block_size, 128));
   }
   if (ok && (config->flags & PKV_FLAG_TIMING)) {
     h->timing = true;
@@ -973,7 +976,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
   }
   if (n_pre > 0 && n_stage > 0) {
-    // E4M3 / NVFP4 K and V converted once to bf16, then the prefill
+    // NVFP4 K and V, or E4M3 V, converted once to bf16, then the prefill
     StageParams sp{};
     sp.k_pool = static_cast<const uint8_t *>(k_cache);
     sp.v_pool = static_cast<const uint8_t *>(v_cache);
@@ -995,13 +998,19 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     timing_end(h, PKV_KERNEL_STAGE, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "K/V staging launch");
     PrefillParams ps = pp;
-    ps.k_scale = h->d_stage_ks;
-    ps.v_scale = nullptr;
     ps.stage_base = reinterpret_cast<const int32_t *>(work + base_off);
-    ps.num_blocks = n_stage;
-    ps.rows_total = static_cast<int32_t>(n_stage * c.num_kv_heads * bs);
+    ps.stage_blocks = n_stage;
+    ps.stage_rows = static_cast<int32_t>(n_stage * c.num_kv_heads * bs);
+    const bool with_k = c.kv_dtype == PKV_KV_NVFP4;
+    if (with_k) {   // K from the staging pool too, with its staged block scales
+      ps.k_scale = h->d_stage_ks;
+      ps.v_scale = nullptr;
+      ps.num_blocks = n_stage;
+      ps.rows_total = ps.stage_rows;
+    }
     timing_begin(h, PKV_KERNEL_PREFILL, s);
-    e = launch_prefill_tc(qmap, h->stage_map_k, h->stage_map_v, ps, n_pre, kFmtStaged, s);
+    e = launch_prefill_tc(qmap, with_k ? h->stage_map_k : h->pf_k, h->stage_map_v, ps, n_pre,
+                          with_k ? kFmtStaged : kFmtStagedV, s);
     timing_end(h, PKV_KERNEL_PREFILL, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
   } else if (n_pre > 0) {

@@ -112,20 +112,26 @@ struct PrefillParams {
   // launch_prefill_merge
   float *part_o;
   float *part_lse;
-  // K/V staged as bf16 (stage_kv.cu, kernel format kFmtStaged): block j of
-  // request i is staging block stage_base[i] + j, k_scale holds the K scale
-  // of each staging (block, KV head), rows_total counts the staging pools'
-  // rows; NULL: blocks come from block_tables
+  // K/V staged as bf16 (stage_kv.cu; kernel formats kFmtStaged and
+  // kFmtStagedV): block j of request i is staging block stage_base[i] + j of
+  // stage_blocks, stage_rows rows in the staging pools; kFmtStaged: k_scale
+  // holds the K scale of each staging (block, KV head); NULL: blocks come
+  // from block_tables
   const int32_t *stage_base;
+  int64_t stage_blocks;
+  int32_t stage_rows;
 };
 
-// Kernel format of the tensor-core prefill over staged K/V (beyond the
-// pkv_kv_dtype values): bf16 tiles, K exact code values with a block scale
-// per 16-key group, V already scaled.
+// Kernel formats of the tensor-core prefill over staged K/V (beyond the
+// pkv_kv_dtype values).  kFmtStaged (NVFP4 pools): K and V staged as bf16
+// tiles, K exact code values with a block scale per 16-key group, V already
+// scaled.  kFmtStagedV (E4M3 pools): K read from the pool as for E4M3 (FP8
+// QK, block scale per 16-key group), V staged as bf16, already scaled.
 constexpr int kFmtStaged = 3;
+constexpr int kFmtStagedV = 4;
 
-// Staging of E4M3 / NVFP4 K and V as bf16 for the tensor-core prefill
-// (stage_kv.cu).  reqs[3 r .. 3 r + 2] = (request index, first staging
+// Staging for the tensor-core prefill (stage_kv.cu): NVFP4 K and V, or
+// E4M3 V alone, as bf16.  reqs[3 r .. 3 r + 2] = (request index, first staging
 // block, context length) for the staged requests, ascending by first block.
 struct StageParams {
   const uint8_t *k_pool;
@@ -136,9 +142,9 @@ struct StageParams {
   int32_t bt_stride;
   const int32_t *reqs;
   int32_t n_reqs;
-  __nv_bfloat16 *k_stage;   // [staging blocks][hkv][bs][128]
+  __nv_bfloat16 *k_stage;   // [staging blocks][hkv][bs][128]; NVFP4 only
   __nv_bfloat16 *v_stage;
-  float *k_stage_scale;     // [staging blocks][hkv]
+  float *k_stage_scale;     // [staging blocks][hkv]; NVFP4 only
   int32_t hkv, bs;
   int64_t num_blocks;       // blocks of the quantised pools
   int32_t *err;

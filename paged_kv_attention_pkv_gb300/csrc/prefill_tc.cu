@@ -122,6 +122,9 @@ cudaError_t launch_prefill_tc(const CUtensorMap &qmap, const CUtensorMap &kmap,
   if (kv_dtype == kFmtStaged)
     prefill_tc_kernel<kFmtStaged><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap,
                                                                               vmap, p);
+  else if (kv_dtype == kFmtStagedV)
+    prefill_tc_kernel<kFmtStagedV><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap,
+                                                                               vmap, p);
   else if (kv_dtype == PKV_KV_NVFP4)
     prefill_tc_kernel<PKV_KV_NVFP4><<<num_items, kTcThreads, kTcSmemBytes, s>>>(qmap, kmap,
                                                                                vmap, p);
@@ -144,6 +147,7 @@ cudaError_t configure_prefill_tc() {
   cudaError_t e = configure_one<PKV_KV_BF16>();
   if (e == cudaSuccess) e = configure_one<PKV_KV_FP8_E4M3>();
   if (e == cudaSuccess) e = configure_one<kFmtStaged>();
+  if (e == cudaSuccess) e = configure_one<kFmtStagedV>();
   return e != cudaSuccess ? e : configure_one<PKV_KV_NVFP4>();
 }
 

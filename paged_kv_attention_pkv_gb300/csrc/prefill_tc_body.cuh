@@ -108,9 +108,11 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 // One prefill work item processed by all kTcThreads threads of the CTA;
 // `smem` is 1024-byte aligned (kTcSmemBytes - 1024 bytes).  FMT is the pool
 // format (pkv_kv_dtype): bf16, E4M3 or NVFP4 codes with one fp32 scale per
-// (block, KV head); or kFmtStaged, E4M3 / NVFP4 K and V staged as bf16
+// (block, KV head); or kFmtStaged, NVFP4 K and V staged as bf16
 // (stage_kv.cu): the bf16 data path, with K's block scales (K holds exact
-// code values) applied per 16-key group as for the quantised pools.
+// code values) applied per 16-key group as for the quantised pools; or
+// kFmtStagedV, E4M3 K from the pool (FP8 QK as for FMT = E4M3) and V staged
+// as bf16 (bf16 PV), no converter warps.
 template <int FMT>
 __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
                                                 const CUtensorMap &kmap,
@@ -121,9 +123,12 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
   constexpr bool NV = FMT == PKV_KV_NVFP4;
   constexpr bool CONV = FP8 || NV;    // converter warps, scale ring, Q converted
   constexpr bool STG = FMT == kFmtStaged;
-  constexpr bool KSC = CONV || STG;   // K block scales per 16-key group (scale ring)
-  constexpr bool QCV = CONV;          // the softmax warps convert Q first (q_ready)
-  constexpr bool QF16 = NV;           // ... into f16 (QK in f16)
+  constexpr bool HYB = FMT == kFmtStagedV;
+  constexpr bool K8 = FP8 || HYB;            // E4M3 K tiles, FP8 QK
+  constexpr bool SV = STG || HYB;            // V from the staging pool
+  constexpr bool KSC = CONV || STG || HYB;   // K block scales per 16-key group (scale ring)
+  constexpr bool QCV = CONV || HYB;          // the softmax warps convert Q first (q_ready)
+  constexpr bool QF16 = NV;                  // ... into f16 (QK in f16), else E4M3 hi + lo
   constexpr int VST = NV ? kVstN : kVst;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint64_t *q_full = bars + 0;
@@ -209,8 +214,9 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
 
   if (warp >= 8) {
    setmaxnreg_dec<kRegsCtl>();
-   if (!CONV && (warp == 9 || warp == 10)) {
-    // ---------------- TMA producers: warp 9 loads Q and K, warp 10 V ----
+   if ((!CONV && !HYB && (warp == 9 || warp == 10)) || (HYB && warp == 10)) {
+    // ---------------- TMA producers: warp 9 loads Q and K, warp 10 V (only
+    // V over E4M3 K, which warp 9 loads as for E4M3 pools) ----
     // Each ring is filled in tile order; K_j waits for the QKs of tile
     // j - kKst, V_j for the PVs of tile j - kVst.  Small blocks take one box
     // per block and 64-column half (16 copies per 128-key tile for 16-token
@@ -220,20 +226,21 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
     const bool is_k = warp == 9;
     const CUtensorMap *map = is_k ? &kmap : &vmap;
     const int nst = is_k ? kKst : kVst;
-    uint8_t *ring = smem + (is_k ? kOffK : kOffV);
+    uint8_t *ring = smem + (is_k ? kOffK : HYB ? kOffV8 : kOffV);
     uint64_t *full = is_k ? k_full : v_full;
     uint64_t *empty = is_k ? k_empty : v_empty;
     const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride + kb / p.bs;
     const int br = p.bs < 128 ? p.bs : 128;
     const int nbox = 128 / br;  // <= 8
     // staged K/V: a request's blocks are consecutive in the staging pool
-    const int32_t sbase = STG ? __ldg(p.stage_base + it.seq) + kb / p.bs : -1;
+    const int32_t sbase = SV ? __ldg(p.stage_base + it.seq) + kb / p.bs : -1;
+    const int64_t nblk = SV ? p.stage_blocks : p.num_blocks;
     auto tile_rows = [&](int j) {
       const int key = j * 128 + lane * br;
-      int32_t y = p.rows_total;
+      int32_t y = SV ? p.stage_rows : p.rows_total;
       if (lane < nbox && j < n_tiles && key < kspan) {
-        const int32_t blk = STG ? sbase + key / p.bs : __ldg(bt + key / p.bs);
-        if (blk >= 0 && blk < p.num_blocks)
+        const int32_t blk = SV ? sbase + key / p.bs : __ldg(bt + key / p.bs);
+        if (blk >= 0 && blk < nblk)
           y = (blk * p.hkv + it.kv_head) * p.bs + key % p.bs;
         else if (is_k)
           record_error(p.err, kErrBadBlock);
@@ -281,9 +288,13 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         break;
       }
       uint8_t *dst = ring + s * kTile;
+      // boxes holding keys of this item; staged V over E4M3 K takes every
+      // box (those past the item's keys start past the pool's last row and
+      // arrive as zeros, and the staged rows past a request's context are
+      // zeros)
       int n = 0;
       for (int r = 0; r < 128; r += br)
-        if (j * 128 + r < kspan) ++n;
+        if ((HYB && !is_k) || j * 128 + r < kspan) ++n;
       if (lane == 0) mbar_arrive_expect_tx(&full[s], n * br * 128 * 2);
       for (int bx = 0; bx < n; ++bx) {
         const int32_t y = __shfl_sync(0xffffffffu, y_cur, bx);
@@ -294,10 +305,11 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       }
       y_cur = y_next;
     }
-   } else if (FP8 && warp == 9) {
+   } else if (K8 && warp == 9) {
     // ---------------- TMA producer, E4M3 pools: Q, the E4M3 K ring, the
     // E4M3 V staging ring (one box per block, no column halves), and each
-    // tile's block scales for the softmax and the converters ----
+    // tile's block scales for the softmax and the converters; over staged V
+    // (warp 10 loads it) Q, K and the K scales ----
     const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride + kb / p.bs;
     const int br = p.bs < 128 ? p.bs : 128;
     const int nbox = 128 / br;  // <= 8
@@ -312,7 +324,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
           y = (blk * p.hkv + it.kv_head) * p.bs + key % p.bs;
           const int64_t si = static_cast<int64_t>(blk) * p.hkv + it.kv_head;
           sk = __ldg(p.k_scale + si);
-          sv = __ldg(p.v_scale + si);
+          sv = HYB ? 1.f : __ldg(p.v_scale + si);   // staged V is already scaled
         } else {
           record_error(p.err, kErrBadBlock);
         }
@@ -361,18 +373,20 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         if (lane == 0)
           tma_load_2d(smem + kOffK8 + s * kTile8 + bx * br * 128, &kmap, 0, y, &k_full[s]);
       }
-      // V tile j into staging j & 1 once the converters are done with j - 2
-      const int v2 = j & 1;
-      if (j >= 2 &&
-          !__all_sync(0xffffffffu, mbar_wait(&vs_empty[v2], ((j >> 1) - 1) & 1))) {
-        if (lane == 0) record_error(p.err, kErrTimeout);
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&vs_full[v2], n * br * 128);
-      for (int bx = 0; bx < n; ++bx) {
-        const int32_t y = __shfl_sync(0xffffffffu, y_cur, bx);
-        if (lane == 0)
-          tma_load_2d(smem + kOffVs8 + v2 * kTile8 + bx * br * 128, &vmap, 0, y, &vs_full[v2]);
+      if constexpr (!HYB) {
+        // V tile j into staging j & 1 once the converters are done with j - 2
+        const int v2 = j & 1;
+        if (j >= 2 &&
+            !__all_sync(0xffffffffu, mbar_wait(&vs_empty[v2], ((j >> 1) - 1) & 1))) {
+          if (lane == 0) record_error(p.err, kErrTimeout);
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&vs_full[v2], n * br * 128);
+        for (int bx = 0; bx < n; ++bx) {
+          const int32_t y = __shfl_sync(0xffffffffu, y_cur, bx);
+          if (lane == 0)
+            tma_load_2d(smem + kOffVs8 + v2 * kTile8 + bx * br * 128, &vmap, 0, y, &vs_full[v2]);
+        }
       }
       y_cur = y_next;
       sk_cur = sk_nxt;
@@ -622,9 +636,9 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       constexpr uint64_t kTileDesc = kTile >> 4;
       const uint64_t qd0 = smem_desc_sw128(smem_addr(smem + kOffQ), 16, 1024);
       const uint64_t kd0 =
-          smem_desc_sw128(smem_addr(smem + (NV ? kOffKn : FP8 ? kOffK8 : kOffK)), 16, 1024);
+          smem_desc_sw128(smem_addr(smem + (NV ? kOffKn : K8 ? kOffK8 : kOffK)), 16, 1024);
       const uint64_t vd0 =
-          smem_desc_sw128(smem_addr(smem + (NV ? kOffVn : FP8 ? kOffV8 : kOffV)), kHalf, 1024);
+          smem_desc_sw128(smem_addr(smem + (NV ? kOffVn : K8 ? kOffV8 : kOffV)), kHalf, 1024);
       auto qk = [&](int t, int j) {   // S_t = Q_t K_j^T
         const int s = j & (kKst - 1);
         // K arrives by TMA (async proxy, like the MMA): the mbarrier alone
@@ -633,7 +647,7 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
         if (NV) tc_fence_after();
         const uint64_t a0 = qd0 + t * kTileDesc;
         const uint32_t d = tmem + t * 128;
-        if constexpr (FP8) {
+        if constexpr (K8) {
           // S = (Q_hi + Q_lo) K^T: E4M3 K codes, four 32-byte k-steps per part
           // (Q_hi in the tile's first half, Q_lo in its second)
           const uint64_t b0 = kd0 + s * (kTile8 >> 4);
@@ -738,9 +752,9 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       // |q sq| in [128, 256)), becomes hi + lo, both E4M3 (about bf16
       // precision), written in place over the row: hi into the tile's first
       // 128-byte half, lo into its second (each the 128B-swizzled K-major
-      // layout of a 128 x 128 E4M3 tile).  NVFP4 pools and staged K/V: the
-      // row becomes f16 in place (largest |q sq| in [2^14, 2^15), the bf16
-      // layout).  1/sq goes into this row's scale.
+      // layout of a 128 x 128 E4M3 tile); likewise with E4M3 K over staged V.
+      // NVFP4 pools: the row becomes f16 in place (largest |q sq| in
+      // [2^14, 2^15), the bf16 layout).  1/sq goes into this row's scale.
       ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0));
       if (ok) {
         const uint32_t qt = smem_addr(smem + kOffQ + t * kTile);
@@ -909,8 +923,9 @@ __device__ __forceinline__ void prefill_tc_item(const CUtensorMap &qmap,
       // of other requests or never loaded): zero them before any PV reads
       // them.  Q tile 0 does it when it reaches that tile (its PV comes
       // first), otherwise Q tile 1.  (E4M3 and NVFP4 pools: the converters write
-      // those rows as zeros.)
-      if (!CONV && j == n_tiles - 1 && kspan - key0 < 128 && (t == 0 || nt0 < n_tiles)) {
+      // those rows as zeros; staged V over E4M3 K: they arrive as zeros.)
+      if (!CONV && !HYB && j == n_tiles - 1 && kspan - key0 < 128 &&
+          (t == 0 || nt0 < n_tiles)) {
         const int vvalid = kspan - key0;
         const int vs = j % kVst;
         if (!__all_sync(0xffffffffu, mbar_wait(&v_full[vs], (j / kVst) & 1))) {

@@ -8,16 +8,19 @@
 // quantised codes inside the prefill kernel therefore repeats the same
 // conversion once per item, on two converter warps that cannot keep up with
 // the tensor cores.  Staging converts each context block once per step
-// instead: every (block, KV head) tile a prefill request reads becomes bf16
-// in staging pools laid out like a bf16 pool (page "vLLM 优化
+// instead, into staging pools laid out like a bf16 pool (page "vLLM 优化
 // DeepSeek-V4.1-Flash：智能体吞吐提升 5 倍", section Kernels: the FP8 and NVFP4
-// KV formats).  K keeps its exact code values, e4m3(code) or e2m1(code) *
-// e4m3(micro scale) (at most 6 significant bits: exact in bf16), and its
-// block scale goes to a staging scale array, applied to the fp32 scores per
-// 16-key group as over the quantised pools (rounding K times its scale, even
-// to f16, moves the scores of peaked queries by up to 1e-2); V becomes its
-// value times the block scale, rounded once to nearest even.  The
-// tensor-core prefill then reads the staging pools with bf16 MMAs.
+// KV formats).
+//
+// NVFP4 pools stage K and V.  K keeps its exact code values,
+// e2m1(code) * e4m3(micro scale) (at most 6 significant bits: exact in
+// bf16), and its block scale goes to a staging scale array, applied to the
+// fp32 scores per 16-key group as over the quantised pools (rounding K times
+// its scale, even to f16, moves the scores of peaked queries by up to 1e-2).
+// E4M3 pools stage V alone: the prefill reads E4M3 K from the pool with FP8
+// MMAs, which need no conversion.  V becomes its value times the block
+// scale, rounded once to nearest even.  The tensor-core prefill then reads
+// the staged tiles with bf16 MMAs.
 //
 // Staged blocks of one request are consecutive: request r's block j is
 // staging block first_r + j.  Rows past the request's context are written as
@@ -42,8 +45,8 @@ __device__ __forceinline__ int staged_request(const StageParams &p, int sb) {
   return lo;
 }
 
-// One CTA per staging block: every KV head, K and V, 16-byte output chunks
-// (8 elements) in row order, so consecutive threads write consecutive
+// One CTA per staging block: every KV head, K (NVFP4) and V, 16-byte output
+// chunks (8 elements) in row order, so consecutive threads write consecutive
 // bytes.
 template <int FMT>
 __global__ void __launch_bounds__(256) stage_kv_kernel(const StageParams p) {
@@ -65,13 +68,15 @@ __global__ void __launch_bounds__(256) stage_kv_kernel(const StageParams p) {
   const int32_t blk = s_info[0];
   const int valid = s_info[1];
   const int bs = p.bs, hkv = p.hkv;
-  for (int h = threadIdx.x; h < hkv; h += blockDim.x)
-    p.k_stage_scale[static_cast<int64_t>(sb) * hkv + h] =
-        blk >= 0 ? __ldg(p.k_scale + static_cast<int64_t>(blk) * hkv + h) : 0.f;
+  constexpr bool V_ONLY = FMT == PKV_KV_FP8_E4M3;
+  if constexpr (!V_ONLY)
+    for (int h = threadIdx.x; h < hkv; h += blockDim.x)
+      p.k_stage_scale[static_cast<int64_t>(sb) * hkv + h] =
+          blk >= 0 ? __ldg(p.k_scale + static_cast<int64_t>(blk) * hkv + h) : 0.f;
   const int per_kv = hkv * bs * 16;   // chunks of one of K / V
-  for (int c = threadIdx.x; c < 2 * per_kv; c += blockDim.x) {
-    const bool is_v = c >= per_kv;
-    const int cc = is_v ? c - per_kv : c;
+  for (int c = threadIdx.x; c < (V_ONLY ? 1 : 2) * per_kv; c += blockDim.x) {
+    const bool is_v = V_ONLY || c >= per_kv;
+    const int cc = is_v && !V_ONLY ? c - per_kv : c;
     const int q = cc & 15;              // chunk: elements 8q .. 8q + 7
     const int r = (cc >> 4) % bs;       // row in the block
     const int h = (cc >> 4) / bs;       // KV head

@@ -113,6 +113,7 @@ SWEEP = [
     ("fp8_prefill_gqa4", 32, 8, 16, [1, 40, 3, 130], [17, 300, 2000, 130], "fp8"),
     ("fp8_prefill_gqa8_bs64", 64, 8, 64, [1, 70, 5], [5000, 700, 65], "fp8"),
     ("fp8_prefill_gqa3", 6, 2, 64, [10, 1, 33], [100, 64, 1500], "fp8"),
+    ("fp8_prefill_bs128", 16, 4, 128, [200, 2], [1300, 300], "fp8"),
     ("gqa256_chunks", 256, 1, 16, [1, 2, 9], [40, 50, 300], "bf16"),
     # NVFP4 pools (decode kernel; prefill rows as 8-row chunks)
     ("nvfp4_gqa8_bs64", 64, 8, 64, [1, 1, 1, 1], [1, 63, 65, 5000], "nvfp4"),
@@ -135,6 +136,7 @@ SWEEP = [
     ("split_gqa3", 24, 8, 16, [300, 1], [2300, 900], "bf16"),
     ("split_bs256", 8, 2, 256, [33, 2], [3000, 700], "bf16"),
     ("split_fp8", 32, 8, 64, [40], [6000], "fp8"),
+    ("split_fp8_bs256", 8, 2, 256, [33, 2], [3000, 700], "fp8"),
     ("split_nvfp4", 32, 8, 16, [40, 1], [6000, 3000], "nvfp4"),
 ]
 
