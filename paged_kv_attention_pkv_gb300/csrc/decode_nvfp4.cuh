@@ -82,10 +82,16 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
   uint8_t *ring = smem + warp * S * kDecStageBytesNvfp4;
   uint64_t *full = bars + warp * S;
   const int32_t *bt = p.block_tables + static_cast<int64_t>(it.seq) * p.bt_stride;
-  const int gs = p.bs < kNvfp4Group ? p.bs : kNvfp4Group;   // rows per group
+  // block sizes are powers of two: keys map to blocks and row groups by shifts
+  const int bs_sh = 31 - __clz(p.bs);
+  const int gs_sh = bs_sh < 6 ? bs_sh : 6;                  // kNvfp4Group = 64 rows
+  const int gs = 1 << gs_sh;                                // rows per group
   const int br = gs < KS ? gs : KS;                         // keys per copy
   const int tile_rows = p.bs / 8 * 9;                       // 64-byte rows per tile
   const int group_rows = gs / 8 * 9;
+  // a stage (KS keys from a multiple of KS, in one run of a shard) lies in
+  // one block when blocks hold at least KS keys
+  const bool one_block = p.bs >= KS;
 
   // Fill ring slot i % S with stage i (lane 0 only): per run of br keys
   // inside one group, the code rows by TMA and the micro scales by a bulk
@@ -102,16 +108,16 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
     for (int r = 0; r < KS; r += br) {
       if (key0 + r >= ke) break;
       const int gk = gkey0 + r;
-      const int32_t blk = __ldg(bt + gk / p.bs);
+      const int32_t blk = __ldg(bt + (gk >> bs_sh));
       int32_t row = p.rows_total;   // outside the map: TMA fills zeros
       int64_t sbyte = 0;            // (a flagged bad block reads scales from offset 0)
       if (blk < 0 || blk >= p.num_blocks) {
         record_error(p.err, kErrBadBlock);
       } else {
-        const int in_blk = gk % p.bs;
-        const int grp0 = (blk * p.hkv + it.kv_head) * tile_rows + in_blk / gs * group_rows;
-        row = grp0 + in_blk % gs;
-        sbyte = static_cast<int64_t>(grp0 + gs) * 64 + (in_blk % gs) * 8;
+        const int in_blk = gk & (p.bs - 1);
+        const int grp0 = (blk * p.hkv + it.kv_head) * tile_rows + (in_blk >> gs_sh) * group_rows;
+        row = grp0 + (in_blk & (gs - 1));
+        sbyte = static_cast<int64_t>(grp0 + gs) * 64 + (in_blk & (gs - 1)) * 8;
       }
       tma_load_2d(st + r * 64, &kmap, 0, row, &full[slot]);
       tma_load_2d(st + kNvCodeBytes + r * 64, &vmap, 0, row, &full[slot]);
@@ -186,16 +192,31 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
 #pragma unroll
     for (int sub = 0; sub < kSubs; ++sub) {
       const int k16 = kb + (warp + i * NW) * KS + 16 * sub;
-      blk[sub] = (i < my_n && k16 < ke) ? __ldg(bt + global_key(p, k16) / p.bs) : -1;
+      if (sub > 0 && one_block)
+        blk[sub] = k16 < ke ? blk[0] : -1;
+      else
+        blk[sub] = (i < my_n && k16 < ke) ? __ldg(bt + (global_key(p, k16) >> bs_sh)) : -1;
     }
   };
   int32_t blk_next[kSubs];
   stage_blocks(0, blk_next);
 
   // rows this thread reads: QK rows nv_key(g) and nv_key(g) + 8; V^T rows for
-  // MMA keys 2t, 2t+1 (A/B) and 2t+8, 2t+9 (C/D)
+  // MMA keys 2t, 2t+1 (A/B) and 2t+8, 2t+9 (C/D).  Offsets in sub-tile 0;
+  // sub-tile sub adds 1024 sub to the code offsets (the swizzle acts on
+  // address bits 4-8 only) and 128 sub to the micro-scale offsets.
   const int qk_row = nv_key(g);
   const int pv_a = nv_key(2 * t), pv_b = nv_key(2 * t + 1);
+  const uint32_t o_ka = swz64(qk_row * 64 + 16 * t), o_kb = swz64((qk_row + 8) * 64 + 16 * t);
+  const uint32_t o_ksa = qk_row * 8 + 2 * t, o_ksb = o_ksa + 64;
+  const uint32_t o_va = swz64(pv_a * 64 + 8 * g), o_vb = swz64(pv_b * 64 + 8 * g);
+  const uint32_t o_vc = swz64((pv_a + 8) * 64 + 8 * g), o_vd = swz64((pv_b + 8) * 64 + 8 * g);
+  const uint32_t o_vsa = pv_a * 8 + g, o_vsb = pv_b * 8 + g;
+  // smallest position of the item's rows: a stage whose keys all lie at or
+  // below it and before ke needs no mask
+  const int pos_lo = it.hist + it.row0 / group;
+  // running maxima as used for P (m - kPExp, 0 before any key)
+  float mp0 = -kPExp, mp1 = -kPExp;
 
   int consumed = 0;
   bool timed_out = false;
@@ -206,7 +227,10 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
     for (int sub = 0; sub < kSubs; ++sub) {
       const int32_t blk = blk_next[sub];
       sk_sub[sub] = sv_sub[sub] = 0.f;
-      if (blk >= 0 && blk < p.num_blocks) {
+      if (sub > 0 && one_block) {   // the same block's scales (sub-tiles past ke: unused)
+        sk_sub[sub] = sk_sub[0];
+        sv_sub[sub] = sv_sub[0];
+      } else if (blk >= 0 && blk < p.num_blocks) {
         const int64_t si = static_cast<int64_t>(blk) * p.hkv + it.kv_head;
         sk_sub[sub] = __ldg(p.k_scale + si);
         sv_sub[sub] = __ldg(p.v_scale + si);
@@ -231,12 +255,11 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
     for (int sub = 0; sub < kSubs; ++sub) {
       s[sub][0] = s[sub][1] = s[sub][2] = s[sub][3] = 0.f;
       if (key0 + 16 * sub >= ke) continue;
-      const int rA = 16 * sub + qk_row, rB = rA + 8;
-      const uint4 x = lds128(kc + swz64(rA * 64 + 16 * t));
-      const uint4 y = lds128(kc + swz64(rB * 64 + 16 * t));
+      const uint4 x = lds128(kc + 1024 * sub + o_ka);
+      const uint4 y = lds128(kc + 1024 * sub + o_kb);
       // micro scales of micro blocks 2t, 2t+1 of both rows, as f16 pairs
-      const uint32_t sa = e4m3x2lo_to_f16x2(lds16(ksc + rA * 8 + 2 * t));
-      const uint32_t sb = e4m3x2lo_to_f16x2(lds16(ksc + rB * 8 + 2 * t));
+      const uint32_t sa = e4m3x2lo_to_f16x2(lds16(ksc + 128 * sub + o_ksa));
+      const uint32_t sb = e4m3x2lo_to_f16x2(lds16(ksc + 128 * sub + o_ksb));
       const uint32_t sa0 = __byte_perm(sa, 0, 0x1010), sa1 = __byte_perm(sa, 0, 0x3232);
       const uint32_t sb0 = __byte_perm(sb, 0, 0x1010), sb1 = __byte_perm(sb, 0, 0x3232);
       const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
@@ -256,19 +279,27 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
     // ---- scale, mask (validity on item-local keys, causality on global
     // positions), online softmax per column over the whole stage
     float tm0 = -CUDART_INF_F, tm1 = -CUDART_INF_F;
+    const bool unmasked = !MASK && key0 + KS <= ke && gkey0 + KS - 1 <= pos_lo;
 #pragma unroll
     for (int sub = 0; sub < kSubs; ++sub) {
       const float sc0 = p.scale_log2 * sk_sub[sub] * inv_sq0;
       const float sc1 = p.scale_log2 * sk_sub[sub] * inv_sq1;
-      const int kr0 = key0 + 16 * sub + qk_row, kr1 = kr0 + 8;
-      const int gr0 = gkey0 + 16 * sub + qk_row, gr1 = gr0 + 8;
-      s[sub][0] = (kr0 < ke && gr0 <= pos0) ? s[sub][0] * sc0 : -CUDART_INF_F;
-      s[sub][1] = (kr0 < ke && gr0 <= pos1) ? s[sub][1] * sc1 : -CUDART_INF_F;
-      s[sub][2] = (kr1 < ke && gr1 <= pos0) ? s[sub][2] * sc0 : -CUDART_INF_F;
-      s[sub][3] = (kr1 < ke && gr1 <= pos1) ? s[sub][3] * sc1 : -CUDART_INF_F;
-      if constexpr (MASK) {   // masked shard view: keys another shard owns
-        if (!shard_owns(p, gr0)) s[sub][0] = s[sub][1] = -CUDART_INF_F;
-        if (!shard_owns(p, gr1)) s[sub][2] = s[sub][3] = -CUDART_INF_F;
+      if (unmasked) {
+        s[sub][0] *= sc0;
+        s[sub][1] *= sc1;
+        s[sub][2] *= sc0;
+        s[sub][3] *= sc1;
+      } else {
+        const int kr0 = key0 + 16 * sub + qk_row, kr1 = kr0 + 8;
+        const int gr0 = gkey0 + 16 * sub + qk_row, gr1 = gr0 + 8;
+        s[sub][0] = (kr0 < ke && gr0 <= pos0) ? s[sub][0] * sc0 : -CUDART_INF_F;
+        s[sub][1] = (kr0 < ke && gr0 <= pos1) ? s[sub][1] * sc1 : -CUDART_INF_F;
+        s[sub][2] = (kr1 < ke && gr1 <= pos0) ? s[sub][2] * sc0 : -CUDART_INF_F;
+        s[sub][3] = (kr1 < ke && gr1 <= pos1) ? s[sub][3] * sc1 : -CUDART_INF_F;
+        if constexpr (MASK) {   // masked shard view: keys another shard owns
+          if (!shard_owns(p, gr0)) s[sub][0] = s[sub][1] = -CUDART_INF_F;
+          if (!shard_owns(p, gr1)) s[sub][2] = s[sub][3] = -CUDART_INF_F;
+        }
       }
       tm0 = fmaxf(tm0, fmaxf(s[sub][0], s[sub][2]));
       tm1 = fmaxf(tm1, fmaxf(s[sub][1], s[sub][3]));
@@ -278,28 +309,33 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
       tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
       tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
     }
-    const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
-    const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
-    const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-    const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-    const float mp0 = mu0 - kPExp, mp1 = mu1 - kPExp;
-    m0 = mn0;
-    m1 = mn1;
-    l0 *= al0;
-    l1 *= al1;
+    // rescale only when a column's maximum grew (otherwise every factor is
+    // exactly 1)
+    if (__any_sync(0xffffffffu, tm0 > m0 || tm1 > m1)) {
+      const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
+      const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+      const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+      const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
+      mp0 = mu0 - kPExp;
+      mp1 = mu1 - kPExp;
+      m0 = mn0;
+      m1 = mn1;
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      acc[mt][0] *= al0;
-      acc[mt][1] *= al1;
-      acc[mt][2] *= al0;
-      acc[mt][3] *= al1;
+      for (int mt = 0; mt < 8; ++mt) {
+        acc[mt][0] *= al0;
+        acc[mt][1] *= al1;
+        acc[mt][2] *= al0;
+        acc[mt][3] *= al1;
+      }
     }
 #pragma unroll
     for (int sub = 0; sub < kSubs; ++sub) {
       const int k16 = key0 + 16 * sub;
       if (k16 >= ke) break;
-      const float p0 = exp2f(s[sub][0] - mp0), p1 = exp2f(s[sub][1] - mp1);
-      const float p2 = exp2f(s[sub][2] - mp0), p3 = exp2f(s[sub][3] - mp1);
+      const float p0 = ex2(s[sub][0] - mp0), p1 = ex2(s[sub][1] - mp1);
+      const float p2 = ex2(s[sub][2] - mp0), p3 = ex2(s[sub][3] - mp1);
       l0 += p0 + p2;
       l1 += p1 + p3;
       // ---- P^T as the B operand (f16, V's block scale folded in)
@@ -308,14 +344,14 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
       const uint32_t b1 = movmatrix_trans(pack_f16(p2 * pv_scale, p3 * pv_scale));
       // ---- O^T += V^T P^T: this thread's micro block g of rows A, B, C, D
       const int rA = 16 * sub + pv_a, rB = 16 * sub + pv_b, rC = rA + 8, rD = rB + 8;
-      const uint2 uA = lds64(vc + swz64(rA * 64 + 8 * g));
-      const uint2 uB = lds64(vc + swz64(rB * 64 + 8 * g));
-      const uint2 uC = lds64(vc + swz64(rC * 64 + 8 * g));
-      const uint2 uD = lds64(vc + swz64(rD * 64 + 8 * g));
-      const uint32_t sab =
-          e4m3x2lo_to_f16x2(lds8(vsc + rA * 8 + g) | (lds8(vsc + rB * 8 + g) << 8));
+      const uint2 uA = lds64(vc + 1024 * sub + o_va);
+      const uint2 uB = lds64(vc + 1024 * sub + o_vb);
+      const uint2 uC = lds64(vc + 1024 * sub + o_vc);
+      const uint2 uD = lds64(vc + 1024 * sub + o_vd);
+      const uint32_t vs = vsc + 128 * sub;
+      const uint32_t sab = e4m3x2lo_to_f16x2(lds8(vs + o_vsa) | (lds8(vs + o_vsb) << 8));
       const uint32_t scd =
-          e4m3x2lo_to_f16x2(lds8(vsc + rC * 8 + g) | (lds8(vsc + rD * 8 + g) << 8));
+          e4m3x2lo_to_f16x2(lds8(vs + o_vsa + 64) | (lds8(vs + o_vsb + 64) << 8));
       auto pv4 = [&](auto masked) {
         uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
         if (decltype(masked)::value) {

@@ -27,6 +27,14 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // 2^e as a float, exactly, for integer e in [-126, 127].
 __device__ __forceinline__ float exp2_int(int e) { return __int_as_float((e + 127) << 23); }
 
+// 2^x by the hardware approximation (relative error about 2^-22; results
+// below 2^-126 flush to zero, 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void record_error(int32_t *err, int32_t bit) {
   if (err != nullptr) atomicOr(err, bit);
 }

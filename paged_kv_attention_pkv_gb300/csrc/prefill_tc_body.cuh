@@ -61,12 +61,6 @@ constexpr uint32_t kIdescPV16 = idesc_f16(128, 128, 0, 1);
 constexpr uint32_t kIdescQK16 = idesc_f16(128, 128, 0, 0);
 constexpr float kRescaleThreshold = 8.f;          // log2 units
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
