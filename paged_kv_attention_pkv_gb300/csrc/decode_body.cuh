@@ -20,18 +20,21 @@ struct DecTile {
   static_assert(kKBytes * 2 == kDecStageBytes, "stage layout");
 };
 
+// log2 of the block size (a power of two).
+__device__ __forceinline__ int bs_shift(const DecodeParams &p) { return 31 - __clz(p.bs); }
+
 // Row of the pool maps holding key `key` of KV head `kvh` of a request, or
 // rows_total (entirely outside the map: TMA fills zeros) for a bad block id.
 __device__ __forceinline__ int32_t pool_row(const int32_t *bt, int32_t key,
                                             int32_t kvh, const DecodeParams &p,
                                             int32_t *blk_out) {
-  const int32_t blk = __ldg(bt + key / p.bs);
+  const int32_t blk = __ldg(bt + (key >> bs_shift(p)));
   *blk_out = blk;
   if (blk < 0 || blk >= p.num_blocks) {
     record_error(p.err, kErrBadBlock);
     return p.rows_total;
   }
-  return (blk * p.hkv + kvh) * p.bs + key % p.bs;
+  return (blk * p.hkv + kvh) * p.bs + (key & (p.bs - 1));
 }
 
 // E4M3 pools: key of MMA key slot r (0..15) of a 16-key sub-tile.  The V^T
@@ -307,13 +310,25 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
   // E4M3 pools: the per-block scales of a stage's sub-tiles are loaded
   // before its wait (block ids one stage ahead), so their latency hides
   // behind the copy instead of sitting between the MMAs and the softmax
+  // (a stage, KS keys from a multiple of KS in one run of a shard, lies in
+  // one block when blocks hold at least KS keys)
+  const bool one_block = p.bs >= KS;
+  const int bs_sh = bs_shift(p);
   auto stage_blocks = [&](int i, int32_t (&blk)[Tile::kSubs]) {
 #pragma unroll
     for (int sub = 0; sub < Tile::kSubs; ++sub) {
       const int k16 = kb + (warp + i * kDecWarps) * KS + 16 * sub;
-      blk[sub] = (FP8 && i < my_n && k16 < ke) ? __ldg(bt + global_key(p, k16) / p.bs) : -1;
+      if (sub > 0 && one_block)
+        blk[sub] = k16 < ke ? blk[0] : -1;
+      else
+        blk[sub] = (FP8 && i < my_n && k16 < ke) ? __ldg(bt + (global_key(p, k16) >> bs_sh)) : -1;
     }
   };
+  // smallest position of the item's rows: a stage whose keys all lie at or
+  // below it and before ke needs no mask
+  const int pos_lo = it.hist + it.row0 / p.group;
+  // running maxima as used for P (E4M3: m - kPExp; 0 before any key)
+  float mp0 = FP8 ? -kPExp : 0.f, mp1 = mp0;
   int32_t blk_next[Tile::kSubs];
   stage_blocks(0, blk_next);
 
@@ -328,7 +343,10 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       for (int sub = 0; sub < Tile::kSubs; ++sub) {
         const int32_t blk = blk_next[sub];
         sk_sub[sub] = sv_sub[sub] = 0.f;
-        if (blk >= 0 && blk < p.num_blocks) {
+        if (sub > 0 && one_block) {   // the same block's scales (sub-tiles past ke: unused)
+          sk_sub[sub] = sk_sub[0];
+          sv_sub[sub] = sv_sub[0];
+        } else if (blk >= 0 && blk < p.num_blocks) {
           const int64_t si = static_cast<int64_t>(blk) * p.hkv + it.kv_head;
           sk_sub[sub] = __ldg(p.k_scale + si);
           sv_sub[sub] = __ldg(p.v_scale + si);
@@ -379,6 +397,7 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
     // ---- scale, mask (validity on item-local keys, causality on global
     // positions), online softmax per column over the stage
     float tm0 = -CUDART_INF_F, tm1 = -CUDART_INF_F;
+    const bool unmasked = !MASK && key0 + KS <= ke && gkey0 + KS - 1 <= pos_lo;
 #pragma unroll
     for (int sub = 0; sub < Tile::kSubs; ++sub) {
       float sc0 = p.scale_log2, sc1 = p.scale_log2;
@@ -386,15 +405,22 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
         sc0 *= sk_sub[sub] * inv_sq0;
         sc1 *= sk_sub[sub] * inv_sq1;
       }
-      const int kr0 = key0 + 16 * sub + krow0, kr1 = key0 + 16 * sub + krow1;
-      const int gr0 = gkey0 + 16 * sub + krow0, gr1 = gkey0 + 16 * sub + krow1;
-      s[sub][0] = (kr0 < ke && gr0 <= pos0) ? s[sub][0] * sc0 : -CUDART_INF_F;
-      s[sub][1] = (kr0 < ke && gr0 <= pos1) ? s[sub][1] * sc1 : -CUDART_INF_F;
-      s[sub][2] = (kr1 < ke && gr1 <= pos0) ? s[sub][2] * sc0 : -CUDART_INF_F;
-      s[sub][3] = (kr1 < ke && gr1 <= pos1) ? s[sub][3] * sc1 : -CUDART_INF_F;
-      if constexpr (MASK) {   // masked shard view: keys another shard owns
-        if (!shard_owns(p, gr0)) s[sub][0] = s[sub][1] = -CUDART_INF_F;
-        if (!shard_owns(p, gr1)) s[sub][2] = s[sub][3] = -CUDART_INF_F;
+      if (unmasked) {
+        s[sub][0] *= sc0;
+        s[sub][1] *= sc1;
+        s[sub][2] *= sc0;
+        s[sub][3] *= sc1;
+      } else {
+        const int kr0 = key0 + 16 * sub + krow0, kr1 = key0 + 16 * sub + krow1;
+        const int gr0 = gkey0 + 16 * sub + krow0, gr1 = gkey0 + 16 * sub + krow1;
+        s[sub][0] = (kr0 < ke && gr0 <= pos0) ? s[sub][0] * sc0 : -CUDART_INF_F;
+        s[sub][1] = (kr0 < ke && gr0 <= pos1) ? s[sub][1] * sc1 : -CUDART_INF_F;
+        s[sub][2] = (kr1 < ke && gr1 <= pos0) ? s[sub][2] * sc0 : -CUDART_INF_F;
+        s[sub][3] = (kr1 < ke && gr1 <= pos1) ? s[sub][3] * sc1 : -CUDART_INF_F;
+        if constexpr (MASK) {   // masked shard view: keys another shard owns
+          if (!shard_owns(p, gr0)) s[sub][0] = s[sub][1] = -CUDART_INF_F;
+          if (!shard_owns(p, gr1)) s[sub][2] = s[sub][3] = -CUDART_INF_F;
+        }
       }
       tm0 = fmaxf(tm0, fmaxf(s[sub][0], s[sub][2]));
       tm1 = fmaxf(tm1, fmaxf(s[sub][1], s[sub][3]));
@@ -404,28 +430,33 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
       tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
     }
-    const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
-    const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
-    const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
-    const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-    const float mp0 = FP8 ? mu0 - kPExp : mu0, mp1 = FP8 ? mu1 - kPExp : mu1;
-    m0 = mn0;
-    m1 = mn1;
-    l0 *= al0;
-    l1 *= al1;
+    // rescale only when a column's maximum grew (otherwise every factor is
+    // exactly 1)
+    if (__any_sync(0xffffffffu, tm0 > m0 || tm1 > m1)) {
+      const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
+      const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+      const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+      const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
+      mp0 = FP8 ? mu0 - kPExp : mu0;
+      mp1 = FP8 ? mu1 - kPExp : mu1;
+      m0 = mn0;
+      m1 = mn1;
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      acc[mt][0] *= al0;
-      acc[mt][1] *= al1;
-      acc[mt][2] *= al0;
-      acc[mt][3] *= al1;
+      for (int mt = 0; mt < 8; ++mt) {
+        acc[mt][0] *= al0;
+        acc[mt][1] *= al1;
+        acc[mt][2] *= al0;
+        acc[mt][3] *= al1;
+      }
     }
 #pragma unroll
     for (int sub = 0; sub < Tile::kSubs; ++sub) {
       const int k16 = key0 + 16 * sub;
       if (k16 >= ke) break;
-      const float p0 = exp2f(s[sub][0] - mp0), p1 = exp2f(s[sub][1] - mp1);
-      const float p2 = exp2f(s[sub][2] - mp0), p3 = exp2f(s[sub][3] - mp1);
+      const float p0 = ex2(s[sub][0] - mp0), p1 = ex2(s[sub][1] - mp1);
+      const float p2 = ex2(s[sub][2] - mp0), p3 = ex2(s[sub][3] - mp1);
       l0 += p0 + p2;
       l1 += p1 + p3;
       const float pv_scale = FP8 ? sv_sub[sub] : 1.f;
