@@ -425,14 +425,15 @@ __device__ __forceinline__ void decode_item(const CUtensorMap &kmap, const CUten
       tm0 = fmaxf(tm0, fmaxf(s[sub][0], s[sub][2]));
       tm1 = fmaxf(tm1, fmaxf(s[sub][1], s[sub][3]));
     }
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
-      tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
-    }
-    // rescale only when a column's maximum grew (otherwise every factor is
-    // exactly 1)
+    // a column's maximum grows only if one of its scores lies above it: only
+    // then reduce the stage maxima over the column's threads and rescale
+    // (otherwise every factor is exactly 1)
     if (__any_sync(0xffffffffu, tm0 > m0 || tm1 > m1)) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
+        tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
+      }
       const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
       const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
       const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;

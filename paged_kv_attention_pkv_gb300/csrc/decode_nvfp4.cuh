@@ -304,14 +304,15 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
       tm0 = fmaxf(tm0, fmaxf(s[sub][0], s[sub][2]));
       tm1 = fmaxf(tm1, fmaxf(s[sub][1], s[sub][3]));
     }
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
-      tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
-    }
-    // rescale only when a column's maximum grew (otherwise every factor is
-    // exactly 1)
+    // a column's maximum grows only if one of its scores lies above it: only
+    // then reduce the stage maxima over the column's threads and rescale
+    // (otherwise every factor is exactly 1)
     if (__any_sync(0xffffffffu, tm0 > m0 || tm1 > m1)) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, o));
+        tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, o));
+      }
       const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
       const float mu0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
       const float mu1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
@@ -349,43 +350,30 @@ __device__ __forceinline__ void decode_item_nvfp4(const CUtensorMap &kmap,
       const uint2 uC = lds64(vc + 1024 * sub + o_vc);
       const uint2 uD = lds64(vc + 1024 * sub + o_vd);
       const uint32_t vs = vsc + 128 * sub;
-      const uint32_t sab = e4m3x2lo_to_f16x2(lds8(vs + o_vsa) | (lds8(vs + o_vsb) << 8));
-      const uint32_t scd =
-          e4m3x2lo_to_f16x2(lds8(vs + o_vsa + 64) | (lds8(vs + o_vsb + 64) << 8));
-      auto pv4 = [&](auto masked) {
-        uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
-        if (decltype(masked)::value) {
-          mlo = (key0 + rA < ke ? 0x0000FFFFu : 0u) | (key0 + rB < ke ? 0xFFFF0000u : 0u);
-          mhi = (key0 + rC < ke ? 0x0000FFFFu : 0u) | (key0 + rD < ke ? 0xFFFF0000u : 0u);
-        }
+      uint32_t sab = e4m3x2lo_to_f16x2(lds8(vs + o_vsa) | (lds8(vs + o_vsb) << 8));
+      uint32_t scd = e4m3x2lo_to_f16x2(lds8(vs + o_vsa + 64) | (lds8(vs + o_vsb + 64) << 8));
+      if (k16 + 16 > ke) {
+        // the item's last, partial sub-tile: keys past ke get micro scale 0
+        // (their rows may hold stale bytes; codes are always finite, a stale
+        // micro scale may not be, and P is 0 there)
+        sab &= (key0 + rA < ke ? 0x0000FFFFu : 0u) | (key0 + rB < ke ? 0xFFFF0000u : 0u);
+        scd &= (key0 + rC < ke ? 0x0000FFFFu : 0u) | (key0 + rD < ke ? 0xFFFF0000u : 0u);
+      }
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
-          const uint32_t a = w ? uA.y : uA.x, b = w ? uB.y : uB.x;
-          const uint32_t c = w ? uC.y : uC.x, d = w ? uD.y : uD.x;
-          // pair the two keys' nibbles per head dim: even dims, odd dims
-          uint32_t ae[4], ao[4], ce[4], co[4];
-          e2m1x8_to_f16x2((a & 0x0F0F0F0Fu) | ((b << 4) & 0xF0F0F0F0u), ae);
-          e2m1x8_to_f16x2(((a >> 4) & 0x0F0F0F0Fu) | (b & 0xF0F0F0F0u), ao);
-          e2m1x8_to_f16x2((c & 0x0F0F0F0Fu) | ((d << 4) & 0xF0F0F0F0u), ce);
-          e2m1x8_to_f16x2(((c >> 4) & 0x0F0F0F0Fu) | (d & 0xF0F0F0F0u), co);
+      for (int w = 0; w < 2; ++w) {
+        const uint32_t a = w ? uA.y : uA.x, b = w ? uB.y : uB.x;
+        const uint32_t c = w ? uC.y : uC.x, d = w ? uD.y : uD.x;
+        // pair the two keys' nibbles per head dim: even dims, odd dims
+        uint32_t ae[4], ao[4], ce[4], co[4];
+        e2m1x8_to_f16x2((a & 0x0F0F0F0Fu) | ((b << 4) & 0xF0F0F0F0u), ae);
+        e2m1x8_to_f16x2(((a >> 4) & 0x0F0F0F0Fu) | (b & 0xF0F0F0F0u), ao);
+        e2m1x8_to_f16x2((c & 0x0F0F0F0Fu) | ((d << 4) & 0xF0F0F0F0u), ce);
+        e2m1x8_to_f16x2(((c >> 4) & 0x0F0F0F0Fu) | (d & 0xF0F0F0F0u), co);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t a0 = hmul2(ae[j], sab), a1 = hmul2(ao[j], sab);
-            uint32_t a2 = hmul2(ce[j], scd), a3 = hmul2(co[j], scd);
-            if (decltype(masked)::value) {
-              a0 &= mlo;
-              a1 &= mlo;
-              a2 &= mhi;
-              a3 &= mhi;
-            }
-            mma_f16(acc[4 * w + j], a0, a1, a2, a3, b0, b1);
-          }
-        }
-      };
-      if (k16 + 16 > ke)
-        pv4(std::true_type{});
-      else
-        pv4(std::false_type{});
+        for (int j = 0; j < 4; ++j)
+          mma_f16(acc[4 * w + j], hmul2(ae[j], sab), hmul2(ao[j], sab), hmul2(ce[j], scd),
+                  hmul2(co[j], scd), b0, b1);
+      }
     }
     __syncwarp();
     ++consumed;
