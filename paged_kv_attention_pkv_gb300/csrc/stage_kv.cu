@@ -45,9 +45,10 @@ __device__ __forceinline__ int staged_request(const StageParams &p, int sb) {
   return lo;
 }
 
-// One CTA per staging block: every KV head, K (NVFP4) and V, 16-byte output
-// chunks (8 elements) in row order, so consecutive threads write consecutive
-// bytes.
+// One CTA per staging block: every KV head, K (NVFP4) and V.  A thread
+// takes one 16-byte load of codes per unit (16 E4M3 or 32 E2M1 elements)
+// and writes its 2 or 4 16-byte bf16 chunks; units run in row order, so a
+// warp reads and writes contiguous spans.
 template <int FMT>
 __global__ void __launch_bounds__(256) stage_kv_kernel(const StageParams p) {
   const int sb = blockIdx.x;
@@ -68,28 +69,34 @@ __global__ void __launch_bounds__(256) stage_kv_kernel(const StageParams p) {
   const int32_t blk = s_info[0];
   const int valid = s_info[1];
   const int bs = p.bs, hkv = p.hkv;
+  const int bs_sh = 31 - __clz(bs);   // block sizes are powers of two
   constexpr bool V_ONLY = FMT == PKV_KV_FP8_E4M3;
+  constexpr int kUnitSh = V_ONLY ? 3 : 2;        // units per 128-element row: 8 or 4
+  constexpr int kOut = (kHeadDim >> kUnitSh) / 8;   // 16-byte bf16 chunks per unit
   if constexpr (!V_ONLY)
     for (int h = threadIdx.x; h < hkv; h += blockDim.x)
       p.k_stage_scale[static_cast<int64_t>(sb) * hkv + h] =
           blk >= 0 ? __ldg(p.k_scale + static_cast<int64_t>(blk) * hkv + h) : 0.f;
-  const int per_kv = hkv * bs * 16;   // chunks of one of K / V
+  const int per_kv = (hkv << bs_sh) << kUnitSh;   // units of one of K / V
   for (int c = threadIdx.x; c < (V_ONLY ? 1 : 2) * per_kv; c += blockDim.x) {
     const bool is_v = V_ONLY || c >= per_kv;
     const int cc = is_v && !V_ONLY ? c - per_kv : c;
-    const int q = cc & 15;              // chunk: elements 8q .. 8q + 7
-    const int r = (cc >> 4) % bs;       // row in the block
-    const int h = (cc >> 4) / bs;       // KV head
-    uint32_t o[4] = {0u, 0u, 0u, 0u};
+    const int q = cc & ((1 << kUnitSh) - 1);    // unit of the row
+    const int r = (cc >> kUnitSh) & (bs - 1);   // row in the block
+    const int h = (cc >> kUnitSh) >> bs_sh;     // KV head
+    uint32_t o[4 * kOut];
+#pragma unroll
+    for (int k = 0; k < 4 * kOut; ++k) o[k] = 0u;
     if (blk >= 0 && r < valid) {
       const int64_t tile = static_cast<int64_t>(blk) * hkv + h;
       const float sc = is_v ? __ldg(p.v_scale + tile) : 1.f;   // K: exact codes
       const uint8_t *pool = is_v ? p.v_pool : p.k_pool;
       if constexpr (FMT == PKV_KV_FP8_E4M3) {
-        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(pool + (tile * bs + r) * 128) + q);
-        const uint32_t ww[2] = {w.x, w.y};
+        // elements 16q .. 16q + 15
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(pool + ((tile << bs_sh) + r) * 128) + q);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 4; ++u) {
           const float2 a = e4m3x2_to_f32(ww[u] & 0xFFFFu);
           const float2 b = e4m3x2_to_f32(ww[u] >> 16);
           o[2 * u] = pack_bf16(a.x * sc, a.y * sc);
@@ -97,25 +104,37 @@ __global__ void __launch_bounds__(256) stage_kv_kernel(const StageParams p) {
         }
       } else {
         // NVFP4 tile: rows in groups of min(bs, 64), a group's code rows
-        // (64 bytes) then its micro-scale rows (8 bytes)
-        const int gs = bs < kNvfp4Group ? bs : kNvfp4Group;
-        const uint8_t *grp = pool + tile * bs * kNvfp4RowBytes + (r / gs) * gs * kNvfp4RowBytes;
-        const uint32_t codes =
-            __ldg(reinterpret_cast<const uint32_t *>(grp + (r % gs) * 64) + q);
-        const float mu = e4m3x2_to_f32(grp[gs * 64 + (r % gs) * 8 + (q >> 1)]).x;
-        const float ms = mu * sc;
-        uint32_t f[4];
-        e2m1x8_to_f16x2(codes, f);
+        // (64 bytes) then its micro-scale rows (8 bytes); elements
+        // 32q .. 32q + 31 are micro blocks 2q and 2q + 1
+        const int gs_sh = bs_sh < 6 ? bs_sh : 6;
+        const int gs = 1 << gs_sh;
+        const int rg = r & (gs - 1);
+        const uint8_t *grp = pool + ((tile << bs_sh) + ((r >> gs_sh) << gs_sh)) * kNvfp4RowBytes;
+        const uint4 codes = __ldg(reinterpret_cast<const uint4 *>(grp + rg * 64) + q);
+        const uint16_t mus =
+            __ldg(reinterpret_cast<const uint16_t *>(grp + gs * 64 + rg * 8) + q);
+        const float2 mu = e4m3x2_to_f32(mus);
+        const float ms[2] = {mu.x * sc, mu.y * sc};
+        const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&f[u]));
-          o[u] = pack_bf16(v.x * ms, v.y * ms);
+        for (int u = 0; u < 4; ++u) {   // 8 elements of micro block 2q + u / 2
+          uint32_t f[4];
+          e2m1x8_to_f16x2(cw[u], f);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&f[k]));
+            o[4 * u + k] = pack_bf16(v.x * ms[u >> 1], v.y * ms[u >> 1]);
+          }
         }
       }
     }
-    __nv_bfloat16 *dst = (is_v ? p.v_stage : p.k_stage) +
-                         ((static_cast<int64_t>(sb) * hkv + h) * bs + r) * kHeadDim;
-    reinterpret_cast<uint4 *>(dst)[q] = make_uint4(o[0], o[1], o[2], o[3]);
+    uint4 *dst = reinterpret_cast<uint4 *>((is_v ? p.v_stage : p.k_stage) +
+                                           (((static_cast<int64_t>(sb) * hkv + h) << bs_sh) + r) *
+                                               kHeadDim) +
+                 q * kOut;
+#pragma unroll
+    for (int k = 0; k < kOut; ++k)
+      dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
   }
 }
 
