@@ -64,6 +64,7 @@ CASES = {
     "small-fp8": (4, [0]),                    # one ~0.6-1M-token FP8 request
     "small-nvfp4": (4, [0, 1]),               # two such requests, NVFP4 KV
     "small-prefill-fp8": (2, [4, 5]),         # two post-tool-call sessions, E4M3 KV
+    "small-prefill-nvfp4": (2, [4, 5]),       # the same with NVFP4 KV
     "small-mixed": (3, [0, 40, 80, 119, 127]),   # 4 decodes + the 392-token chunk, ~2 GB
     # the whole post-tool-call step, for captures of its 26K-token KV append
     # (216 MB bf16, 162 MB E4M3, 138 MB NVFP4 per launch)
@@ -71,8 +72,8 @@ CASES = {
     "append-c3-fp8": (2, list(range(16))),
     "append-c3-nvfp4": (2, list(range(16))),
 }
-CASE_KV = {"small-nvfp4": "nvfp4", "small-prefill-fp8": "fp8", "append-c3-fp8": "fp8",
-           "append-c3-nvfp4": "nvfp4"}
+CASE_KV = {"small-nvfp4": "nvfp4", "small-prefill-fp8": "fp8", "small-prefill-nvfp4": "nvfp4",
+           "append-c3-fp8": "fp8", "append-c3-nvfp4": "nvfp4"}
 
 
 def case_spec(name: str) -> W.Spec:
