@@ -576,8 +576,12 @@ def secondary(args, world, peaks, device):
                                  kv_dtype="fp8")
     nv_pf = dataclasses.replace(W.config_spec(2), name="c3_nvfp4_post_tool_prefill",
                                 kv_dtype="nvfp4")
+    gpu_index = int(device.split(":")[1]) if ":" in device else 0
     for idx, steps in ((2, 10), (fp8_pf, 10), (nv_pf, 5), (3, 10), (4, 50), (nvfp4, 50)):
-        r = time_workload(idx, steps, 3, world, peaks, device)
+        # clocks sampled during each timed loop: the tensor-bound steps run
+        # at the power cap's clocks once the GPU is warm
+        smp = ClockSampler(gpu_index)
+        r = time_workload(idx, steps, 3, world, peaks, device, sampler=smp)
         spec, work = r["spec"], r["work"]
         unstaged = None
         if "stage" in r["kinds"]:
@@ -592,7 +596,8 @@ def secondary(args, world, peaks, device):
                                     "frac": round(tf / peaks["bf16_tflops"], 4)}}
         ms_step = r["ms"] / steps
         ent = {"workload": spec.name, "ms_per_step": round(ms_step, 4),
-               "kernel_ms": {k: round(v[1], 4) for k, v in r["kinds"].items()}}
+               "kernel_ms": {k: round(v[1], 4) for k, v in r["kinds"].items()},
+               "clocks": smp.summary(*r["wall"])}
         if "mixed" in r["kinds"]:
             # one launch for both kinds; the per-kind figures below come from
             # the same step run as separate decode and prefill launches
