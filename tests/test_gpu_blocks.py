@@ -27,16 +27,33 @@ def kv_rows(tokens, pos0, seed):
     return torch.from_numpy(out).to(torch.bfloat16)
 
 
-def test_pool_tables_feed_prefill_prefix_hits_and_decode():
+KV_DTYPES = {"bf16": pkv.KV_BF16, "fp8": pkv.KV_FP8_E4M3, "nvfp4": pkv.KV_NVFP4}
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "nvfp4"])
+def test_pool_tables_feed_prefill_prefix_hits_and_decode(kv):
+    """Quantised pools run their prefill steps through the staging pools
+    (each request stages the shared prefix blocks it reads)."""
     rng = np.random.default_rng(4)
     prefix = list(rng.integers(0, 1000, 100))
     reqs = {1: prefix + list(rng.integers(0, 1000, 37)),
             2: prefix + list(rng.integers(0, 1000, 21))}
     bp = pkv.Blocks(NB, BS)
-    kc = torch.full((NB, HKV, BS, D), float("nan"), dtype=torch.bfloat16, device=DEV)
-    vc = torch.full_like(kc, float("nan"))
-    cfg = pkv.make_config(HQ, HKV, BS, NB, 4, 256, softmax_scale=1 / math.sqrt(D),
-                          flags=pkv.FLAG_VALIDATE)
+    cfg = pkv.make_config(HQ, HKV, BS, NB, 4, 256, kv_dtype=KV_DTYPES[kv],
+                          softmax_scale=1 / math.sqrt(D), flags=pkv.FLAG_VALIDATE,
+                          stage_tokens=4 * 256)
+    shape, dtype, scale_shape = pkv.pool_shapes(cfg)
+    if kv == "bf16":
+        kc = torch.full(shape, float("nan"), dtype=dtype, device=DEV)
+        ks = vs = None
+    else:
+        # poison: NaN E4M3 codes / NVFP4 bytes whose micro scales are NaN
+        kc = torch.full(shape, 0x7F if kv == "fp8" else 0xFF, dtype=dtype, device=DEV)
+        # block scales of N(0, 1) rows, varying from block to block
+        g = torch.Generator().manual_seed(5)
+        ks = (0.006 + 0.01 * torch.rand(scale_shape, generator=g)).to(DEV)
+        vs = (0.006 + 0.01 * torch.rand(scale_shape, generator=g)).to(DEV)
+    vc = kc.clone()
     h = pkv.Handle(cfg)
     done = {}
 
@@ -65,12 +82,20 @@ def test_pool_tables_feed_prefill_prefix_hits_and_decode():
         q = torch.cat(qs).to(DEV)
         kn, vn = torch.cat(knew).to(DEV), torch.cat(vnew).to(DEV)
         sl = torch.from_numpy(np.concatenate(slots)).to(DEV)
-        kc0 = kc.view(torch.int16).cpu().numpy().view(np.uint16).copy()
-        vc0 = vc.view(torch.int16).cpu().numpy().view(np.uint16).copy()
-        h.write_slots(kn, vn, sl, kc, vc)
-        out, _ = h.attention_varlen(q, kc, vc, torch.from_numpy(qsl).to(DEV),
-                                    torch.from_numpy(lens).to(DEV), torch.from_numpy(bt).to(DEV),
-                                    qsl, lens)
+        if kv == "bf16":
+            kc0 = kc.view(torch.int16).cpu().numpy().view(np.uint16).copy()
+            vc0 = vc.view(torch.int16).cpu().numpy().view(np.uint16).copy()
+            ks0 = vs0 = None
+        else:
+            kc0, vc0 = kc.cpu().numpy().copy(), vc.cpu().numpy().copy()
+            ks0, vs0 = ks.cpu().numpy(), vs.cpu().numpy()
+        h.write_slots(kn, vn, sl, kc, vc, ks, vs)
+        out, lse = h.attention_varlen(q, kc, vc, torch.from_numpy(qsl).to(DEV),
+                                      torch.from_numpy(lens).to(DEV),
+                                      torch.from_numpy(bt).to(DEV), qsl, lens,
+                                      lse=torch.empty(q.shape[:2], dtype=torch.float32,
+                                                      device=DEV),
+                                      k_scale=ks, v_scale=vs)
         torch.cuda.synchronize()
         h.check_device_errors()
         for req, toks, _ in batch:
@@ -78,10 +103,12 @@ def test_pool_tables_feed_prefill_prefix_hits_and_decode():
             done[req] = len(toks)
         # oracle: its own append into the pool as it was, then attention
         oracle.write_slots(kc0, vc0, W.bf16_bits(kn), W.bf16_bits(vn),
-                           np.concatenate(slots))
-        ref, ref_lse = oracle.attention(kc0, vc0, W.bf16_bits(q), qsl, lens, bt, 1 / math.sqrt(D))
+                           np.concatenate(slots), ks0, vs0)
+        ref, ref_lse = oracle.attention(kc0, vc0, W.bf16_bits(q), qsl, lens, bt,
+                                        1 / math.sqrt(D), ks0, vs0)
         got = out.double().cpu().numpy().reshape(-1, D)
-        U.check(got, ref, None, None, "bf16", "pool-driven step", scaled=True)
+        got_lse = lse.double().cpu().numpy().reshape(-1)
+        U.check(got, ref, got_lse, ref_lse, kv, f"pool-driven step ({kv})", scaled=True)
         return tables
 
     t1 = step([(1, reqs[1], len(reqs[1]))])                  # prefill of request 1
