@@ -56,6 +56,37 @@ std::string fmt(const char *f, ...) {
   return buf;
 }
 
+// Planner: split-KV decode items and prefill tiles, longest first.
+struct Plan {
+  std::vector<pkv_work_item> dec, pre;
+  int partials = 0;
+  int dec_groups = 0;   // split decode pairs: their first ranges lead `dec`
+  int dec_max_split = 1;   // most ranges of one decode pair
+  int pre_groups = 0;   // split prefill items: their first ranges lead `pre`
+  // scratch of make_plan; a handle keeps its Plan from step to step, so
+  // these (and dec, pre) stop allocating once they have grown
+  std::vector<pkv_work_item> tmp;
+  std::vector<int64_t> unit_cost, unit_id, group_cost;
+  std::vector<uint64_t> keys;
+  std::vector<std::pair<int64_t, int32_t>> groups, tiles;
+};
+
+// Moves the items for which lead(item) holds to the front of v, both parts
+// in their order (a stable partition through the scratch vector tmp);
+// returns how many lead.
+template <class F>
+int lead_first(std::vector<pkv_work_item> &v, std::vector<pkv_work_item> &tmp, F lead) {
+  tmp.clear();
+  for (const auto &w : v)
+    if (lead(w)) tmp.push_back(w);
+  const int n = static_cast<int>(tmp.size());
+  if (n == 0) return 0;
+  for (const auto &w : v)
+    if (!lead(w)) tmp.push_back(w);
+  v.swap(tmp);
+  return n;
+}
+
 struct TimingRing {
   cudaEvent_t start[kTimingSlots];
   cudaEvent_t stop[kTimingSlots];
@@ -66,6 +97,7 @@ struct TimingRing {
 
 struct pkv_handle {
   pkv_config cfg{};
+  Plan plan;   // the last step's plan (its vectors keep their capacity)
   int device = 0;
   int num_sms = 0;
   std::string last_error;
@@ -146,14 +178,6 @@ std::string check_config(const pkv_config *c, pkv_status *st) {
   return "";
 }
 
-// Planner: split-KV decode items and prefill tiles, longest first.
-struct Plan {
-  std::vector<pkv_work_item> dec, pre;
-  int partials = 0;
-  int dec_groups = 0;   // split decode pairs: their first ranges lead `dec`
-  int dec_max_split = 1;   // most ranges of one decode pair
-  int pre_groups = 0;   // split prefill items: their first ranges lead `pre`
-};
 
 // Keys an item list walks for a sequence of L keys: all of them, or, for
 // context-parallel shard r of n with tokens dealt out in runs of k (run j
@@ -173,6 +197,10 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
   if (B < 0 || T < 0) return "num_seqs and num_tokens must be >= 0";
   if (B > 0 && (qsl == nullptr || lens == nullptr))
     return "query_start_loc_host and seq_lens_host are required";
+  plan->dec.clear();
+  plan->pre.clear();
+  plan->partials = plan->dec_groups = plan->pre_groups = 0;
+  plan->dec_max_split = 1;
   if (B == 0) {
     if (T != 0) return "num_tokens must be 0 when num_seqs is 0";
     *st = PKV_OK;
@@ -214,8 +242,6 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
     if (parts <= max_partials) break;
     chunk *= 2;
   }
-  plan->dec.clear();
-  plan->pre.clear();
   int part = 0;
   for (int i = 0; i < B; ++i) {
     const int q = qsl[i + 1] - qsl[i];
@@ -305,7 +331,8 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
       int64_t(plan->pre.size()) * 2 <= std::max(num_sms, 1)) {
     int64_t total_tiles = 0;
     for (const auto &w : plan->pre) total_tiles += (w.k_end + 127) / 128;
-    std::vector<pkv_work_item> split;
+    std::vector<pkv_work_item> &split = plan->tmp;
+    split.clear();
     for (const auto &w : plan->pre) {
       const int nt = (w.k_end + 127) / 128;
       const int unit = std::max(1, c.block_size / 128);    // boundary granularity, tiles
@@ -349,8 +376,11 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
   auto dec_cost = [](const pkv_work_item &w) { return int64_t(w.k_end) - w.k_begin; };
   {
     const size_t n = plan->dec.size();
-    std::vector<int64_t> unit_cost(n), unit_id(n);
-    std::vector<int64_t> group_max(size_t(B) * H, -1);
+    std::vector<int64_t> &unit_cost = plan->unit_cost, &unit_id = plan->unit_id;
+    std::vector<int64_t> &group_max = plan->group_cost;
+    unit_cost.resize(n);
+    unit_id.resize(n);
+    group_max.assign(size_t(B) * H, -1);
     auto chunked = [&](const pkv_work_item &w) {
       return int64_t(qsl[w.seq + 1] - qsl[w.seq]) * G > kDecCols;
     };
@@ -365,23 +395,55 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
       unit_cost[k] = ch ? group_max[size_t(w.seq) * H + w.kv_head] : dec_cost(w);
       unit_id[k] = ch ? int64_t(w.seq) * H + w.kv_head : int64_t(B) * H + int64_t(k);
     }
-    std::vector<size_t> order(n);
-    for (size_t k = 0; k < n; ++k) order[k] = k;
-    std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) {
-      if (unit_cost[a] != unit_cost[b]) return unit_cost[a] > unit_cost[b];
-      if (unit_id[a] != unit_id[b]) return unit_id[a] < unit_id[b];
-      return dec_cost(plan->dec[a]) > dec_cost(plan->dec[b]);
-    });
-    std::vector<pkv_work_item> sorted(n);
-    for (size_t k = 0; k < n; ++k) sorted[k] = plan->dec[order[k]];
+    std::vector<pkv_work_item> &sorted = plan->tmp;
+    sorted.resize(n);
+    bool any_chunked = false;
+    for (size_t k = 0; k < n && !any_chunked; ++k) any_chunked = unit_id[k] < int64_t(B) * H;
+    if (!any_chunked) {
+      // every item its own unit: cost descending, then item order.  All
+      // ranges but a request's last have the full split length, the largest
+      // cost: those lead in item order, and only the others are sorted (one
+      // 64-bit key each; costs and indices below 2^31)
+      int64_t top = 0;
+      for (size_t k = 0; k < n; ++k) top = std::max(top, unit_cost[k]);
+      std::vector<uint64_t> &keys = plan->keys;
+      keys.clear();
+      size_t m = 0;
+      for (size_t k = 0; k < n; ++k) {
+        if (unit_cost[k] == top)
+          sorted[m++] = plan->dec[k];
+        else
+          keys.push_back((uint64_t(0x7FFFFFFF - unit_cost[k]) << 32) | uint64_t(k));
+      }
+      std::sort(keys.begin(), keys.end());
+      for (const uint64_t key : keys) sorted[m++] = plan->dec[key & 0xFFFFFFFFu];
+    } else {
+      // unit cost descending, unit id ascending, own cost descending, then
+      // the original index: the order a stable sort on the first three gives
+      struct Key {
+        int64_t cost, unit;
+        int32_t own, idx;
+        bool operator<(const Key &o) const {
+          if (cost != o.cost) return cost > o.cost;
+          if (unit != o.unit) return unit < o.unit;
+          if (own != o.own) return own > o.own;
+          return idx < o.idx;
+        }
+      };
+      std::vector<Key> keys(n);
+      for (size_t k = 0; k < n; ++k)
+        keys[k] = Key{unit_cost[k], unit_id[k], static_cast<int32_t>(dec_cost(plan->dec[k])),
+                      static_cast<int32_t>(k)};
+      std::sort(keys.begin(), keys.end());
+      for (size_t k = 0; k < n; ++k) sorted[k] = plan->dec[keys[k].idx];
+    }
     plan->dec.swap(sorted);
     // the first range of each split pair leads the list (the merge kernel
     // takes its groups from there); these are full-length ranges, so the
     // longest-first order barely moves
-    const auto lead = std::stable_partition(
-        plan->dec.begin(), plan->dec.end(),
-        [](const pkv_work_item &w) { return w.part >= 0 && w.part == w.pair; });
-    plan->dec_groups = static_cast<int>(lead - plan->dec.begin());
+    plan->dec_groups = lead_first(plan->dec, plan->tmp, [](const pkv_work_item &w) {
+      return w.part >= 0 && w.part == w.pair;
+    });
     plan->dec_max_split = 1;
     for (const auto &w : plan->dec) plan->dec_max_split = std::max(plan->dec_max_split, int(w.n_split));
   }
@@ -391,23 +453,47 @@ std::string make_plan(const pkv_config &c, const int32_t *qsl, const int32_t *le
   auto pre_cost = [](const pkv_work_item &w) {
     return (int64_t(w.k_end) - w.k_begin) * w.n_rows;
   };
-  std::vector<int64_t> group_cost(size_t(B) * H, 0);
+  std::vector<int64_t> &group_cost = plan->group_cost;
+  group_cost.assign(size_t(B) * H, 0);
   for (const auto &w : plan->pre) group_cost[size_t(w.seq) * H + w.kv_head] += pre_cost(w);
-  std::stable_sort(plan->pre.begin(), plan->pre.end(),
-                   [&](const pkv_work_item &a, const pkv_work_item &b) {
-                     const int64_t ga = group_cost[size_t(a.seq) * H + a.kv_head];
-                     const int64_t gb = group_cost[size_t(b.seq) * H + b.kv_head];
-                     if (ga != gb) return ga > gb;
-                     if (a.seq != b.seq) return a.seq < b.seq;
-                     if (a.kv_head != b.kv_head) return a.kv_head < b.kv_head;
-                     return pre_cost(a) > pre_cost(b);
-                   });
+  {
+    // The tiles of one (request, KV head) are adjacent in plan->pre (built
+    // per request and KV head; a split keeps its ranges in place): order the
+    // groups by cost descending, then (request, KV head), and the tiles of a
+    // group by cost descending, then their original order.
+    const size_t n = plan->pre.size();
+    std::vector<std::pair<int64_t, int32_t>> &groups = plan->groups;   // (cost, first tile)
+    groups.clear();
+    for (size_t k = 0; k < n; ++k) {
+      const pkv_work_item &w = plan->pre[k];
+      if (k == 0 || w.seq != plan->pre[k - 1].seq || w.kv_head != plan->pre[k - 1].kv_head)
+        groups.emplace_back(group_cost[size_t(w.seq) * H + w.kv_head], static_cast<int32_t>(k));
+    }
+    // cost descending, first tile ascending (the groups' original order)
+    std::sort(groups.begin(), groups.end(),
+              [](const std::pair<int64_t, int32_t> &a, const std::pair<int64_t, int32_t> &b) {
+                return a.first != b.first ? a.first > b.first : a.second < b.second;
+              });
+    std::vector<pkv_work_item> &sorted = plan->tmp;
+    sorted.clear();
+    std::vector<std::pair<int64_t, int32_t>> &tiles = plan->tiles;   // (-cost, index)
+    for (const auto &gr : groups) {
+      size_t e = size_t(gr.second) + 1;
+      const pkv_work_item &w0 = plan->pre[size_t(gr.second)];
+      while (e < n && plan->pre[e].seq == w0.seq && plan->pre[e].kv_head == w0.kv_head) ++e;
+      tiles.clear();
+      for (size_t k = size_t(gr.second); k < e; ++k)
+        tiles.emplace_back(-pre_cost(plan->pre[k]), static_cast<int32_t>(k));
+      std::sort(tiles.begin(), tiles.end());
+      for (const auto &tl : tiles) sorted.push_back(plan->pre[size_t(tl.second)]);
+    }
+    plan->pre.swap(sorted);
+  }
   // the first range of each split item leads the list: the merge kernel
   // takes its groups from there
-  const auto lead = std::stable_partition(
-      plan->pre.begin(), plan->pre.end(),
-      [](const pkv_work_item &w) { return w.part >= 0 && w.part == w.pair; });
-  plan->pre_groups = static_cast<int>(lead - plan->pre.begin());
+  plan->pre_groups = lead_first(plan->pre, plan->tmp, [](const pkv_work_item &w) {
+    return w.part >= 0 && w.part == w.pair;
+  });
   *st = PKV_OK;
   return "";
 }
@@ -771,7 +857,7 @@ pkv_status attention_step(pkv_handle *h, const void *q, const void *k_cache,
     return fail(h, PKV_ERR_INVALID_ARG, fmt("num_seqs %d exceeds max_num_seqs %d", num_seqs, c.max_num_seqs));
   if (num_tokens > c.max_num_tokens)
     return fail(h, PKV_ERR_INVALID_ARG, fmt("num_tokens %d exceeds max_num_tokens %d", num_tokens, c.max_num_tokens));
-  Plan plan;
+  Plan &plan = h->plan;
   pkv_status st;
   std::string msg = make_plan(c, qsl_host, lens_host, num_seqs, num_tokens, h->num_sms,
                               kMaxPartials, &plan, &st, dcp);
@@ -1147,7 +1233,7 @@ pkv_status pkv_graph_prepare(pkv_handle *h, const int32_t *qsl_host,
   const pkv_config &c = h->cfg;
   if (num_seqs > c.max_num_seqs || num_tokens > c.max_num_tokens)
     return fail(h, PKV_ERR_INVALID_ARG, "step larger than the handle serves");
-  Plan plan;
+  Plan &plan = h->plan;
   pkv_status st;
   std::string msg = make_plan(c, qsl_host, lens_host, num_seqs, num_tokens, h->num_sms,
                               kMaxPartials, &plan, &st);
@@ -1223,7 +1309,7 @@ pkv_status pkv_plan(const pkv_config *config, const int32_t *qsl_host,
     g_create_error = msg;
     return st;
   }
-  Plan plan;
+  static thread_local Plan plan;   // scratch reused by this thread's calls
   msg = make_plan(*config, qsl_host, lens_host, num_seqs, num_tokens, num_sms,
                   kMaxPartials, &plan, &st);
   if (st != PKV_OK) {
